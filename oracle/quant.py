@@ -1,0 +1,115 @@
+"""Weight-only quantisation (W8A16 per-row, W4A16 group-128) and dequantisation.
+
+The AutoMegaKernel explainer ("Key contributions": int8 weight-only kernels
+that are greedy-lossless, int4 kernels that cut weight traffic 2.42x and are
+lossy) fixes only "symmetric, per output channel, fp16 scale = max|w|/127"
+for int8 and "symmetric group-128, fp16 scales" for int4.  Readings taken for
+what is left open:
+
+* int8: s = fp16(fp32(max_k |w_rk|) / 127) with both roundings to nearest
+  even; q = clamp(round_half_even(fp32(w) / fp32(s)), -127, 127); s == 0 gives
+  q == 0.
+* int4: groups of 128 consecutive k per row; s = fp16(fp32(max|w|) / 7);
+  q = clamp(round_half_even(w / s), -7, 7); stored as two's-complement
+  nibbles, the even k in the low nibble.
+* Dequantisation is w' = fp32(q) * fp32(s), which is exact in float32
+  (at most 4 + 11 significant bits), so it is checked bit for bit.
+"""
+import numpy as np
+
+
+def _fp16_of_fp32(x):
+    return np.asarray(x, np.float32).astype(np.float16)
+
+
+def _round_half_even_div(w32, s32):
+    """round_half_even(fp32(w / s)) with an fp32 division."""
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = (w32 / s32).astype(np.float32)
+    return np.rint(r)          # numpy rint rounds half to even
+
+
+def quantize_int8_rows(w):
+    """w: float32 [N, K] (bf16-exact values).  Returns (q int8 [N,K], s float16 [N])."""
+    w = np.asarray(w, np.float32)
+    amax = np.max(np.abs(w), axis=1)
+    s16 = _fp16_of_fp32(amax / np.float32(127.0))
+    s32 = s16.astype(np.float32)[:, None]
+    q = np.zeros(w.shape, np.int8)
+    nz = s32[:, 0] != 0
+    r = _round_half_even_div(w[nz], s32[nz])
+    q[nz] = np.clip(r, -127, 127).astype(np.int8)
+    return q, s16
+
+
+def quantize_int4_g128(w, group=128):
+    """w: float32 [N, K], K % 128 == 0.  Returns (q int8 [N,K] in [-7,7], s float16 [N, K/128])."""
+    w = np.asarray(w, np.float32)
+    n, k = w.shape
+    assert k % group == 0
+    g = w.reshape(n, k // group, group)
+    amax = np.max(np.abs(g), axis=2)
+    s16 = _fp16_of_fp32(amax / np.float32(7.0))
+    s32 = s16.astype(np.float32)[:, :, None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = _round_half_even_div(g, s32)
+    r = np.where(s32 == 0, 0.0, r)
+    q = np.clip(r, -7, 7).astype(np.int8).reshape(n, k)
+    return q, s16
+
+
+def pack_int4_nibbles(q):
+    """q int8 [N, K] in [-8, 7] -> uint8 [N, K/2]; even k in the low nibble."""
+    u = (np.asarray(q).astype(np.int16) & 0xF).astype(np.uint8)
+    return (u[:, 0::2] | (u[:, 1::2] << 4)).astype(np.uint8)
+
+
+def unpack_int4_nibbles(b):
+    """Inverse of pack_int4_nibbles (sign-extends each nibble)."""
+    b = np.asarray(b, np.uint8)
+    lo = (b & 0xF).astype(np.int8)
+    hi = (b >> 4).astype(np.int8)
+    lo = np.where(lo >= 8, lo - 16, lo).astype(np.int8)
+    hi = np.where(hi >= 8, hi - 16, hi).astype(np.int8)
+    out = np.empty((b.shape[0], b.shape[1] * 2), np.int8)
+    out[:, 0::2] = lo
+    out[:, 1::2] = hi
+    return out
+
+
+def dequant_int8(q, s16):
+    """w' = fp32(q) * fp32(s), float32 [N, K]."""
+    return (np.asarray(q).astype(np.float32) * s16.astype(np.float32)[:, None]).astype(np.float32)
+
+
+def dequant_int4(q, s16, group=128):
+    n, k = q.shape
+    s = np.repeat(s16.astype(np.float32), group, axis=1)
+    return (np.asarray(q).astype(np.float32) * s).astype(np.float32)
+
+
+GEMV_TENSORS = ("wq", "wk", "wv", "wo", "wgate", "wup", "wdown")
+
+
+def quantised_model_weights(shape, weights, wdtype, base_dtype="bf16"):
+    """Dequantised float64 copies of every GEMV weight (LM head included).
+
+    The embedding and the norm gains stay in their storage type.  Returns a
+    dict usable as ``llama.Model(..., dequantised=...)`` plus the raw
+    quantised (q, s) pairs for byte comparisons."""
+    from .llama import bf16_bits_to_f64, fp16_bits_to_f64
+    widen = bf16_bits_to_f64 if base_dtype == "bf16" else fp16_bits_to_f64
+    names = [f"l{i}.{t}" for i in range(shape.n_layers) for t in GEMV_TENSORS] + ["lm_head"]
+    deq, raw = {}, {}
+    for nm in names:
+        w32 = widen(weights[nm]).astype(np.float32)
+        if wdtype == "int8":
+            q, s = quantize_int8_rows(w32)
+            deq[nm] = dequant_int8(q, s).astype(np.float64)
+        elif wdtype == "int4":
+            q, s = quantize_int4_g128(w32)
+            deq[nm] = dequant_int4(q, s).astype(np.float64)
+        else:
+            raise ValueError(wdtype)
+        raw[nm] = (q, s)
+    return deq, raw
