@@ -1,0 +1,58 @@
+// Host-side internal API shared by the library's C++ translation units.
+#pragma once
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "mk_internal.h"
+
+namespace mk {
+
+void set_error(const char* fmt, ...);
+const char* thread_error();
+
+uint16_t f32_to_f16_rne(float f);
+float f16_to_f32(uint16_t h);
+float base_to_f32(uint16_t v, int base);
+
+mk_status check_desc(const mk_model_desc* d);
+int64_t row_stride(int64_t K, int wdtype);
+BlobLayout blob_layout(const mk_model_desc* d);
+
+// Resolved schedule knobs.
+struct Config {
+    int sms, slot_bytes, n_slots, C;
+    int64_t watchdog_ns;
+};
+mk_status resolve_config(const mk_model_desc* d, const mk_schedule_config* cfg, int n_sms,
+                         Config* out);
+
+// IR buffers of the decode path.
+enum Buf : int32_t { B_X = 0, B_QKV, B_PART, B_H, B_LOGITS, B_KEY, B_OUT, B_KV, B_COUNT };
+
+// Result of lowering: the IR (owning storage) and the matching device tables.
+struct Lowering {
+    std::vector<mk_ir_task> tasks;
+    std::vector<mk_ir_access> acc;
+    std::vector<std::vector<int32_t>> queues;
+    std::vector<DevTask> dev;
+    int32_t n_counters = 0;
+    int64_t bytes_per_sm_max = 0, bytes_per_sm_min = 0;
+};
+mk_status lower(const mk_model_desc* d, const Config& c, Lowering* out);
+
+// Flatten a lowering into a library-owned mk_ir.
+mk_ir* to_ir(const Lowering& lw, int n_sms);
+
+// The validator on a flat IR.
+mk_status validate_ir(const mk_ir* ir, std::string* why);
+
+// Workspace layout (byte offsets).
+struct WsLayout {
+    int64_t status, counters, key, tasks, queue, queue_off, inv_freq, x, qkv, part_ml, part_acc,
+        h, tok, out_ids, total;
+};
+WsLayout ws_layout(const mk_model_desc* d, const Config& c, int64_t n_tasks, int32_t n_counters);
+
+}  // namespace mk

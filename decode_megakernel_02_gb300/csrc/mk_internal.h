@@ -1,0 +1,105 @@
+// Internal definitions shared by the host lowering (C++) and the persistent
+// decode kernel (CUDA).  Not part of the public ABI.
+#pragma once
+#include <stdint.h>
+
+#include "mk.h"
+
+namespace mk {
+
+// Instructions of the VM (AutoMegaKernel explainer, "Methodology", Layer 1:
+// GEMV, attention, RMSNorm ... micro-kernels behind one task ABI).
+enum Op : int32_t {
+    OP_QKV = 1,   // RMSNorm prologue + [Wq;Wk;Wv] GEMV rows -> qkv (fp32)
+    OP_ATTN = 2,  // RoPE + KV append + split-KV GQA attention chunk -> partials
+    OP_O = 3,     // merge partials + Wo GEMV rows + residual add -> x
+    OP_GU = 4,    // RMSNorm prologue + interleaved gate/up rows + SwiGLU -> h
+    OP_DOWN = 5,  // Wdown GEMV rows + residual add -> x
+    OP_LM = 6,    // final RMSNorm + LM-head rows + block argmax -> logits, key
+    OP_FIN = 7    // read the step's argmax key -> out id
+};
+
+constexpr int NT = 256;                 // consumer threads per CTA
+constexpr int NW = NT / 32;             // consumer warps
+constexpr int THREADS = NT + 32;        // + one producer (weight streaming) warp
+constexpr int MAX_RPS = 32;             // rows per ring slot
+constexpr int MAXG = 8;                 // 8-element k groups per thread: K <= 8*NT*MAXG
+constexpr int MAX_K = 8 * NT * MAXG;    // 16384
+constexpr int MAX_REP = 8;              // query heads per KV head
+constexpr int ATTN_TILE = 64;           // positions per online-softmax tile
+constexpr int CTR_STRIDE = 32;          // u32 words between counters (128 B lines)
+
+// k-groups per thread that a slot of RP rows (RP a power of two) may need; a
+// ring slot holds at most ~32 KiB, so many rows come with short rows.  The
+// lowering keeps every task within this bound.
+#ifdef __CUDACC__
+__host__ __device__
+#endif
+constexpr int maxg_for(int rp) { return rp >= 16 ? 2 : rp == 8 ? 4 : MAXG; }
+
+// One entry of the device task table (one IR task).
+struct DevTask {
+    int32_t op, layer;
+    int32_t row0, nrows;    // GEMV: first row / row count.  ATTN: kv head / chunk
+    int32_t K;              // GEMV: reduction length.  ATTN: chunks per head
+    int32_t row_bytes;      // GEMV: packed row stride
+    int32_t rps;            // GEMV: rows per ring slot
+    int32_t rp_log2;        // GEMV: log2 of the power of two >= rps
+    int64_t w_off;          // GEMV: blob offset of row0
+    int32_t n_waits;
+    int32_t wait_ctr[2];
+    int32_t wait_cnt[2];
+    int32_t wait_off[2];
+    int32_t signal_ctr;
+    int32_t pad[1];
+};
+static_assert(sizeof(DevTask) == 80, "DevTask layout");
+
+// Byte offsets of the packed weight blob.
+struct BlobLayout {
+    int64_t row_qkv, row_o, row_gu, row_down, row_lm;   // row strides
+    int64_t norm_bytes;                                 // bytes per norm-gain vector (padded)
+    int64_t layer_bytes;                                // one layer block
+    int64_t l_attn_norm, l_ffn_norm, l_qkv, l_o, l_gu, l_down;   // inside a layer block
+    int64_t final_norm, lm, embed, total;
+};
+
+// Kernel parameters (passed by value).
+struct VmParams {
+    const uint8_t* w;          // packed blob
+    uint16_t* kv;              // bf16 KV cache [L][2][Hkv][max_seq][hd]
+    uint32_t* status;          // [0] status, [1] task id, [2] detail, [3] last token
+    uint32_t* counters;        // n_counters lines of CTR_STRIDE words
+    unsigned long long* key;   // the step's packed argmax key
+    const DevTask* tasks;
+    const int32_t* queue;
+    const int32_t* queue_off;  // [n_sms + 1]
+    const float* inv_freq;     // [hd/2]
+    float* x;                  // residual stream [d]
+    float* qkv;                // [q_dim + 2 kv_dim]
+    float* part_ml;            // [Hq][C][2]  (running max, sum)
+    float* part_acc;           // [Hq][C][hd]
+    float* h;                  // SwiGLU output [F]
+    const int32_t* forced;     // nullable: token fed at step s
+    int32_t* out_ids;          // nullable: argmax of step s
+    float* logits;             // nullable: [n_steps][V]
+    // model
+    int32_t L, d, Hq, Hkv, hd, F, V, max_seq, wdtype, base_dtype, q_dim, kv_dim, C;
+    float eps;
+    int64_t layer_bytes, l_attn_norm, l_ffn_norm, final_norm, embed;
+    // run
+    int32_t n_steps, pos0, epoch0, skip_lm;
+    int32_t pending;           // token fed at step 0 (no forcing); -1: status[3]
+    int32_t n_slots, slot_bytes;
+    int64_t watchdog_ns;
+};
+
+// Status codes written by the device into status[0].
+enum : uint32_t { DEV_OK = 0, DEV_TIMEOUT = 1, DEV_BAD_KEY = 2, DEV_BAD_TOKEN = 3 };
+
+// Argmax key: [tag:15][orderable fp32:32][0x1FFFF - index:17].  A larger tag
+// (step) always wins, so the word needs no reset between steps.
+constexpr int KEY_IDX_BITS = 17;
+constexpr int KEY_TAG_MAX = 32767;
+
+}  // namespace mk

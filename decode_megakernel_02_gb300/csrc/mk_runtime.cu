@@ -1,0 +1,451 @@
+// Runtime half of the C ABI: contract + schedule checks at create, then one
+// cooperative launch per prefill/decode call on the caller's stream.
+//
+// Netra Kernel summary (section details): the runtime binds persistent and
+// boundary buffers and replays a fixed launch on a caller-owned stream; the
+// AutoMegaKernel explainer ("Methodology", safety gate): a schedule that fails
+// validation is rejected before any GPU launch.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "mk_host.h"
+
+namespace mk {
+const void* vm_kernel_for(int wdtype, int base);
+size_t vm_shared_bytes(int n_slots, int slot_bytes);
+cudaError_t launch_dequant(int wdtype, const uint8_t* rows, int64_t stride, int first, int step, int nrows,
+                           int K, float* out, cudaStream_t st);
+cudaError_t launch_watchdog(uint32_t* ctr, uint32_t* status, int64_t limit_ns, cudaStream_t st);
+}  // namespace mk
+
+using namespace mk;
+
+struct mk_handle {
+    mk_model_desc d;
+    Config c;
+    WsLayout ws;
+    BlobLayout bl;
+    int32_t n_tasks = 0, n_counters = 0;
+    const uint8_t* w = nullptr;
+    uint16_t* kv = nullptr;
+    uint8_t* wsp = nullptr;
+    cudaStream_t st = nullptr;
+    int device = 0;
+    const void* kfn = nullptr;
+    size_t smem = 0;
+    int32_t pos = 0, pending = -1;
+    bool has_seq = false;
+    uint32_t epoch = 0;
+    bool dirty = false;
+    int64_t launches = 0;
+    std::string err;
+};
+
+namespace {
+
+mk_status herr(mk_handle* h, mk_status st, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    if (h) h->err = buf;
+    set_error("%s", buf);
+    return st;
+}
+
+mk_status cuda_fail(mk_handle* h, cudaError_t e, const char* what) {
+    return herr(h, MK_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define CK(h, call)                                   \
+    do {                                              \
+        cudaError_t e_ = (call);                      \
+        if (e_ != cudaSuccess) return cuda_fail(h, e_, #call); \
+    } while (0)
+
+mk_status reset_sync_state(mk_handle* h) {
+    CK(h, cudaMemsetAsync(h->wsp + h->ws.status, 0, 16, h->st));
+    CK(h, cudaMemsetAsync(h->wsp + h->ws.counters, 0, (size_t)h->n_counters * CTR_STRIDE * 4, h->st));
+    CK(h, cudaMemsetAsync(h->wsp + h->ws.key, 0, 8, h->st));
+    h->epoch = 0;
+    h->dirty = false;
+    return MK_OK;
+}
+
+mk_status launch(mk_handle* h, int n_steps, const int32_t* forced, int32_t* out_ids, float* logits,
+                 int skip_lm) {
+    if (h->dirty || h->epoch + (uint32_t)n_steps >= (uint32_t)KEY_TAG_MAX - 1u) {
+        mk_status st = reset_sync_state(h);
+        if (st) return st;
+    }
+    VmParams p{};
+    p.w = h->w;
+    p.kv = h->kv;
+    p.status = (uint32_t*)(h->wsp + h->ws.status);
+    p.counters = (uint32_t*)(h->wsp + h->ws.counters);
+    p.key = (unsigned long long*)(h->wsp + h->ws.key);
+    p.tasks = (const DevTask*)(h->wsp + h->ws.tasks);
+    p.queue = (const int32_t*)(h->wsp + h->ws.queue);
+    p.queue_off = (const int32_t*)(h->wsp + h->ws.queue_off);
+    p.inv_freq = (const float*)(h->wsp + h->ws.inv_freq);
+    p.x = (float*)(h->wsp + h->ws.x);
+    p.qkv = (float*)(h->wsp + h->ws.qkv);
+    p.part_ml = (float*)(h->wsp + h->ws.part_ml);
+    p.part_acc = (float*)(h->wsp + h->ws.part_acc);
+    p.h = (float*)(h->wsp + h->ws.h);
+    p.forced = forced;
+    p.out_ids = out_ids;
+    p.logits = logits;
+    const mk_model_desc& d = h->d;
+    p.L = d.n_layers;
+    p.d = d.d_model;
+    p.Hq = d.n_q_heads;
+    p.Hkv = d.n_kv_heads;
+    p.hd = d.head_dim;
+    p.F = d.d_ffn;
+    p.V = d.vocab;
+    p.max_seq = d.max_seq;
+    p.wdtype = d.wdtype;
+    p.base_dtype = d.base_dtype;
+    p.q_dim = d.n_q_heads * d.head_dim;
+    p.kv_dim = d.n_kv_heads * d.head_dim;
+    p.C = h->c.C;
+    p.eps = d.rms_eps;
+    p.layer_bytes = h->bl.layer_bytes;
+    p.l_attn_norm = h->bl.l_attn_norm;
+    p.l_ffn_norm = h->bl.l_ffn_norm;
+    p.final_norm = h->bl.final_norm;
+    p.embed = h->bl.embed;
+    p.n_steps = n_steps;
+    p.pos0 = h->pos;
+    p.epoch0 = (int32_t)h->epoch;
+    p.skip_lm = skip_lm;
+    p.pending = h->pending;
+    p.n_slots = h->c.n_slots;
+    p.slot_bytes = h->c.slot_bytes;
+    p.watchdog_ns = h->c.watchdog_ns;
+    void* args[] = {&p};
+    CK(h, cudaLaunchCooperativeKernel(h->kfn, dim3(h->c.sms), dim3(THREADS), args, h->smem, h->st));
+    h->epoch += (uint32_t)n_steps;
+    h->launches++;
+    return MK_OK;
+}
+
+mk_status read_status(mk_handle* h) {
+    uint32_t s[4] = {0, 0, 0, 0};
+    CK(h, cudaMemcpyAsync(s, h->wsp + h->ws.status, sizeof s, cudaMemcpyDeviceToHost, h->st));
+    CK(h, cudaStreamSynchronize(h->st));
+    if (s[0] == DEV_OK) return MK_OK;
+    h->dirty = true;
+    if (s[0] == DEV_TIMEOUT)
+        return herr(h, MK_ERR_TIMEOUT, "device wait gave up (task %u, detail %u); counters are reset on the next launch",
+                    s[1], s[2]);
+    return herr(h, MK_ERR_DEVICE, "device reported error %u (task 0x%x, step %u)", s[0], s[1], s[2]);
+}
+
+}  // namespace
+
+extern "C" {
+
+mk_status mk_workspace_size(const mk_model_desc* desc, const mk_schedule_config* cfg, int32_t n_sms,
+                            size_t* bytes) {
+    mk_status st = check_desc(desc);
+    if (st) return st;
+    if (!bytes) {
+        set_error("bytes is NULL");
+        return MK_ERR_INVALID_ARG;
+    }
+    if (n_sms <= 0) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) {
+            set_error("no CUDA device to take the SM count from: %s", cudaGetErrorString(e));
+            return MK_ERR_CUDA;
+        }
+    }
+    Config c;
+    if ((st = resolve_config(desc, cfg, n_sms, &c))) return st;
+    Lowering lw;
+    if ((st = lower(desc, c, &lw))) return st;
+    *bytes = (size_t)ws_layout(desc, c, (int64_t)lw.tasks.size(), lw.n_counters).total;
+    return MK_OK;
+}
+
+mk_status mk_create(const mk_model_desc* desc, const mk_schedule_config* cfg, const void* weights_dev,
+                    size_t weights_bytes, void* kv_dev, size_t kv_bytes, void* workspace_dev,
+                    size_t workspace_bytes, mk_stream_t stream, mk_handle** out) {
+    mk_status st = check_desc(desc);
+    if (st) return st;
+    if (!out || !weights_dev || !kv_dev || !workspace_dev) {
+        set_error("NULL argument");
+        return MK_ERR_INVALID_ARG;
+    }
+    *out = nullptr;
+    if (((uintptr_t)weights_dev & 255) || ((uintptr_t)workspace_dev & 255) || ((uintptr_t)kv_dev & 15)) {
+        set_error("misaligned buffer: weights and workspace need 256-byte, the KV cache 16-byte alignment");
+        return MK_ERR_INVALID_ARG;
+    }
+    int dev = 0, n_sms = 0, smem_optin = 0, coop = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+    if (e != cudaSuccess) {
+        set_error("CUDA device query failed: %s", cudaGetErrorString(e));
+        return MK_ERR_CUDA;
+    }
+    if (!coop) {
+        set_error("device %d does not support cooperative launches", dev);
+        return MK_ERR_UNSUPPORTED;
+    }
+    Config c;
+    if ((st = resolve_config(desc, cfg, n_sms, &c))) return st;
+    const size_t fixed = vm_shared_bytes(0, c.slot_bytes);
+    int max_slots = (int)(((size_t)smem_optin - fixed) / (size_t)c.slot_bytes);
+    if (max_slots > 16) max_slots = 16;
+    if (c.n_slots == 0) c.n_slots = max_slots;
+    if (c.n_slots < 2 || c.n_slots > max_slots) {
+        set_error("ring of %d slots of %d bytes does not fit %d bytes of shared memory (2..%d slots)", c.n_slots,
+                  c.slot_bytes, smem_optin, max_slots);
+        return MK_ERR_INVALID_ARG;
+    }
+    Lowering lw;
+    if ((st = lower(desc, c, &lw))) return st;
+    {
+        mk_ir* ir = to_ir(lw, c.sms);
+        std::string why;
+        st = validate_ir(ir, &why);
+        mk_free_ir(ir);
+        if (st) {
+            set_error("schedule rejected before launch: %s", why.c_str());
+            return MK_ERR_SCHEDULE_INVALID;
+        }
+    }
+    size_t need_w = 0, need_kv = 0;
+    mk_packed_size(desc, &need_w);
+    mk_kv_cache_size(desc, &need_kv);
+    WsLayout ws = ws_layout(desc, c, (int64_t)lw.tasks.size(), lw.n_counters);
+    if (weights_bytes < need_w || kv_bytes < need_kv || workspace_bytes < (size_t)ws.total) {
+        set_error("buffer too small: weights %zu/%zu, kv %zu/%zu, workspace %zu/%lld", weights_bytes, need_w,
+                  kv_bytes, need_kv, workspace_bytes, (long long)ws.total);
+        return MK_ERR_CAPACITY;
+    }
+    mk_handle* h = new mk_handle();
+    h->d = *desc;
+    h->c = c;
+    h->ws = ws;
+    h->bl = blob_layout(desc);
+    h->n_tasks = (int32_t)lw.tasks.size();
+    h->n_counters = lw.n_counters;
+    h->w = (const uint8_t*)weights_dev;
+    h->kv = (uint16_t*)kv_dev;
+    h->wsp = (uint8_t*)workspace_dev;
+    h->st = (cudaStream_t)stream;
+    h->device = dev;
+    h->kfn = vm_kernel_for(desc->wdtype, desc->base_dtype);
+    h->smem = vm_shared_bytes(c.n_slots, c.slot_bytes);
+    if (!h->kfn) {
+        delete h;
+        set_error("no kernel for wdtype %d / base %d", desc->wdtype, desc->base_dtype);
+        return MK_ERR_UNSUPPORTED;
+    }
+    auto fail = [&](mk_status s) {
+        set_error("%s", h->err.c_str());
+        delete h;
+        return s;
+    };
+    e = cudaFuncSetAttribute(h->kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->smem);
+    if (e != cudaSuccess) return fail(cuda_fail(h, e, "cudaFuncSetAttribute"));
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, h->kfn, THREADS, h->smem);
+    if (e != cudaSuccess) return fail(cuda_fail(h, e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor"));
+    if (per_sm < 1 || (int64_t)per_sm * n_sms < c.sms)
+        return fail(herr(h, MK_ERR_UNSUPPORTED, "%d CTAs cannot be co-resident (%d per SM)", c.sms, per_sm));
+
+    // device tables: tasks, queues, RoPE inverse frequencies
+    std::vector<int32_t> queue, qoff(c.sms + 1);
+    for (int s = 0; s < c.sms; ++s) {
+        qoff[s] = (int32_t)queue.size();
+        for (int id : lw.queues[s]) queue.push_back(id);
+    }
+    qoff[c.sms] = (int32_t)queue.size();
+    std::vector<float> inv(desc->head_dim / 2);
+    for (int i = 0; i < desc->head_dim / 2; ++i)
+        inv[i] = (float)std::pow((double)desc->rope_theta, -2.0 * i / (double)desc->head_dim);
+    e = cudaMemcpyAsync(h->wsp + ws.tasks, lw.dev.data(), lw.dev.size() * sizeof(DevTask), cudaMemcpyHostToDevice, h->st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(h->wsp + ws.queue, queue.data(), queue.size() * 4, cudaMemcpyHostToDevice, h->st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(h->wsp + ws.queue_off, qoff.data(), qoff.size() * 4, cudaMemcpyHostToDevice, h->st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(h->wsp + ws.inv_freq, inv.data(), inv.size() * 4, cudaMemcpyHostToDevice, h->st);
+    if (e != cudaSuccess) return fail(cuda_fail(h, e, "uploading the schedule"));
+    if ((st = reset_sync_state(h))) return fail(st);
+    e = cudaStreamSynchronize(h->st);
+    if (e != cudaSuccess) return fail(cuda_fail(h, e, "cudaStreamSynchronize"));
+    *out = h;
+    return MK_OK;
+}
+
+mk_status mk_prefill(mk_handle* h, const int32_t* tokens_host, int32_t n) {
+    if (!h || !tokens_host) {
+        set_error("NULL argument");
+        return MK_ERR_INVALID_ARG;
+    }
+    if (n < 1) return herr(h, MK_ERR_INVALID_ARG, "prefill needs at least one token");
+    if (n > h->d.max_seq) return herr(h, MK_ERR_CAPACITY, "prompt of %d tokens > max_seq %d", n, h->d.max_seq);
+    for (int i = 0; i < n; ++i)
+        if (tokens_host[i] < 0 || tokens_host[i] >= h->d.vocab)
+            return herr(h, MK_ERR_INVALID_ARG, "token %d at %d out of range", tokens_host[i], i);
+    h->pos = 0;
+    h->has_seq = false;
+    if (n > 1) {
+        CK(h, cudaMemcpyAsync(h->wsp + h->ws.tok, tokens_host, (size_t)(n - 1) * 4, cudaMemcpyHostToDevice, h->st));
+        mk_status st = launch(h, n - 1, (const int32_t*)(h->wsp + h->ws.tok), nullptr, nullptr, 1);
+        if (st) return st;
+        if ((st = read_status(h))) return st;
+    }
+    h->pos = n - 1;
+    h->pending = tokens_host[n - 1];
+    h->has_seq = true;
+    return MK_OK;
+}
+
+static mk_status check_decode(mk_handle* h, int32_t n_steps) {
+    if (!h) {
+        set_error("NULL handle");
+        return MK_ERR_INVALID_ARG;
+    }
+    if (!h->has_seq) return herr(h, MK_ERR_INVALID_ARG, "no sequence: call mk_prefill first");
+    if (n_steps < 1 || n_steps >= KEY_TAG_MAX - 1) return herr(h, MK_ERR_INVALID_ARG, "n_steps %d out of range", n_steps);
+    if ((int64_t)h->pos + n_steps > h->d.max_seq)
+        return herr(h, MK_ERR_CAPACITY, "pos %d + %d steps > max_seq %d", h->pos, n_steps, h->d.max_seq);
+    return MK_OK;
+}
+
+mk_status mk_decode(mk_handle* h, int32_t n_steps, int32_t* out_ids_host) {
+    mk_status st = check_decode(h, n_steps);
+    if (st) return st;
+    if (!out_ids_host) return herr(h, MK_ERR_INVALID_ARG, "out_ids_host is NULL");
+    int32_t* ids_dev = (int32_t*)(h->wsp + h->ws.out_ids);
+    if ((st = launch(h, n_steps, nullptr, ids_dev, nullptr, 0))) return st;
+    CK(h, cudaMemcpyAsync(out_ids_host, ids_dev, (size_t)n_steps * 4, cudaMemcpyDeviceToHost, h->st));
+    if ((st = read_status(h))) return st;
+    h->pos += n_steps;
+    h->pending = out_ids_host[n_steps - 1];
+    return MK_OK;
+}
+
+mk_status mk_decode_async(mk_handle* h, int32_t n_steps, const int32_t* forced_dev, int32_t* out_ids_dev,
+                          float* logits_dev) {
+    mk_status st = check_decode(h, n_steps);
+    if (st) return st;
+    if ((st = launch(h, n_steps, forced_dev, out_ids_dev, logits_dev, 0))) return st;
+    h->pos += n_steps;
+    h->pending = -1;  // the last argmax stays on the device
+    return MK_OK;
+}
+
+mk_status mk_finish(mk_handle* h) {
+    if (!h) {
+        set_error("NULL handle");
+        return MK_ERR_INVALID_ARG;
+    }
+    return read_status(h);
+}
+
+mk_status mk_get_state(const mk_handle* h, int32_t* pos, int32_t* pending) {
+    if (!h) {
+        set_error("NULL handle");
+        return MK_ERR_INVALID_ARG;
+    }
+    if (pos) *pos = h->pos;
+    if (pending) *pending = h->pending;
+    return MK_OK;
+}
+
+mk_status mk_set_state(mk_handle* h, int32_t pos, int32_t pending) {
+    if (!h) {
+        set_error("NULL handle");
+        return MK_ERR_INVALID_ARG;
+    }
+    if (!h->has_seq || pos < 0 || pos > h->pos) return herr(h, MK_ERR_INVALID_ARG, "can only rewind to 0..%d", h->pos);
+    if (pending < 0 || pending >= h->d.vocab) return herr(h, MK_ERR_INVALID_ARG, "pending token %d out of range", pending);
+    h->pos = pos;
+    h->pending = pending;
+    return MK_OK;
+}
+
+mk_status mk_get_launch_info(const mk_handle* h, int32_t* ctas, int32_t* threads, int32_t* smem_bytes,
+                             int32_t* n_slots, int32_t* n_tasks) {
+    if (!h) {
+        set_error("NULL handle");
+        return MK_ERR_INVALID_ARG;
+    }
+    if (ctas) *ctas = h->c.sms;
+    if (threads) *threads = THREADS;
+    if (smem_bytes) *smem_bytes = (int32_t)h->smem;
+    if (n_slots) *n_slots = h->c.n_slots;
+    if (n_tasks) *n_tasks = h->n_tasks;
+    return MK_OK;
+}
+
+int64_t mk_launch_count(const mk_handle* h) { return h ? h->launches : 0; }
+
+const char* mk_last_error(const mk_handle* h) { return h ? h->err.c_str() : thread_error(); }
+
+void mk_destroy(mk_handle* h) { delete h; }
+
+mk_status mk_debug_dequant(const mk_model_desc* desc, const void* weights_dev, int32_t tensor, int32_t layer,
+                           float* out_dev, mk_stream_t stream) {
+    size_t off = 0, stride = 0;
+    int32_t first = 0, step = 1, rows = 0;
+    mk_status st = mk_tensor_layout(desc, tensor, layer, &off, &stride, &first, &step, &rows);
+    if (st) return st;
+    if (!weights_dev || !out_dev || stride == 0) {
+        set_error("NULL pointer or not a GEMV tensor");
+        return MK_ERR_INVALID_ARG;
+    }
+    int K = 0;
+    switch (tensor) {
+        case MK_T_WO: K = desc->n_q_heads * desc->head_dim; break;
+        case MK_T_WDOWN: K = desc->d_ffn; break;
+        default: K = desc->d_model; break;
+    }
+    cudaError_t e = launch_dequant(desc->wdtype, (const uint8_t*)weights_dev + off, (int64_t)stride, first, step,
+                                   rows, K, out_dev, (cudaStream_t)stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) {
+        set_error("dequant kernel: %s", cudaGetErrorString(e));
+        return MK_ERR_CUDA;
+    }
+    return MK_OK;
+}
+
+mk_status mk_debug_watchdog(int32_t timeout_us, void* counter_dev, mk_stream_t stream) {
+    if (!counter_dev || timeout_us < 1) {
+        set_error("bad arguments");
+        return MK_ERR_INVALID_ARG;
+    }
+    uint32_t* base = (uint32_t*)counter_dev;
+    cudaError_t e = launch_watchdog(base, base + 16, (int64_t)timeout_us * 1000, (cudaStream_t)stream);
+    uint32_t s = 0;
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&s, base + 16, 4, cudaMemcpyDeviceToHost, (cudaStream_t)stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) {
+        set_error("watchdog kernel: %s", cudaGetErrorString(e));
+        return MK_ERR_CUDA;
+    }
+    if (s == DEV_TIMEOUT) {
+        set_error("wait gave up after %d us", timeout_us);
+        return MK_ERR_TIMEOUT;
+    }
+    return MK_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,725 @@
+// Lowering of the decoder to a task DAG synchronised by monotonic counters,
+// and the static validator that must accept it before any launch.
+//
+// AutoMegaKernel explainer, "Methodology": Layer 2 lowers the model to a typed
+// schedule IR (a task DAG synchronised by monotonic counters) under a
+// ScheduleConfig (tiling, SM assignment, pipelining depth); the safety gate
+// validate() certifies deadlock freedom (acyclic DAG, wait thresholds
+// 1 <= t <= #producers, valid per-SM queue order), race freedom (joined
+// multi-producer counters, happens-before on memory accesses) and correctness
+// (output reachability, referential integrity), and a schedule that fails is
+// rejected before it can reach the GPU.
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <iterator>
+#include <numeric>
+#include <string>
+#include <vector>
+
+#include "mk_host.h"
+
+namespace mk {
+
+static int64_t up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
+static int ceil_log2(int v) {
+    int r = 0;
+    while ((1 << r) < v) ++r;
+    return r;
+}
+
+// ------------------------------------------------------------------ config
+mk_status resolve_config(const mk_model_desc* d, const mk_schedule_config* cfg, int n_sms,
+                         Config* out) {
+    mk_schedule_config z{};
+    if (!cfg) cfg = &z;
+    if (n_sms < 1) {
+        set_error("n_sms %d < 1", n_sms);
+        return MK_ERR_INVALID_ARG;
+    }
+    Config c{};
+    c.sms = cfg->sms > 0 ? std::min(cfg->sms, n_sms) : n_sms;
+    if (cfg->sms < 0 || cfg->slot_bytes < 0 || cfg->n_slots < 0 || cfg->attn_chunks < 0 ||
+        cfg->watchdog_ms < 0) {
+        set_error("negative schedule knob");
+        return MK_ERR_INVALID_ARG;
+    }
+    BlobLayout b = blob_layout(d);
+    int64_t need = std::max({2 * b.row_gu, b.row_qkv, b.row_o, b.row_down, b.row_lm});
+    int64_t slot = cfg->slot_bytes ? cfg->slot_bytes : 32768;
+    if (slot % 1024) {
+        set_error("slot_bytes %d is not a multiple of 1024", cfg->slot_bytes);
+        return MK_ERR_INVALID_ARG;
+    }
+    if (slot < need) {
+        if (cfg->slot_bytes) {
+            set_error("slot_bytes %d < %lld, the largest row unit", cfg->slot_bytes, (long long)need);
+            return MK_ERR_INVALID_ARG;
+        }
+        slot = up(need, 1024);
+    }
+    if (slot > 65536) {
+        set_error("a weight row unit of %lld bytes exceeds the 64 KiB ring slot limit", (long long)need);
+        return MK_ERR_UNSUPPORTED;
+    }
+    c.slot_bytes = (int)slot;
+    c.n_slots = cfg->n_slots;  // 0: resolved against the device's shared memory at create
+    if (cfg->attn_chunks) {
+        c.C = cfg->attn_chunks;
+    } else {
+        int by_len = std::max(1, d->max_seq / 64);
+        int by_sms = std::max(1, c.sms / d->n_kv_heads);
+        c.C = std::max(1, std::min(by_len, by_sms));
+    }
+    if (c.C > 1024) {
+        set_error("attn_chunks %d > 1024", c.C);
+        return MK_ERR_INVALID_ARG;
+    }
+    c.watchdog_ns = (int64_t)(cfg->watchdog_ms ? cfg->watchdog_ms : 1000) * 1000000;
+    *out = c;
+    return MK_OK;
+}
+
+// ------------------------------------------------------------------ lowering
+namespace {
+
+struct Builder {
+    const mk_model_desc* d;
+    Config c;
+    Lowering* lw;
+    std::vector<int64_t> load;
+    int S;
+
+    // Split `units` (of unit_rows rows, unit_bytes bytes) across the CTAs: every
+    // CTA gets units/S, and the remainder goes to the CTAs with the least
+    // weight bytes so far, so that total bytes per CTA per token stay level.
+    std::vector<std::pair<int, std::pair<int64_t, int64_t>>> split(int64_t units, int64_t unit_bytes) {
+        std::vector<int64_t> cnt(S, units / S);
+        int64_t rem = units % S;
+        std::vector<int> order(S);
+        std::iota(order.begin(), order.end(), 0);
+        std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return load[a] < load[b]; });
+        for (int64_t i = 0; i < rem; ++i) cnt[order[i]] += 1;
+        std::vector<std::pair<int, std::pair<int64_t, int64_t>>> out;
+        int64_t u = 0;
+        for (int s = 0; s < S; ++s) {
+            if (!cnt[s]) continue;
+            out.push_back({s, {u, u + cnt[s]}});
+            load[s] += cnt[s] * unit_bytes;
+            u += cnt[s];
+        }
+        return out;
+    }
+
+    int add_task(int sm, const DevTask& t, std::vector<mk_ir_access> acc) {
+        mk_ir_task it{};
+        it.sm = sm;
+        it.op = t.op;
+        it.layer = t.layer;
+        it.n_waits = t.n_waits;
+        for (int i = 0; i < 2; ++i) {
+            it.wait_ctr[i] = t.wait_ctr[i];
+            it.wait_count[i] = t.wait_cnt[i];
+            it.wait_epoch_off[i] = t.wait_off[i];
+        }
+        it.signal_ctr = t.signal_ctr;
+        it.acc_begin = (int32_t)lw->acc.size();
+        it.n_acc = (int32_t)acc.size();
+        lw->acc.insert(lw->acc.end(), acc.begin(), acc.end());
+        int id = (int)lw->tasks.size();
+        lw->tasks.push_back(it);
+        lw->dev.push_back(t);
+        lw->queues[sm].push_back(id);
+        return id;
+    }
+
+    void set_wait(const std::vector<int>& ids, int ctr, int cnt, int off) {
+        for (int id : ids) {
+            mk_ir_task& it = lw->tasks[id];
+            DevTask& t = lw->dev[id];
+            it.n_waits = t.n_waits = 1;
+            it.wait_ctr[0] = t.wait_ctr[0] = ctr;
+            it.wait_count[0] = t.wait_cnt[0] = cnt;
+            it.wait_epoch_off[0] = t.wait_off[0] = off;
+        }
+    }
+};
+
+mk_ir_access A(int buf, int kind, int64_t lo, int64_t hi, int64_t stride = 0, int64_t grow = 0) {
+    mk_ir_access a;
+    a.buf = buf;
+    a.kind = kind;
+    a.lo = lo;
+    a.hi = hi;
+    a.stride = stride;
+    a.grow = grow;
+    return a;
+}
+
+}  // namespace
+
+// Nominal position for the access model: KV reads cover [0, P0 + e) and the
+// step's write lands at P0 + e.
+static constexpr int64_t P0 = 1;
+
+mk_status lower(const mk_model_desc* d, const Config& c, Lowering* lw) {
+    *lw = Lowering{};
+    Builder B{d, c, lw, std::vector<int64_t>(c.sms, 0), c.sms};
+    lw->queues.assign(c.sms, {});
+    const int L = d->n_layers, hd = d->head_dim, Hq = d->n_q_heads, Hkv = d->n_kv_heads;
+    const int rep = Hq / Hkv, C = c.C;
+    const int64_t qd = (int64_t)Hq * hd, kd = (int64_t)Hkv * hd, dm = d->d_model, F = d->d_ffn,
+                  V = d->vocab;
+    const BlobLayout bl = blob_layout(d);
+    const int CTR_LM = 5 * L;
+    lw->n_counters = 5 * L + 1;
+    auto ctr = [&](int l, int k) { return 5 * l + k; };
+    const int64_t ML_BYTES = (int64_t)Hq * C * 2 * 4;
+
+    auto gemv_task = [&](int op, int l, int64_t row0, int64_t nrows, int64_t K, int64_t rb,
+                         int64_t region, int unit_rows, int signal) {
+        DevTask t{};
+        t.op = op;
+        t.layer = l;
+        t.row0 = (int32_t)row0;
+        t.nrows = (int32_t)nrows;
+        t.K = (int32_t)K;
+        t.row_bytes = (int32_t)rb;
+        int rps = (int)std::min<int64_t>(MAX_RPS, c.slot_bytes / rb);
+        rps -= rps % unit_rows;
+        // the unrolled slot kernel for a power-of-two row tile handles at most
+        // maxg_for(tile) k-groups per thread
+        const int ng = (int)((K / 8 + NT - 1) / NT);
+        while (rps > unit_rows && ng > maxg_for(1 << ceil_log2(rps))) rps = (rps / 2) - (rps / 2) % unit_rows;
+        t.rps = rps;
+        t.rp_log2 = ceil_log2(rps);
+        t.w_off = region + row0 * rb;
+        t.signal_ctr = signal;
+        return t;
+    };
+
+    std::vector<int> prev;  // tasks of the previous stage
+    int prev_ctr = -1;
+    std::vector<int> first_qkv;
+    int fin_sm = -1;
+    std::vector<int> lm_ids;
+
+    for (int l = 0; l < L; ++l) {
+        const int64_t lb = bl.layer_bytes * l;
+        // ---- QKV: RMSNorm(x) -> rows of [Wq; Wk; Wv]
+        std::vector<int> ids;
+        for (auto& p : B.split(qd + 2 * kd, bl.row_qkv)) {
+            int64_t r0 = p.second.first, r1 = p.second.second;
+            DevTask t = gemv_task(OP_QKV, l, r0, r1 - r0, dm, bl.row_qkv, lb + bl.l_qkv, 1, ctr(l, 0));
+            std::vector<mk_ir_access> acc;
+            acc.push_back(l == 0 ? A(B_KEY, MK_ACC_READ, 0, 8) : A(B_X, MK_ACC_READ, 0, 4 * dm));
+            acc.push_back(A(B_QKV, MK_ACC_WRITE, 4 * r0, 4 * r1));
+            ids.push_back(B.add_task(p.first, t, acc));
+        }
+        if (l == 0) {
+            first_qkv = ids;
+            fin_sm = lw->tasks[ids[0]].sm;
+        } else {
+            B.set_wait(ids, prev_ctr, (int)prev.size(), 0);
+        }
+        prev = ids;
+        prev_ctr = ctr(l, 0);
+
+        // ---- attention: one task per (kv head, chunk), placed on the least-loaded CTAs
+        ids.clear();
+        const int64_t est = std::max<int64_t>(1, d->max_seq / 2 / C) * hd * 2 * 2;
+        for (int g = 0; g < Hkv; ++g) {
+            for (int ch = 0; ch < C; ++ch) {
+                int sm = (int)(std::min_element(B.load.begin(), B.load.end()) - B.load.begin());
+                B.load[sm] += est;
+                DevTask t{};
+                t.op = OP_ATTN;
+                t.layer = l;
+                t.row0 = g;
+                t.nrows = ch;
+                t.K = C;
+                t.signal_ctr = ctr(l, 1);
+                std::vector<mk_ir_access> acc;
+                acc.push_back(A(B_QKV, MK_ACC_READ, 4 * (int64_t)g * rep * hd, 4 * (int64_t)(g + 1) * rep * hd));
+                acc.push_back(A(B_QKV, MK_ACC_READ, 4 * (qd + (int64_t)g * hd), 4 * (qd + (int64_t)(g + 1) * hd)));
+                acc.push_back(A(B_QKV, MK_ACC_READ, 4 * (qd + kd + (int64_t)g * hd),
+                                4 * (qd + kd + (int64_t)(g + 1) * hd)));
+                for (int kv = 0; kv < 2; ++kv) {
+                    int64_t base = (((int64_t)l * 2 + kv) * Hkv + g) * d->max_seq * hd * 2;
+                    acc.push_back(A(B_KV, MK_ACC_READ, base, base + P0 * hd * 2, 0, hd * 2));
+                    if (ch == C - 1)  // the chunk holding the newest position appends it
+                        acc.push_back(A(B_KV, MK_ACC_WRITE, base + P0 * hd * 2, base + (P0 + 1) * hd * 2, hd * 2, 0));
+                }
+                for (int i = g * rep; i < (g + 1) * rep; ++i) {
+                    int64_t ml = ((int64_t)i * C + ch) * 2 * 4, ac = ML_BYTES + ((int64_t)i * C + ch) * hd * 4;
+                    acc.push_back(A(B_PART, MK_ACC_WRITE, ml, ml + 8));
+                    acc.push_back(A(B_PART, MK_ACC_WRITE, ac, ac + hd * 4));
+                }
+                ids.push_back(B.add_task(sm, t, acc));
+            }
+        }
+        B.set_wait(ids, prev_ctr, (int)prev.size(), 0);
+        prev = ids;
+        prev_ctr = ctr(l, 1);
+
+        // ---- O: merge partials -> rows of Wo, residual add
+        ids.clear();
+        for (auto& p : B.split(dm, bl.row_o)) {
+            int64_t r0 = p.second.first, r1 = p.second.second;
+            DevTask t = gemv_task(OP_O, l, r0, r1 - r0, qd, bl.row_o, lb + bl.l_o, 1, ctr(l, 2));
+            std::vector<mk_ir_access> acc;
+            acc.push_back(A(B_PART, MK_ACC_READ, 0, ML_BYTES + (int64_t)Hq * C * hd * 4));
+            if (l == 0) acc.push_back(A(B_KEY, MK_ACC_READ, 0, 8));
+            acc.push_back(A(B_X, MK_ACC_WRITE, 4 * r0, 4 * r1));
+            ids.push_back(B.add_task(p.first, t, acc));
+        }
+        B.set_wait(ids, prev_ctr, (int)prev.size(), 0);
+        prev = ids;
+        prev_ctr = ctr(l, 2);
+
+        // ---- gate/up (interleaved pairs) + SwiGLU
+        ids.clear();
+        for (auto& p : B.split(F, 2 * bl.row_gu)) {
+            int64_t u0 = p.second.first, u1 = p.second.second;
+            DevTask t = gemv_task(OP_GU, l, 2 * u0, 2 * (u1 - u0), dm, bl.row_gu, lb + bl.l_gu, 2, ctr(l, 3));
+            std::vector<mk_ir_access> acc;
+            acc.push_back(A(B_X, MK_ACC_READ, 0, 4 * dm));
+            acc.push_back(A(B_H, MK_ACC_WRITE, 4 * u0, 4 * u1));
+            ids.push_back(B.add_task(p.first, t, acc));
+        }
+        B.set_wait(ids, prev_ctr, (int)prev.size(), 0);
+        prev = ids;
+        prev_ctr = ctr(l, 3);
+
+        // ---- down + residual
+        ids.clear();
+        for (auto& p : B.split(dm, bl.row_down)) {
+            int64_t r0 = p.second.first, r1 = p.second.second;
+            DevTask t = gemv_task(OP_DOWN, l, r0, r1 - r0, F, bl.row_down, lb + bl.l_down, 1, ctr(l, 4));
+            std::vector<mk_ir_access> acc;
+            acc.push_back(A(B_H, MK_ACC_READ, 0, 4 * F));
+            acc.push_back(A(B_X, MK_ACC_WRITE, 4 * r0, 4 * r1));
+            ids.push_back(B.add_task(p.first, t, acc));
+        }
+        B.set_wait(ids, prev_ctr, (int)prev.size(), 0);
+        prev = ids;
+        prev_ctr = ctr(l, 4);
+    }
+
+    // ---- final norm + LM head + block argmax
+    for (auto& p : B.split(V, bl.row_lm)) {
+        int64_t r0 = p.second.first, r1 = p.second.second;
+        DevTask t = gemv_task(OP_LM, L, r0, r1 - r0, dm, bl.row_lm, bl.lm, 1, CTR_LM);
+        std::vector<mk_ir_access> acc;
+        acc.push_back(A(B_X, MK_ACC_READ, 0, 4 * dm));
+        acc.push_back(A(B_LOGITS, MK_ACC_WRITE, 4 * r0, 4 * r1, 4 * V, 0));
+        acc.push_back(A(B_KEY, MK_ACC_ATOMIC, 0, 8));
+        lm_ids.push_back(B.add_task(p.first, t, acc));
+    }
+    B.set_wait(lm_ids, prev_ctr, (int)prev.size(), 0);
+
+    // ---- read the key -> out id; on the CTA that starts the next step first
+    {
+        DevTask t{};
+        t.op = OP_FIN;
+        t.layer = L;
+        t.signal_ctr = -1;
+        std::vector<mk_ir_access> acc;
+        acc.push_back(A(B_KEY, MK_ACC_READ, 0, 8));
+        acc.push_back(A(B_OUT, MK_ACC_WRITE, 0, 4, 4, 0));
+        int id = B.add_task(fin_sm, t, acc);
+        B.set_wait({id}, CTR_LM, (int)lm_ids.size(), 0);
+    }
+    // The first layer of step e waits for the LM head of step e-1 (the token).
+    B.set_wait(first_qkv, CTR_LM, (int)lm_ids.size(), -1);
+
+    auto mm = std::minmax_element(B.load.begin(), B.load.end());
+    lw->bytes_per_sm_min = *mm.first;
+    lw->bytes_per_sm_max = *mm.second;
+    return MK_OK;
+}
+
+mk_ir* to_ir(const Lowering& lw, int n_sms) {
+    mk_ir* ir = new mk_ir{};
+    ir->n_sms = n_sms;
+    ir->n_tasks = (int32_t)lw.tasks.size();
+    ir->n_counters = lw.n_counters;
+    ir->n_buffers = B_COUNT;
+    ir->n_acc = (int32_t)lw.acc.size();
+    ir->tasks = new mk_ir_task[std::max<size_t>(1, lw.tasks.size())];
+    std::copy(lw.tasks.begin(), lw.tasks.end(), ir->tasks);
+    ir->acc = new mk_ir_access[std::max<size_t>(1, lw.acc.size())];
+    std::copy(lw.acc.begin(), lw.acc.end(), ir->acc);
+    ir->queue = new int32_t[std::max<size_t>(1, lw.tasks.size())];
+    ir->queue_off = new int32_t[n_sms + 1];
+    int32_t o = 0;
+    for (int s = 0; s < n_sms; ++s) {
+        ir->queue_off[s] = o;
+        if (s < (int)lw.queues.size())
+            for (int id : lw.queues[s]) ir->queue[o++] = id;
+    }
+    ir->queue_off[n_sms] = o;
+    ir->buf_flags = new int32_t[B_COUNT]();
+    ir->buf_flags[B_LOGITS] = MK_BUF_OUTPUT;
+    ir->buf_flags[B_OUT] = MK_BUF_OUTPUT;
+    return ir;
+}
+
+// ------------------------------------------------------------------ validator
+namespace {
+
+constexpr int EPOCHS = 3;  // unrolled steps for happens-before and races
+
+struct Fail {
+    std::string* why;
+    mk_status operator()(const std::string& s) {
+        if (why) *why = s;
+        return MK_ERR_SCHEDULE_INVALID;
+    }
+};
+
+}  // namespace
+
+mk_status validate_ir(const mk_ir* ir, std::string* why) {
+    Fail fail{why};
+    if (!ir) return fail("IR is NULL");
+    const int T = ir->n_tasks, NC = ir->n_counters, NB = ir->n_buffers, S = ir->n_sms;
+    if (T < 1 || NC < 0 || NB < 1 || S < 1 || ir->n_acc < 0) return fail("empty or negative IR sizes");
+    if (!ir->tasks || !ir->queue || !ir->queue_off || (ir->n_acc && !ir->acc)) return fail("NULL IR array");
+
+    // ---- well formed: queues, ids, ranges
+    if (ir->queue_off[0] != 0 || ir->queue_off[S] != T) return fail("queues do not hold every task once");
+    std::vector<int> qcount(T, 0), seqpos(T, -1), qlen(S);
+    for (int s = 0; s < S; ++s) {
+        if (ir->queue_off[s + 1] < ir->queue_off[s]) return fail("queue offsets decrease");
+        qlen[s] = ir->queue_off[s + 1] - ir->queue_off[s];
+        for (int i = ir->queue_off[s]; i < ir->queue_off[s + 1]; ++i) {
+            int t = ir->queue[i];
+            if (t < 0 || t >= T) return fail("queue of SM " + std::to_string(s) + " names task " + std::to_string(t));
+            if (ir->tasks[t].sm != s)
+                return fail("task " + std::to_string(t) + " queued on SM " + std::to_string(s) +
+                            " but placed on SM " + std::to_string(ir->tasks[t].sm));
+            qcount[t]++;
+            seqpos[t] = i - ir->queue_off[s];
+        }
+    }
+    for (int t = 0; t < T; ++t)
+        if (qcount[t] != 1) return fail("task " + std::to_string(t) + " queued " + std::to_string(qcount[t]) + " times");
+    std::vector<int> nprod(NC, 0);
+    for (int t = 0; t < T; ++t) {
+        const mk_ir_task& k = ir->tasks[t];
+        if (k.n_waits < 0 || k.n_waits > MK_IR_MAX_WAITS) return fail("task " + std::to_string(t) + " has bad n_waits");
+        for (int w = 0; w < k.n_waits; ++w)
+            if (k.wait_ctr[w] < 0 || k.wait_ctr[w] >= NC)
+                return fail("task " + std::to_string(t) + " waits on missing counter " + std::to_string(k.wait_ctr[w]));
+        if (k.signal_ctr != -1 && (k.signal_ctr < 0 || k.signal_ctr >= NC))
+            return fail("task " + std::to_string(t) + " signals missing counter " + std::to_string(k.signal_ctr));
+        if (k.signal_ctr >= 0) nprod[k.signal_ctr]++;
+        if (k.n_acc < 0 || k.acc_begin < 0 || k.acc_begin + k.n_acc > ir->n_acc)
+            return fail("task " + std::to_string(t) + " has a dangling access list");
+        for (int a = k.acc_begin; a < k.acc_begin + k.n_acc; ++a) {
+            const mk_ir_access& x = ir->acc[a];
+            if (x.buf < 0 || x.buf >= NB) return fail("task " + std::to_string(t) + " touches missing buffer");
+            if (x.kind < MK_ACC_READ || x.kind > MK_ACC_ATOMIC) return fail("task " + std::to_string(t) + " has a bad access kind");
+            if (x.hi < x.lo || x.lo < 0 || x.grow < 0) return fail("task " + std::to_string(t) + " has a bad byte range");
+        }
+    }
+
+    // ---- deadlock: satisfiable thresholds.  race: joined counters.
+    for (int t = 0; t < T; ++t) {
+        const mk_ir_task& k = ir->tasks[t];
+        for (int w = 0; w < k.n_waits; ++w) {
+            int c = k.wait_ctr[w], cnt = k.wait_count[w], off = k.wait_epoch_off[w];
+            if (off != 0 && off != -1)
+                return fail("task " + std::to_string(t) + " waits with epoch offset " + std::to_string(off));
+            if (cnt < 1 || cnt > nprod[c])
+                return fail("deadlock: task " + std::to_string(t) + " waits for " + std::to_string(cnt) +
+                            " signals on counter " + std::to_string(c) + " which has " +
+                            std::to_string(nprod[c]) + " producers (need 1 <= t <= #producers)");
+            if (cnt != nprod[c])
+                return fail("race: task " + std::to_string(t) + " waits for " + std::to_string(cnt) + " of " +
+                            std::to_string(nprod[c]) + " producers of counter " + std::to_string(c) +
+                            " (multi-producer counters must be joined)");
+        }
+    }
+
+    // ---- unrolled happens-before graph: nodes are task instances (t, e) and
+    //      counter instances (c, e); edges: queue order, producer -> counter,
+    //      counter(e + off) -> waiting task(e).
+    const int NT_ = T * EPOCHS, NCN = NC * EPOCHS, N = NT_ + NCN;
+    auto tn = [&](int t, int e) { return e * T + t; };
+    auto cn = [&](int c, int e) { return NT_ + e * NC + c; };
+    std::vector<std::vector<int>> prodlist(NC);
+    for (int t = 0; t < T; ++t)
+        if (ir->tasks[t].signal_ctr >= 0) prodlist[ir->tasks[t].signal_ctr].push_back(t);
+    std::vector<int> indeg(N, 0);
+    std::vector<std::vector<int>> out(N);
+    auto edge = [&](int a, int b) {
+        out[a].push_back(b);
+        indeg[b]++;
+    };
+    for (int s = 0; s < S; ++s) {
+        int prevn = -1;
+        for (int e = 0; e < EPOCHS; ++e)
+            for (int i = ir->queue_off[s]; i < ir->queue_off[s + 1]; ++i) {
+                int n = tn(ir->queue[i], e);
+                if (prevn >= 0) edge(prevn, n);
+                prevn = n;
+            }
+    }
+    for (int e = 0; e < EPOCHS; ++e)
+        for (int t = 0; t < T; ++t) {
+            const mk_ir_task& k = ir->tasks[t];
+            if (k.signal_ctr >= 0) edge(tn(t, e), cn(k.signal_ctr, e));
+            for (int w = 0; w < k.n_waits; ++w) {
+                int ee = e + k.wait_epoch_off[w];
+                if (ee >= 0) edge(cn(k.wait_ctr[w], ee), tn(t, e));
+            }
+        }
+    // Kahn order; a leftover node means a cycle: some wait can never be met.
+    std::vector<int> order;
+    order.reserve(N);
+    {
+        std::vector<int> deg = indeg, stack;
+        for (int n = 0; n < N; ++n)
+            if (!deg[n]) stack.push_back(n);
+        while (!stack.empty()) {
+            int n = stack.back();
+            stack.pop_back();
+            order.push_back(n);
+            for (int m : out[n])
+                if (--deg[m] == 0) stack.push_back(m);
+        }
+        if ((int)order.size() != N) {
+            for (int n = 0; n < NT_; ++n)
+                if (deg[n]) {
+                    int t = n % T;
+                    return fail("deadlock: the dependency graph with per-SM queue order has a cycle "
+                                "through task " + std::to_string(t) + " (SM " +
+                                std::to_string(ir->tasks[t].sm) + ", queue slot " + std::to_string(seqpos[t]) + ")");
+                }
+            return fail("deadlock: cycle among counters");
+        }
+    }
+    // Vector clocks: vc[n][s] = last queue index on SM s that happens before n.
+    std::vector<int32_t> vc((size_t)N * S, -1);
+    std::vector<std::vector<int>> in(N);
+    for (int n = 0; n < N; ++n)
+        for (int m : out[n]) in[m].push_back(n);
+    auto seq = [&](int t, int e) { return e * qlen[ir->tasks[t].sm] + seqpos[t]; };
+    for (int n : order) {
+        int32_t* v = &vc[(size_t)n * S];
+        for (int p : in[n]) {
+            const int32_t* pv = &vc[(size_t)p * S];
+            for (int s = 0; s < S; ++s) v[s] = std::max(v[s], pv[s]);
+        }
+        if (n < NT_) {
+            int t = n % T, e = n / T;
+            v[ir->tasks[t].sm] = std::max(v[ir->tasks[t].sm], seq(t, e));
+        }
+    }
+    auto hb = [&](int ta, int ea, int tb, int eb) {  // (ta,ea) happens before (tb,eb)
+        return vc[(size_t)tn(tb, eb) * S + ir->tasks[ta].sm] >= seq(ta, ea);
+    };
+
+    // ---- counter reuse across steps: a wait at step e must not be satisfiable
+    //      by increments of step e + off + 1, so every producer's next
+    //      increment must come after the waiting task.
+    for (int t = 0; t < T; ++t) {
+        const mk_ir_task& k = ir->tasks[t];
+        for (int w = 0; w < k.n_waits; ++w) {
+            int c = k.wait_ctr[w], off = k.wait_epoch_off[w];
+            for (int p : prodlist[c])
+                if (!hb(t, 1, p, 2 + off))
+                    return fail("race: counter " + std::to_string(c) + " is reused by step e+1 of producer task " +
+                                std::to_string(p) + " before waiting task " + std::to_string(t) + " of step e");
+        }
+    }
+
+    // ---- memory races over the unrolled steps.  For an access X and an SM s,
+    //      the accesses on s that X does not order form one run in queue order:
+    //      they start after vc[X][s] (everything up to there happens before X)
+    //      and end at the first access Y with vc[Y][sm(X)] >= seq(X) (vc is
+    //      monotone along a queue, so every later access on s comes after X).
+    struct Inst {
+        int32_t seq, t, e, kind;
+        int64_t lo, hi;
+    };
+    std::vector<std::vector<std::vector<Inst>>> on(NB, std::vector<std::vector<Inst>>(S));
+    for (int e = 0; e < EPOCHS; ++e)
+        for (int t = 0; t < T; ++t) {
+            const mk_ir_task& k = ir->tasks[t];
+            for (int a = k.acc_begin; a < k.acc_begin + k.n_acc; ++a) {
+                const mk_ir_access& x = ir->acc[a];
+                int64_t lo = x.lo + e * x.stride, hi = x.hi + e * x.stride + e * x.grow;
+                if (hi > lo) on[x.buf][k.sm].push_back({seq(t, e), t, e, x.kind, lo, hi});
+            }
+        }
+    for (int b = 0; b < NB; ++b)
+        for (int s = 0; s < S; ++s)
+            std::stable_sort(on[b][s].begin(), on[b][s].end(), [](const Inst& x, const Inst& y) { return x.seq < y.seq; });
+    for (int b = 0; b < NB; ++b)
+        for (int sx = 0; sx < S; ++sx)
+            for (const Inst& x : on[b][sx]) {
+                if (x.kind == MK_ACC_READ) continue;  // every conflicting pair has a write or atomic side
+                const int32_t* vx = &vc[(size_t)tn(x.t, x.e) * S];
+                for (int s = 0; s < S; ++s) {
+                    const auto& list = on[b][s];
+                    auto it = std::upper_bound(list.begin(), list.end(), vx[s],
+                                               [](int32_t v, const Inst& y) { return v < y.seq; });
+                    for (; it != list.end(); ++it) {
+                        const Inst& y = *it;
+                        if (vc[(size_t)tn(y.t, y.e) * S + sx] >= x.seq) break;  // y comes after x
+                        if (y.t == x.t && y.e == x.e) continue;
+                        if (y.lo >= x.hi || x.lo >= y.hi) continue;
+                        if (x.kind == MK_ACC_ATOMIC && y.kind == MK_ACC_ATOMIC) continue;
+                        return fail("race: task " + std::to_string(x.t) + " (step " + std::to_string(x.e) +
+                                    ") and task " + std::to_string(y.t) + " (step " + std::to_string(y.e) +
+                                    ") touch buffer " + std::to_string(b) + " bytes [" + std::to_string(std::max(x.lo, y.lo)) +
+                                    ", " + std::to_string(std::min(x.hi, y.hi)) + ") without happens-before");
+                    }
+                }
+            }
+
+    // ---- correctness: every task's writes reach an output (two steps).
+    //      Fixpoint over "useful" instances; each round merges the byte ranges
+    //      useful instances read and looks writes up by binary search.
+    {
+        const int E2 = 2;
+        std::vector<char> useful((size_t)T * E2, 0);
+        bool changed = true;
+        while (changed) {
+            changed = false;
+            std::vector<std::vector<std::pair<int64_t, int64_t>>> rr(NB);
+            for (int e = 0; e < E2; ++e)
+                for (int t = 0; t < T; ++t) {
+                    if (!useful[(size_t)e * T + t]) continue;
+                    const mk_ir_task& k = ir->tasks[t];
+                    for (int a = k.acc_begin; a < k.acc_begin + k.n_acc; ++a) {
+                        const mk_ir_access& x = ir->acc[a];
+                        if (x.kind == MK_ACC_WRITE) continue;
+                        int64_t lo = x.lo + e * x.stride, hi = x.hi + e * x.stride + e * x.grow;
+                        if (hi > lo) rr[x.buf].push_back({lo, hi});
+                    }
+                }
+            for (auto& v : rr) {  // merge into disjoint sorted intervals
+                std::sort(v.begin(), v.end());
+                std::vector<std::pair<int64_t, int64_t>> m;
+                for (auto& r : v) {
+                    if (!m.empty() && r.first <= m.back().second) m.back().second = std::max(m.back().second, r.second);
+                    else m.push_back(r);
+                }
+                v.swap(m);
+            }
+            for (int e = 0; e < E2; ++e)
+                for (int t = 0; t < T; ++t) {
+                    char& u = useful[(size_t)e * T + t];
+                    if (u) continue;
+                    const mk_ir_task& k = ir->tasks[t];
+                    for (int a = k.acc_begin; a < k.acc_begin + k.n_acc && !u; ++a) {
+                        const mk_ir_access& x = ir->acc[a];
+                        if (x.kind == MK_ACC_READ) continue;
+                        int64_t lo = x.lo + e * x.stride, hi = x.hi + e * x.stride + e * x.grow;
+                        if (hi <= lo) continue;
+                        if (ir->buf_flags && (ir->buf_flags[x.buf] & MK_BUF_OUTPUT)) {
+                            u = 1;
+                            break;
+                        }
+                        const auto& m = rr[x.buf];
+                        auto it = std::upper_bound(m.begin(), m.end(), std::make_pair(lo, INT64_MAX));
+                        if (it != m.begin() && std::prev(it)->second > lo) u = 1;  // interval starting <= lo
+                        if (it != m.end() && it->first < hi) u = 1;                // interval starting in (lo, hi)
+                    }
+                    if (u) changed = true;
+                }
+        }
+        for (int t = 0; t < T; ++t)
+            if (!useful[t] && !useful[(size_t)T + t])
+                return fail("dead task " + std::to_string(t) + ": its writes never reach an output");
+    }
+    return MK_OK;
+}
+
+WsLayout ws_layout(const mk_model_desc* d, const Config& c, int64_t n_tasks, int32_t n_counters) {
+    WsLayout w{};
+    int64_t o = 0;
+    auto take = [&](int64_t bytes) {
+        int64_t at = o;
+        o = up(o + bytes, 256);
+        return at;
+    };
+    const int64_t qd = (int64_t)d->n_q_heads * d->head_dim, kd = (int64_t)d->n_kv_heads * d->head_dim;
+    w.status = take(256);
+    w.counters = take((int64_t)n_counters * CTR_STRIDE * 4);
+    w.key = take(128);
+    w.tasks = take(n_tasks * (int64_t)sizeof(DevTask));
+    w.queue = take(n_tasks * 4);
+    w.queue_off = take((int64_t)(c.sms + 1) * 4);
+    w.inv_freq = take((int64_t)d->head_dim / 2 * 4);
+    w.x = take((int64_t)d->d_model * 4);
+    w.qkv = take((qd + 2 * kd) * 4);
+    w.part_ml = take((int64_t)d->n_q_heads * c.C * 2 * 4);
+    w.part_acc = take((int64_t)d->n_q_heads * c.C * d->head_dim * 4);
+    w.h = take((int64_t)d->d_ffn * 4);
+    w.tok = take((int64_t)d->max_seq * 4 + 16);
+    w.out_ids = take((int64_t)d->max_seq * 4 + 16);
+    w.total = o;
+    return w;
+}
+
+}  // namespace mk
+
+using namespace mk;
+
+extern "C" {
+
+mk_status mk_build_ir(const mk_model_desc* desc, const mk_schedule_config* cfg, int32_t n_sms,
+                      mk_ir** out) {
+    mk_status st = check_desc(desc);
+    if (st) return st;
+    if (!out) {
+        set_error("out is NULL");
+        return MK_ERR_INVALID_ARG;
+    }
+    Config c;
+    if ((st = resolve_config(desc, cfg, n_sms, &c))) return st;
+    Lowering lw;
+    if ((st = lower(desc, c, &lw))) return st;
+    *out = to_ir(lw, c.sms);
+    return MK_OK;
+}
+
+void mk_free_ir(mk_ir* ir) {
+    if (!ir) return;
+    delete[] ir->tasks;
+    delete[] ir->acc;
+    delete[] ir->queue;
+    delete[] ir->queue_off;
+    delete[] ir->buf_flags;
+    delete ir;
+}
+
+mk_status mk_validate_ir(const mk_ir* ir, char* why, size_t why_len) {
+    std::string w;
+    mk_status st = validate_ir(ir, &w);
+    if (st) set_error("%s", w.c_str());
+    if (why && why_len) {
+        std::snprintf(why, why_len, "%s", st ? w.c_str() : "ok");
+    }
+    return st;
+}
+
+mk_status mk_validate_schedule(const mk_model_desc* desc, const mk_schedule_config* cfg,
+                               int32_t n_sms, char* why, size_t why_len) {
+    mk_ir* ir = nullptr;
+    mk_status st = mk_build_ir(desc, cfg, n_sms, &ir);
+    if (st) {
+        if (why && why_len) std::snprintf(why, why_len, "%s", thread_error());
+        return st;
+    }
+    st = mk_validate_ir(ir, why, why_len);
+    mk_free_ir(ir);
+    return st;
+}
+
+}  // extern "C"

@@ -1,0 +1,287 @@
+/*
+ * mk.h — C ABI of the batch-1 decode megakernel library (libmk.so).
+ *
+ * One persistent, cooperative sm_103a kernel runs the whole greedy decode loop
+ * of a Llama-style dense decoder: one CTA per SM walks its own task queue
+ * (wait on a monotonic counter -> run an instruction -> signal a counter), and
+ * the host is not re-entered per token.  Sources of the design:
+ *   - AutoMegaKernel explainer (gist.science, paper 2606.09682), "Methodology":
+ *     Layer 0 VM (one cooperative threadblock per SM, local queue,
+ *     wait -> dispatch -> signal, monotonic counters), Layer 1 instructions
+ *     (GEMV, attention, RMSNorm), Layer 2 schedule IR + ScheduleConfig, and the
+ *     static validate() gate run before any launch.
+ *   - Kog MI300X monokernel tutorial (news.creeta.com), "How the monokernel
+ *     removes launch overhead": prefill, decode and LM-head sampling in one
+ *     resident kernel, no host re-entry per token.
+ *   - Netra Kernel summary (aitrends.kr 102888), section details: a runtime that
+ *     binds persistent and boundary buffers and launches on a caller-owned
+ *     stream behind a C ABI, with exact contracts and no silent fallback.
+ *
+ * Conventions for every call:
+ *   - Every call returns mk_status; nothing throws or aborts across the ABI.
+ *   - The caller owns all device memory (packed weights, KV cache, workspace)
+ *     and the stream.  The library owns only host-side state and carves its
+ *     device tables (tasks, queues, counters, activations) out of the
+ *     caller's workspace.
+ *   - "host" pointers are ordinary CPU memory; "device" pointers are CUDA
+ *     global memory of the device current at mk_create.
+ *   - On error, mk_last_error(handle) (or mk_last_error(NULL) for calls that
+ *     take no handle) returns a one-line reason; it is valid until the next
+ *     call on the same handle / thread.
+ */
+#ifndef MK_H
+#define MK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* mk_stream_t;
+
+typedef enum {
+    MK_OK = 0,
+    MK_ERR_INVALID_ARG = 1,      /* null/misaligned pointer, bad size, bad state            */
+    MK_ERR_UNSUPPORTED = 2,      /* a model variant outside the contract (biases, odd dims) */
+    MK_ERR_SCHEDULE_INVALID = 3, /* the static validator rejected the schedule: no launch   */
+    MK_ERR_CAPACITY = 4,         /* pos + n_steps > max_seq, or a buffer is too small       */
+    MK_ERR_CUDA = 5,             /* a CUDA runtime call failed                               */
+    MK_ERR_TIMEOUT = 6,          /* a device wait gave up (watchdog); state must be reset    */
+    MK_ERR_DEVICE = 7            /* the kernel reported an inconsistency (e.g. a stale key)  */
+} mk_status;
+
+/* Storage type of the GEMV weights (mk_model_desc.wdtype). */
+enum {
+    MK_W_BF16 = 0,      /* bf16 rows                                                      */
+    MK_W_FP16 = 1,      /* IEEE fp16 rows                                                 */
+    MK_W_INT8_ROW = 2,  /* int8, one fp16 scale per output row (W8A16)                     */
+    MK_W_INT4_G128 = 3  /* int4 nibbles, one fp16 scale per 128 k of a row (W4A16)         */
+};
+
+/* Model variants the contract rejects (mk_model_desc.flags). */
+enum {
+    MK_FLAG_PROJ_BIAS = 1,   /* biased projections: rejected, not silently mis-run          */
+    MK_FLAG_TIED_HEAD = 2,   /* LM head tied to the embedding: rejected (head is separate)  */
+    MK_FLAG_ROPE_SCALING = 4 /* rope scaling variants: rejected                             */
+};
+
+/* Shape of a Llama-style dense decoder (RMSNorm, rotate-half RoPE, GQA,
+ * SwiGLU FFN, final RMSNorm, untied LM head).  Contract: head_dim in {64,128},
+ * n_q_heads % n_kv_heads == 0, n_q_heads / n_kv_heads <= 8,
+ * d_model % 128 == 0, d_ffn % 128 == 0, n_q_heads * head_dim % 128 == 0,
+ * vocab < 131072, max_seq >= 1.  base_dtype (MK_W_BF16 or MK_W_FP16) is the
+ * storage type of the embedding, the norm gains and the packer's source rows;
+ * wdtype may be base_dtype, MK_W_INT8_ROW or MK_W_INT4_G128 (bf16 source). */
+typedef struct {
+    int32_t n_layers, d_model, n_q_heads, n_kv_heads, head_dim, d_ffn, vocab;
+    float rms_eps, rope_theta;
+    int32_t max_seq;
+    int32_t wdtype;
+    int32_t base_dtype;
+    int32_t flags;
+} mk_model_desc;
+
+/* Structural knobs of the lowering (AutoMegaKernel "ScheduleConfig": tiling,
+ * SM assignment, pipelining depth).  0 selects the default. */
+typedef struct {
+    int32_t sms;         /* CTAs (= SMs used); default all SMs of the device              */
+    int32_t slot_bytes;  /* weight ring slot size in bytes, multiple of 1024; 32768        */
+    int32_t n_slots;     /* weight ring depth (pipelining depth); default fills smem       */
+    int32_t attn_chunks; /* split-KV chunks per KV head; default from max_seq and sms     */
+    int32_t watchdog_ms; /* a device wait gives up after this long; default 1000          */
+} mk_schedule_config;
+
+/* ------------------------------------------------------------------ packing
+ * The packer lays every GEMV weight out as contiguous rows in one blob, in
+ * the order the device streams them: per layer [QKV rows (Wq;Wk;Wv)] [O rows]
+ * [gate/up rows interleaved: gate_j, up_j] [down rows], then the LM head, the
+ * norm gains and the embedding.  Quantised rows carry their fp16 scales after
+ * the codes; every row starts on a 16-byte boundary. */
+enum {
+    MK_T_EMBED = 0, MK_T_LM_HEAD = 1, MK_T_FINAL_NORM = 2, MK_T_ATTN_NORM = 3, MK_T_FFN_NORM = 4,
+    MK_T_WQ = 5, MK_T_WK = 6, MK_T_WV = 7, MK_T_WO = 8, MK_T_WGATE = 9, MK_T_WUP = 10,
+    MK_T_WDOWN = 11
+};
+
+/* Bytes of the packed weight blob for desc.  Errors: INVALID_ARG, UNSUPPORTED. */
+mk_status mk_packed_size(const mk_model_desc* desc, size_t* bytes);
+
+/* Pack one tensor into its place in a host blob of mk_packed_size bytes.
+ * src_host: row-major [rows][cols] array of base_dtype bit patterns (uint16),
+ * shapes as in the standard decoder (Wq [Hq*hd][d], Wk/Wv [Hkv*hd][d],
+ * Wo [d][Hq*hd], Wgate/Wup [d_ffn][d], Wdown [d][d_ffn], embed/LM head
+ * [vocab][d], norms [d]).  layer is ignored for the embedding, LM head and
+ * final norm.  Quantised models quantise here (int8 per row, int4 per
+ * 128-group; fp16 scales rounded to nearest even).  Errors: INVALID_ARG
+ * (null pointer, bad id/layer, blob too small), UNSUPPORTED. */
+mk_status mk_pack_tensor(const mk_model_desc* desc, int32_t tensor, int32_t layer,
+                         const void* src_host, void* blob_host, size_t blob_bytes);
+
+/* Byte offset, row stride and row count of a packed tensor inside the blob
+ * (rows of Wq/Wk/Wv/Wgate/Wup are interleaved with their siblings: use the
+ * stride and first_row to locate them).  Errors: INVALID_ARG. */
+mk_status mk_tensor_layout(const mk_model_desc* desc, int32_t tensor, int32_t layer,
+                           size_t* offset, size_t* row_stride, int32_t* first_row,
+                           int32_t* row_step, int32_t* rows);
+
+/* Host quantisers the packer uses (exposed for tests).  w: float32 [n][k]
+ * row-major; q: int8 [n][k]; s16: fp16 bit patterns, [n] (int8) or
+ * [n][k/128] (int4, k % 128 == 0).  Readings: s = fp16(fp32(max|w|)/127 or 7),
+ * q = clamp(round_half_even(fp32(w)/fp32(s)), +-127 or +-7), s == 0 -> q == 0. */
+mk_status mk_quantize_int8(const float* w, int64_t n, int64_t k, int8_t* q, uint16_t* s16);
+mk_status mk_quantize_int4(const float* w, int64_t n, int64_t k, int8_t* q, uint16_t* s16);
+
+/* ------------------------------------------------------------------ sizes */
+/* KV cache bytes: bf16 [n_layers][2 (K,V)][n_kv_heads][max_seq][head_dim]. */
+mk_status mk_kv_cache_size(const mk_model_desc* desc, size_t* bytes);
+
+/* Workspace bytes for desc/cfg on n_sms CTAs (n_sms <= 0: the current device's
+ * SM count, which needs a CUDA device). */
+mk_status mk_workspace_size(const mk_model_desc* desc, const mk_schedule_config* cfg,
+                            int32_t n_sms, size_t* bytes);
+
+/* ------------------------------------------------------------------ schedule IR
+ * The lowered task DAG (AutoMegaKernel "Layer 2": a typed schedule IR whose
+ * tasks are synchronised by monotonic counters).  A task on CTA `sm` runs
+ * once per decode step e (epoch): it waits until every (counter, count,
+ * epoch_off) satisfies counter >= count * (e + 1 + epoch_off), runs, then adds
+ * 1 to signal_ctr (-1: none).  Accesses describe the bytes the instruction
+ * touches at epoch e: [lo + e*stride, hi + e*stride + e*grow) of buffer buf. */
+#define MK_IR_MAX_WAITS 2
+enum { MK_ACC_READ = 1, MK_ACC_WRITE = 2, MK_ACC_ATOMIC = 3 };
+enum { MK_BUF_OUTPUT = 1 };
+
+typedef struct {
+    int32_t sm, op, layer;
+    int32_t n_waits;
+    int32_t wait_ctr[MK_IR_MAX_WAITS];
+    int32_t wait_count[MK_IR_MAX_WAITS];
+    int32_t wait_epoch_off[MK_IR_MAX_WAITS];
+    int32_t signal_ctr;
+    int32_t acc_begin, n_acc;
+} mk_ir_task;
+
+typedef struct {
+    int32_t buf, kind;
+    int64_t lo, hi, stride, grow;
+} mk_ir_access;
+
+typedef struct {
+    int32_t n_sms, n_tasks, n_counters, n_buffers, n_acc;
+    mk_ir_task* tasks;
+    mk_ir_access* acc;
+    int32_t* queue;      /* task ids, SM after SM                                  */
+    int32_t* queue_off;  /* [n_sms + 1]: SM s runs queue[queue_off[s] .. queue_off[s+1]) */
+    int32_t* buf_flags;  /* [n_buffers]: MK_BUF_OUTPUT marks the step's results      */
+} mk_ir;
+
+/* Lower desc/cfg for n_sms CTAs (host only).  *out is library-owned: free it
+ * with mk_free_ir.  Its arrays may be edited in place (tests mutate them). */
+mk_status mk_build_ir(const mk_model_desc* desc, const mk_schedule_config* cfg, int32_t n_sms,
+                      mk_ir** out);
+void mk_free_ir(mk_ir* ir);
+
+/* The static validator (AutoMegaKernel "safety gate", validate()): rejects
+ * the IR unless it is
+ *   well formed  — every id in range, every task queued once on its own SM;
+ *   deadlock-free — every wait threshold satisfiable, 1 <= count <= #producers,
+ *                   epoch_off in {-1, 0}, and the dependency graph including
+ *                   each SM's queue order acyclic;
+ *   race-free    — every multi-producer counter joined (count == #producers),
+ *                   counter reuse across steps ordered, and every pair of
+ *                   conflicting accesses ordered by happens-before over three
+ *                   unrolled steps;
+ *   correct      — every task's writes reach an output buffer.
+ * Returns MK_OK or MK_ERR_SCHEDULE_INVALID with the first reason in `why`
+ * (may be NULL).  Host only; no device is touched. */
+mk_status mk_validate_ir(const mk_ir* ir, char* why, size_t why_len);
+
+/* Lower and validate in one call (no device work). */
+mk_status mk_validate_schedule(const mk_model_desc* desc, const mk_schedule_config* cfg,
+                               int32_t n_sms, char* why, size_t why_len);
+
+/* ------------------------------------------------------------------ runtime */
+typedef struct mk_handle mk_handle;
+
+/* Check the contract, lower the model, run the static validator and only then
+ * upload the schedule into the workspace (async on `stream`).  weights_dev:
+ * the packed blob (mk_packed_size bytes, 256-byte aligned); kv_dev: the KV
+ * cache (mk_kv_cache_size bytes, 16-byte aligned); workspace_dev:
+ * mk_workspace_size bytes, 256-byte aligned.  The device current at this call
+ * is the one used by every later call on the handle.  Errors: INVALID_ARG,
+ * UNSUPPORTED, CAPACITY (buffer too small), SCHEDULE_INVALID (nothing was
+ * written to the device), CUDA. */
+mk_status mk_create(const mk_model_desc* desc, const mk_schedule_config* cfg,
+                    const void* weights_dev, size_t weights_bytes, void* kv_dev, size_t kv_bytes,
+                    void* workspace_dev, size_t workspace_bytes, mk_stream_t stream,
+                    mk_handle** out);
+
+/* Prefill: positions 0..n-2 of tokens_host go through the decoder (KV writes
+ * only, LM head skipped) in one launch; afterwards pos = n-1 and the pending
+ * token is tokens_host[n-1], which the first decode step feeds.  Resets the
+ * sequence (any earlier tokens are discarded).  Synchronous.  Errors:
+ * INVALID_ARG (n < 1, token out of range), CAPACITY (n > max_seq), CUDA,
+ * TIMEOUT. */
+mk_status mk_prefill(mk_handle* h, const int32_t* tokens_host, int32_t n);
+
+/* Greedy decode of n_steps tokens in ONE launch.  Step s feeds the pending
+ * token at position pos, writes KV[pos], emits the argmax (lowest index on
+ * ties) into out_ids_host[s], then pending <- that id and pos += 1.
+ * Synchronous: returns after the ids are on the host.  Errors: INVALID_ARG,
+ * CAPACITY (pos + n_steps > max_seq), CUDA, TIMEOUT, DEVICE. */
+mk_status mk_decode(mk_handle* h, int32_t n_steps, int32_t* out_ids_host);
+
+/* The same launch without any host synchronisation or copy (the hot path).
+ * forced_dev (nullable): int32 [n_steps]; when given, step s feeds
+ * forced_dev[s] instead of the pending token / previous argmax (teacher
+ * forcing).  out_ids_dev (nullable): int32 [n_steps].
+ * logits_dev (nullable): float32 [n_steps][vocab], every step's logits.
+ * pos advances by n_steps at once; the pending token stays on the device.
+ * Call mk_finish before reading results or trusting the state.  Errors:
+ * INVALID_ARG, CAPACITY, CUDA. */
+mk_status mk_decode_async(mk_handle* h, int32_t n_steps, const int32_t* forced_dev,
+                          int32_t* out_ids_dev, float* logits_dev);
+
+/* Wait for the stream and read the device status word: MK_OK, MK_ERR_TIMEOUT
+ * (a wait gave up; mk_create-time state is restored on the next launch) or
+ * MK_ERR_DEVICE. */
+mk_status mk_finish(mk_handle* h);
+
+/* Sequence state: the next position and the pending token (-1 while it only
+ * exists on the device after mk_decode_async). */
+mk_status mk_get_state(const mk_handle* h, int32_t* pos, int32_t* pending);
+
+/* Rewind: continue from position pos (<= current pos) feeding `pending`.
+ * KV entries at positions >= pos are rewritten by the next steps. */
+mk_status mk_set_state(mk_handle* h, int32_t pos, int32_t pending);
+
+/* Launch geometry chosen at mk_create: CTAs, threads per CTA, dynamic shared
+ * memory bytes, ring slots, tasks in the schedule. */
+mk_status mk_get_launch_info(const mk_handle* h, int32_t* ctas, int32_t* threads,
+                             int32_t* smem_bytes, int32_t* n_slots, int32_t* n_tasks);
+
+/* Kernel launches issued by this handle so far (one per prefill/decode call). */
+int64_t mk_launch_count(const mk_handle* h);
+
+const char* mk_last_error(const mk_handle* h);
+void mk_destroy(mk_handle* h);
+
+/* ------------------------------------------------------------------ test support */
+/* Dequantise one packed GEMV tensor on the device with the same device
+ * function the decode kernel uses: out_dev float32 [rows][cols] row-major.
+ * Errors: INVALID_ARG, CUDA. */
+mk_status mk_debug_dequant(const mk_model_desc* desc, const void* weights_dev, int32_t tensor,
+                           int32_t layer, float* out_dev, mk_stream_t stream);
+
+/* Launch a one-CTA kernel that waits on a counter nothing ever signals, with
+ * a watchdog of timeout_us; returns MK_ERR_TIMEOUT when the wait gave up
+ * cleanly (the context stays usable).  counter_dev: 128 zeroed bytes. */
+mk_status mk_debug_watchdog(int32_t timeout_us, void* counter_dev, mk_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MK_H */
