@@ -141,10 +141,13 @@ def test_tiny_capacity_and_state_errors(mk):
     with pytest.raises(mk.MKError) as e:
         dec.decode(1)
     assert e.value.status == mk.MK_ERR_INVALID_ARG  # no prefill yet
-    dec.prefill(synthetic.generate_prompt(w))
+    prompt = synthetic.generate_prompt(w)
+    dec.prefill(prompt)
+    room = w.max_seq - (len(prompt) - 1)   # KV slots pos .. max_seq-1
     with pytest.raises(mk.MKError) as e:
-        dec.decode(w.decode_steps + 1)
+        dec.decode(room + 1)
     assert e.value.status == mk.MK_ERR_CAPACITY
+    assert dec.decode(room).shape == (room,)
     with pytest.raises(mk.MKError) as e:
         dec.prefill(np.zeros(w.max_seq + 1, np.int32))
     assert e.value.status == mk.MK_ERR_CAPACITY
