@@ -59,7 +59,7 @@ def measured_peaks():
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in ("decode_megakernel_02_gb300/csrc/mk_vm.cu", "decode_megakernel_02_gb300/csrc/mk_internal.h",
+    for f in ("decode_megakernel_02_gb300/csrc/mk_vm.cuh", "decode_megakernel_02_gb300/csrc/mk_internal.h",
               "decode_megakernel_02_gb300/csrc/mk_schedule.cpp"):
         with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(fh.read())

@@ -41,7 +41,7 @@ class mk_model_desc(ctypes.Structure):
 
 class mk_schedule_config(ctypes.Structure):
     _fields_ = [("sms", ctypes.c_int32), ("slot_bytes", ctypes.c_int32), ("n_slots", ctypes.c_int32),
-                ("attn_chunks", ctypes.c_int32), ("watchdog_ms", ctypes.c_int32)]
+                ("attn_chunks", ctypes.c_int32), ("watchdog_ms", ctypes.c_int32), ("l2_ahead_kb", ctypes.c_int32)]
 
 
 class mk_ir_task(ctypes.Structure):
@@ -99,6 +99,7 @@ SIGNATURES = {
     "mk_last_error": (ctypes.c_char_p, [_P]),
     "mk_destroy": (None, [_P]),
     "mk_debug_dequant": (_I32, [_DESC, _P, _I32, _I32, _P, _P]),
+    "mk_debug_set_trace": (_I32, [_P, _P, _I32]),
     "mk_debug_watchdog": (_I32, [_I32, _P, _P]),
 }
 
@@ -144,8 +145,8 @@ def make_desc(workload, max_seq=None, wdtype=None, flags=0):
                          workload.rope_theta, max_seq or workload.max_seq, wd, base, flags)
 
 
-def make_config(sms=0, slot_bytes=0, n_slots=0, attn_chunks=0, watchdog_ms=0):
-    return mk_schedule_config(sms, slot_bytes, n_slots, attn_chunks, watchdog_ms)
+def make_config(sms=0, slot_bytes=0, n_slots=0, attn_chunks=0, watchdog_ms=0, l2_ahead_kb=0):
+    return mk_schedule_config(sms, slot_bytes, n_slots, attn_chunks, watchdog_ms, l2_ahead_kb)
 
 
 # ------------------------------------------------------------------ host calls
@@ -354,6 +355,12 @@ class Decoder:
         v = [_I32() for _ in range(5)]
         _check(load().mk_get_launch_info(self.h, *[ctypes.byref(x) for x in v]), self.h)
         return dict(zip(("ctas", "threads", "smem_bytes", "n_slots", "n_tasks"), [x.value for x in v]))
+
+    def set_trace(self, buf=None, records_per_cta=0):
+        """Per-task timestamps of later launches into a device uint64 tensor
+        [ctas, records_per_cta, 8] (None disables)."""
+        _check(load().mk_debug_set_trace(self.h, buf.data_ptr() if buf is not None else None,
+                                         records_per_cta), self.h)
 
     def launch_count(self):
         return load().mk_launch_count(self.h)

@@ -22,20 +22,21 @@ enum Op : int32_t {
 constexpr int NT = 256;                 // consumer threads per CTA
 constexpr int NW = NT / 32;             // consumer warps
 constexpr int THREADS = NT + 32;        // + one producer (weight streaming) warp
-constexpr int MAX_RPS = 32;             // rows per ring slot
-constexpr int MAXG = 8;                 // 8-element k groups per thread: K <= 8*NT*MAXG
-constexpr int MAX_K = 8 * NT * MAXG;    // 16384
+constexpr int MAX_RPS = 64;             // rows per ring slot
+constexpr int MAX_SLOT_BYTES = 69632;   // 68 KiB: largest ring slot the lowering picks
+constexpr int MAXG = 8;                 // 8-element k groups per lane
+constexpr int MAX_K = 8 * NT * MAXG;    // 16384: eight warps x 32 lanes x MAXG groups
 constexpr int MAX_REP = 8;              // query heads per KV head
-constexpr int ATTN_TILE = 64;           // positions per online-softmax tile
+constexpr int ATTN_TILE = 32;           // positions per online-softmax tile
 constexpr int CTR_STRIDE = 32;          // u32 words between counters (128 B lines)
+constexpr int MAX_HC = 1024;            // query heads x split-KV chunks (merge scratch)
 
-// k-groups per thread that a slot of RP rows (RP a power of two) may need; a
-// ring slot holds at most ~32 KiB, so many rows come with short rows.  The
-// lowering keeps every task within this bound.
+// Warps that share one weight row: enough that each lane holds at most
+// MAXG 8-wide k-groups of the input vector in registers (K <= 2048 * wpr).
 #ifdef __CUDACC__
 __host__ __device__
 #endif
-constexpr int maxg_for(int rp) { return rp >= 16 ? 2 : rp == 8 ? 4 : MAXG; }
+constexpr int warps_per_row(int K) { return K <= 2048 ? 1 : K <= 4096 ? 2 : K <= 8192 ? 4 : 8; }
 
 // One entry of the device task table (one IR task).
 struct DevTask {
@@ -44,14 +45,14 @@ struct DevTask {
     int32_t K;              // GEMV: reduction length.  ATTN: chunks per head
     int32_t row_bytes;      // GEMV: packed row stride
     int32_t rps;            // GEMV: rows per ring slot
-    int32_t rp_log2;        // GEMV: log2 of the power of two >= rps
+    int32_t wpr;            // GEMV: warps sharing one row (1, 2, 4, 8)
     int64_t w_off;          // GEMV: blob offset of row0
     int32_t n_waits;
     int32_t wait_ctr[2];
     int32_t wait_cnt[2];
     int32_t wait_off[2];
     int32_t signal_ctr;
-    int32_t pad[1];
+    int32_t rw;             // GEMV: rows per warp group per slot (rps = rw * 8 / wpr)
 };
 static_assert(sizeof(DevTask) == 80, "DevTask layout");
 
@@ -91,7 +92,11 @@ struct VmParams {
     int32_t n_steps, pos0, epoch0, skip_lm;
     int32_t pending;           // token fed at step 0 (no forcing); -1: status[3]
     int32_t n_slots, slot_bytes;
+    int32_t xs_floats;         // shared-memory input vector capacity: max(d, q_dim)
     int64_t watchdog_ns;
+    int64_t l2_ahead;          // weight bytes prefetched into L2 ahead of the ring (0: off)
+    unsigned long long* trace; // nullable: per-task timestamps [ctas][trace_cap][4]
+    int32_t trace_cap;
 };
 
 // Status codes written by the device into status[0].

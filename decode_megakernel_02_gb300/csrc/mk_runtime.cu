@@ -7,6 +7,7 @@
 // validation is rejected before any GPU launch.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -17,8 +18,8 @@
 #include "mk_host.h"
 
 namespace mk {
-const void* vm_kernel_for(int wdtype, int base);
-size_t vm_shared_bytes(int n_slots, int slot_bytes);
+const void* vm_kernel_for(int wdtype, int base, int hd);
+size_t vm_shared_bytes(int n_slots, int slot_bytes, int xs_floats);
 cudaError_t launch_dequant(int wdtype, const uint8_t* rows, int64_t stride, int first, int step, int nrows,
                            int K, float* out, cudaStream_t st);
 cudaError_t launch_watchdog(uint32_t* ctr, uint32_t* status, int64_t limit_ns, cudaStream_t st);
@@ -44,6 +45,9 @@ struct mk_handle {
     uint32_t epoch = 0;
     bool dirty = false;
     int64_t launches = 0;
+    int32_t xs_floats = 0;
+    unsigned long long* trace = nullptr;
+    int32_t trace_cap = 0;
     std::string err;
 };
 
@@ -130,7 +134,11 @@ mk_status launch(mk_handle* h, int n_steps, const int32_t* forced, int32_t* out_
     p.pending = h->pending;
     p.n_slots = h->c.n_slots;
     p.slot_bytes = h->c.slot_bytes;
+    p.xs_floats = h->xs_floats;
     p.watchdog_ns = h->c.watchdog_ns;
+    p.l2_ahead = h->c.l2_ahead;
+    p.trace = h->trace;
+    p.trace_cap = h->trace_cap;
     void* args[] = {&p};
     CK(h, cudaLaunchCooperativeKernel(h->kfn, dim3(h->c.sms), dim3(THREADS), args, h->smem, h->st));
     h->epoch += (uint32_t)n_steps;
@@ -208,9 +216,11 @@ mk_status mk_create(const mk_model_desc* desc, const mk_schedule_config* cfg, co
     }
     Config c;
     if ((st = resolve_config(desc, cfg, n_sms, &c))) return st;
-    const size_t fixed = vm_shared_bytes(0, c.slot_bytes);
+    const int xs_floats = std::max(desc->d_model, desc->n_q_heads * desc->head_dim);
+    const size_t fixed = vm_shared_bytes(0, c.slot_bytes, xs_floats);
     int max_slots = (int)(((size_t)smem_optin - fixed) / (size_t)c.slot_bytes);
     if (max_slots > 16) max_slots = 16;
+    if (c.n_slots == 0 && max_slots > 6) max_slots = 6;  // deeper rings stream no faster
     if (c.n_slots == 0) c.n_slots = max_slots;
     if (c.n_slots < 2 || c.n_slots > max_slots) {
         set_error("ring of %d slots of %d bytes does not fit %d bytes of shared memory (2..%d slots)", c.n_slots,
@@ -250,8 +260,9 @@ mk_status mk_create(const mk_model_desc* desc, const mk_schedule_config* cfg, co
     h->wsp = (uint8_t*)workspace_dev;
     h->st = (cudaStream_t)stream;
     h->device = dev;
-    h->kfn = vm_kernel_for(desc->wdtype, desc->base_dtype);
-    h->smem = vm_shared_bytes(c.n_slots, c.slot_bytes);
+    h->kfn = vm_kernel_for(desc->wdtype, desc->base_dtype, desc->head_dim);
+    h->smem = vm_shared_bytes(c.n_slots, c.slot_bytes, xs_floats);
+    h->xs_floats = xs_floats;
     if (!h->kfn) {
         delete h;
         set_error("no kernel for wdtype %d / base %d", desc->wdtype, desc->base_dtype);
@@ -424,6 +435,17 @@ mk_status mk_debug_dequant(const mk_model_desc* desc, const void* weights_dev, i
         set_error("dequant kernel: %s", cudaGetErrorString(e));
         return MK_ERR_CUDA;
     }
+    return MK_OK;
+}
+
+mk_status mk_debug_set_trace(mk_handle* h, void* trace_dev, int32_t records_per_cta) {
+    if (!h) {
+        set_error("NULL handle");
+        return MK_ERR_INVALID_ARG;
+    }
+    if (trace_dev && records_per_cta < 1) return herr(h, MK_ERR_INVALID_ARG, "records_per_cta must be >= 1");
+    h->trace = (unsigned long long*)trace_dev;
+    h->trace_cap = trace_dev ? records_per_cta : 0;
     return MK_OK;
 }
 

@@ -22,13 +22,20 @@
 namespace mk {
 
 static int64_t up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
-static int ceil_log2(int v) {
-    int r = 0;
-    while ((1 << r) < v) ++r;
-    return r;
-}
 
 // ------------------------------------------------------------------ config
+void plan_rows(int64_t K, int64_t row_bytes, int64_t slot_cap, int* rps, int* rw) {
+    const int groups = NW / warps_per_row((int)K);
+    *rps = 0;
+    *rw = 0;
+    for (int r = 8; r >= 2; r /= 2)
+        if ((int64_t)r * groups * row_bytes <= slot_cap && r * groups <= MAX_RPS) {
+            *rps = r * groups;
+            *rw = r;
+            return;
+        }
+}
+
 mk_status resolve_config(const mk_model_desc* d, const mk_schedule_config* cfg, int n_sms,
                          Config* out) {
     mk_schedule_config z{};
@@ -45,23 +52,29 @@ mk_status resolve_config(const mk_model_desc* d, const mk_schedule_config* cfg, 
         return MK_ERR_INVALID_ARG;
     }
     BlobLayout b = blob_layout(d);
-    int64_t need = std::max({2 * b.row_gu, b.row_qkv, b.row_o, b.row_down, b.row_lm});
-    int64_t slot = cfg->slot_bytes ? cfg->slot_bytes : 32768;
-    if (slot % 1024) {
-        set_error("slot_bytes %d is not a multiple of 1024", cfg->slot_bytes);
-        return MK_ERR_INVALID_ARG;
-    }
-    if (slot < need) {
-        if (cfg->slot_bytes) {
-            set_error("slot_bytes %d < %lld, the largest row unit", cfg->slot_bytes, (long long)need);
+    const int64_t qd = (int64_t)d->n_q_heads * d->head_dim;
+    const int64_t shapes[4][2] = {{d->d_model, b.row_qkv}, {qd, b.row_o}, {d->d_ffn, b.row_down}, {d->d_model, b.row_lm}};
+    int64_t slot = 0;
+    if (cfg->slot_bytes) {
+        if (cfg->slot_bytes % 1024 || cfg->slot_bytes > MAX_SLOT_BYTES) {
+            set_error("slot_bytes %d must be a multiple of 1024 and at most %d", cfg->slot_bytes, MAX_SLOT_BYTES);
             return MK_ERR_INVALID_ARG;
         }
-        slot = up(need, 1024);
+        slot = cfg->slot_bytes;
     }
-    if (slot > 65536) {
-        set_error("a weight row unit of %lld bytes exceeds the 64 KiB ring slot limit", (long long)need);
-        return MK_ERR_UNSUPPORTED;
+    const int64_t cap = slot ? slot : MAX_SLOT_BYTES;
+    int64_t need = 0;
+    for (auto& sh : shapes) {
+        int rps, rw;
+        plan_rows(sh[0], sh[1], cap, &rps, &rw);
+        if (!rps) {
+            set_error("a ring slot of %lld bytes cannot hold two rows per warp group of %lld bytes", (long long)cap,
+                      (long long)sh[1]);
+            return slot ? MK_ERR_INVALID_ARG : MK_ERR_UNSUPPORTED;
+        }
+        need = std::max(need, (int64_t)rps * sh[1]);
     }
+    if (!slot) slot = up(need, 1024);
     c.slot_bytes = (int)slot;
     c.n_slots = cfg->n_slots;  // 0: resolved against the device's shared memory at create
     if (cfg->attn_chunks) {
@@ -69,13 +82,18 @@ mk_status resolve_config(const mk_model_desc* d, const mk_schedule_config* cfg, 
     } else {
         int by_len = std::max(1, d->max_seq / 64);
         int by_sms = std::max(1, c.sms / d->n_kv_heads);
-        c.C = std::max(1, std::min(by_len, by_sms));
+        c.C = std::max(1, std::min(std::min(by_len, by_sms), MAX_HC / d->n_q_heads));
     }
-    if (c.C > 1024) {
-        set_error("attn_chunks %d > 1024", c.C);
+    if (c.C < 1 || (int64_t)c.C * d->n_q_heads > MAX_HC) {
+        set_error("attn_chunks %d: need 1 <= chunks * n_q_heads <= %d", c.C, MAX_HC);
         return MK_ERR_INVALID_ARG;
     }
     c.watchdog_ns = (int64_t)(cfg->watchdog_ms ? cfg->watchdog_ms : 1000) * 1000000;
+    if (cfg->l2_ahead_kb < 0) {
+        set_error("l2_ahead_kb %d < 0", cfg->l2_ahead_kb);
+        return MK_ERR_INVALID_ARG;
+    }
+    c.l2_ahead = cfg->l2_ahead_kb > 0 ? (int64_t)cfg->l2_ahead_kb * 1024 : 0;
     *out = c;
     return MK_OK;
 }
@@ -185,14 +203,12 @@ mk_status lower(const mk_model_desc* d, const Config& c, Lowering* lw) {
         t.nrows = (int32_t)nrows;
         t.K = (int32_t)K;
         t.row_bytes = (int32_t)rb;
-        int rps = (int)std::min<int64_t>(MAX_RPS, c.slot_bytes / rb);
-        rps -= rps % unit_rows;
-        // the unrolled slot kernel for a power-of-two row tile handles at most
-        // maxg_for(tile) k-groups per thread
-        const int ng = (int)((K / 8 + NT - 1) / NT);
-        while (rps > unit_rows && ng > maxg_for(1 << ceil_log2(rps))) rps = (rps / 2) - (rps / 2) % unit_rows;
+        (void)unit_rows;  // rw >= 2 keeps gate/up pairs inside one warp group
+        int rps, rw;
+        plan_rows(K, rb, c.slot_bytes, &rps, &rw);
         t.rps = rps;
-        t.rp_log2 = ceil_log2(rps);
+        t.rw = rw;
+        t.wpr = warps_per_row((int)K);
         t.w_off = region + row0 * rb;
         t.signal_ctr = signal;
         return t;

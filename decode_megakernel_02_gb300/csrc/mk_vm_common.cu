@@ -1,0 +1,86 @@
+// Kernel selection, shared-memory sizing and the test-support kernels.
+#include "mk_vm.cuh"
+
+namespace mk {
+
+// ------------------------------------------------------------------ launch
+const void* vm_kernel_bf16(int hd);
+const void* vm_kernel_fp16(int hd);
+const void* vm_kernel_int8(int hd);
+const void* vm_kernel_int4(int hd);
+
+const void* vm_kernel_for(int wdtype, int base, int hd) {
+    if (hd != 64 && hd != 128) return nullptr;
+    if (base == MK_W_FP16) return wdtype == MK_W_FP16 ? vm_kernel_fp16(hd) : nullptr;
+    switch (wdtype) {
+        case MK_W_BF16: return vm_kernel_bf16(hd);
+        case MK_W_INT8_ROW: return vm_kernel_int8(hd);
+        case MK_W_INT4_G128: return vm_kernel_int4(hd);
+        default: return nullptr;
+    }
+}
+
+size_t vm_shared_bytes(int n_slots, int slot_bytes, int xs_floats) {
+    return (size_t)n_slots * slot_bytes + (size_t)xs_floats * 4 + sizeof(Shared);
+}
+
+// ------------------------------------------------------------------ test kernels
+// Dequantise a packed tensor with the decode kernel's own code -> float path.
+template <int WT>
+__global__ void dequant_kernel(const uint8_t* rows, int64_t stride, int first, int step, int nrows, int K,
+                               float* out) {
+    const int r = blockIdx.x;
+    if (r >= nrows) return;
+    const uint8_t* row = rows + (int64_t)(first + (int64_t)r * step) * stride;
+    for (int k = threadIdx.x; k < K; k += blockDim.x) {
+        float v;
+        if constexpr (WT == MK_W_INT8_ROW) {
+            const uint32_t word = *(const uint32_t*)(row + (k & ~3)) ^ 0x80808080u;
+            v = i8_to_f32(word, k & 3) * half_bits_to_f32(*(const uint16_t*)(row + K));
+        } else if constexpr (WT == MK_W_INT4_G128) {
+            const uint32_t word = *(const uint32_t*)(row + (k >> 3) * 4) ^ 0x88888888u;
+            v = i4_to_f32(word, k & 7) * half_bits_to_f32(*(const uint16_t*)(row + K / 2 + 2 * (k >> 7)));
+        } else if constexpr (WT == MK_W_FP16) {
+            v = half_bits_to_f32(((const uint16_t*)row)[k]);
+        } else {
+            v = bf16_bits_to_f32(((const uint16_t*)row)[k]);
+        }
+        out[(int64_t)r * K + k] = v;
+    }
+}
+
+cudaError_t launch_dequant(int wdtype, const uint8_t* rows, int64_t stride, int first, int step, int nrows,
+                           int K, float* out, cudaStream_t st) {
+    dim3 grid(nrows), block(256);
+    switch (wdtype) {
+        case MK_W_INT8_ROW: dequant_kernel<MK_W_INT8_ROW><<<grid, block, 0, st>>>(rows, stride, first, step, nrows, K, out); break;
+        case MK_W_INT4_G128: dequant_kernel<MK_W_INT4_G128><<<grid, block, 0, st>>>(rows, stride, first, step, nrows, K, out); break;
+        case MK_W_FP16: dequant_kernel<MK_W_FP16><<<grid, block, 0, st>>>(rows, stride, first, step, nrows, K, out); break;
+        default: dequant_kernel<MK_W_BF16><<<grid, block, 0, st>>>(rows, stride, first, step, nrows, K, out); break;
+    }
+    return cudaGetLastError();
+}
+
+// A wait that can never be satisfied, with the same watchdog as the VM: the
+// kernel must give up, report DEV_TIMEOUT and return.
+__global__ void watchdog_kernel(uint32_t* ctr, uint32_t* status, int64_t limit_ns) {
+    if (threadIdx.x != 0) return;
+    const uint64_t t0 = gtimer();
+    for (uint32_t it = 1;; ++it) {
+        if ((int32_t)(ld_acquire(ctr) - 1u) >= 0) {
+            status[0] = DEV_OK;
+            return;
+        }
+        if ((it & 63u) == 0u && gtimer() - t0 > (uint64_t)limit_ns) {
+            status[0] = DEV_TIMEOUT;
+            return;
+        }
+    }
+}
+
+cudaError_t launch_watchdog(uint32_t* ctr, uint32_t* status, int64_t limit_ns, cudaStream_t st) {
+    watchdog_kernel<<<1, 32, 0, st>>>(ctr, status, limit_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace mk

@@ -92,6 +92,8 @@ typedef struct {
     int32_t n_slots;     /* weight ring depth (pipelining depth); default fills smem       */
     int32_t attn_chunks; /* split-KV chunks per KV head; default from max_seq and sms     */
     int32_t watchdog_ms; /* a device wait gives up after this long; default 1000          */
+    int32_t l2_ahead_kb; /* weight KiB per CTA prefetched into L2 ahead of the ring;
+                            default 0 (off)                                             */
 } mk_schedule_config;
 
 /* ------------------------------------------------------------------ packing
@@ -275,6 +277,16 @@ void mk_destroy(mk_handle* h);
  * Errors: INVALID_ARG, CUDA. */
 mk_status mk_debug_dequant(const mk_model_desc* desc, const void* weights_dev, int32_t tensor,
                            int32_t layer, float* out_dev, mk_stream_t stream);
+
+/* Record %globaltimer stamps of every task of later launches into trace_dev,
+ * uint64 [ctas][records_per_cta][8] = {task id | step << 32, wait start,
+ * wait done, after signal, ns consumer warp 0 waited for filled ring slots
+ * (cumulative), ring slots consumed (cumulative), ns the weight-streaming
+ * warp waited for free slots (cumulative), 0}; record k of a CTA is
+ * step * queue_len + queue slot, and records past the capacity are dropped.
+ * NULL disables tracing.  The buffer is caller-owned and must outlive the
+ * launches. */
+mk_status mk_debug_set_trace(mk_handle* h, void* trace_dev, int32_t records_per_cta);
 
 /* Launch a one-CTA kernel that waits on a counter nothing ever signals, with
  * a watchdog of timeout_us; returns MK_ERR_TIMEOUT when the wait gave up
