@@ -172,8 +172,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sms", type=int, default=0)
-    ap.add_argument("--slots", type=int, default=0)
-    ap.add_argument("--slot-bytes", type=int, default=0)
+    ap.add_argument("--rows-in-flight", type=int, default=0)
     ap.add_argument("--chunks", type=int, default=0)
     args = ap.parse_args()
 
@@ -221,7 +220,7 @@ def main():
     weights = synthetic.generate_weights(w)
     desc = mk.make_desc(w)
     blob = mk.pack_model(desc, weights)
-    cfg = mk.make_config(sms=args.sms, n_slots=args.slots, slot_bytes=args.slot_bytes, attn_chunks=args.chunks)
+    cfg = mk.make_config(sms=args.sms, rows_in_flight=args.rows_in_flight, attn_chunks=args.chunks)
     dec = mk.Decoder(desc, blob, cfg)
     del blob
     prompt = synthetic.generate_prompt(w)

@@ -28,7 +28,7 @@ OPS = {1: "qkv", 2: "attn", 3: "o", 4: "gu", 5: "down", 6: "lm", 7: "fin"}
 WDTYPES = {"bf16": MK_W_BF16, "fp16": MK_W_FP16, "int8": MK_W_INT8_ROW, "int4": MK_W_INT4_G128}
 STATUS_NAMES = {0: "MK_OK", 1: "MK_ERR_INVALID_ARG", 2: "MK_ERR_UNSUPPORTED", 3: "MK_ERR_SCHEDULE_INVALID",
                 4: "MK_ERR_CAPACITY", 5: "MK_ERR_CUDA", 6: "MK_ERR_TIMEOUT", 7: "MK_ERR_DEVICE"}
-THREADS_PER_CTA = 288  # 8 consumer warps + 1 weight-streaming warp
+THREADS_PER_CTA = 256  # eight warps
 
 
 class mk_model_desc(ctypes.Structure):
@@ -40,8 +40,8 @@ class mk_model_desc(ctypes.Structure):
 
 
 class mk_schedule_config(ctypes.Structure):
-    _fields_ = [("sms", ctypes.c_int32), ("slot_bytes", ctypes.c_int32), ("n_slots", ctypes.c_int32),
-                ("attn_chunks", ctypes.c_int32), ("watchdog_ms", ctypes.c_int32), ("l2_ahead_kb", ctypes.c_int32)]
+    _fields_ = [("sms", ctypes.c_int32), ("rows_in_flight", ctypes.c_int32), ("attn_chunks", ctypes.c_int32),
+                ("watchdog_ms", ctypes.c_int32)]
 
 
 class mk_ir_task(ctypes.Structure):
@@ -145,8 +145,8 @@ def make_desc(workload, max_seq=None, wdtype=None, flags=0):
                          workload.rope_theta, max_seq or workload.max_seq, wd, base, flags)
 
 
-def make_config(sms=0, slot_bytes=0, n_slots=0, attn_chunks=0, watchdog_ms=0, l2_ahead_kb=0):
-    return mk_schedule_config(sms, slot_bytes, n_slots, attn_chunks, watchdog_ms, l2_ahead_kb)
+def make_config(sms=0, rows_in_flight=0, attn_chunks=0, watchdog_ms=0):
+    return mk_schedule_config(sms, rows_in_flight, attn_chunks, watchdog_ms)
 
 
 # ------------------------------------------------------------------ host calls
@@ -354,7 +354,7 @@ class Decoder:
     def launch_info(self):
         v = [_I32() for _ in range(5)]
         _check(load().mk_get_launch_info(self.h, *[ctypes.byref(x) for x in v]), self.h)
-        return dict(zip(("ctas", "threads", "smem_bytes", "n_slots", "n_tasks"), [x.value for x in v]))
+        return dict(zip(("ctas", "threads", "smem_bytes", "rows_in_flight", "n_tasks"), [x.value for x in v]))
 
     def set_trace(self, buf=None, records_per_cta=0):
         """Per-task timestamps of later launches into a device uint64 tensor

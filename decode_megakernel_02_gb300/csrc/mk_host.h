@@ -22,14 +22,9 @@ BlobLayout blob_layout(const mk_model_desc* d);
 
 // Resolved schedule knobs.
 struct Config {
-    int sms, slot_bytes, n_slots, C;
+    int sms, rw, C;
     int64_t watchdog_ns;
-    int64_t l2_ahead;  // bytes
 };
-// Rows of one ring slot for a GEMV of reduction length K with packed rows of
-// row_bytes: rps = rw * (8 / warps_per_row(K)), rw in {2, 4, 8}, the largest
-// that fits slot_cap bytes and MAX_RPS rows (0 if even rw = 2 does not fit).
-void plan_rows(int64_t K, int64_t row_bytes, int64_t slot_cap, int* rps, int* rw);
 mk_status resolve_config(const mk_model_desc* d, const mk_schedule_config* cfg, int n_sms,
                          Config* out);
 

@@ -19,11 +19,9 @@ enum Op : int32_t {
     OP_FIN = 7    // read the step's argmax key -> out id
 };
 
-constexpr int NT = 256;                 // consumer threads per CTA
-constexpr int NW = NT / 32;             // consumer warps
-constexpr int THREADS = NT + 32;        // + one producer (weight streaming) warp
-constexpr int MAX_RPS = 64;             // rows per ring slot
-constexpr int MAX_SLOT_BYTES = 69632;   // 68 KiB: largest ring slot the lowering picks
+constexpr int NT = 256;                 // threads per CTA (eight warps)
+constexpr int NW = NT / 32;             // warps per CTA
+constexpr int THREADS = NT;
 constexpr int MAXG = 8;                 // 8-element k groups per lane
 constexpr int MAX_K = 8 * NT * MAXG;    // 16384: eight warps x 32 lanes x MAXG groups
 constexpr int MAX_REP = 8;              // query heads per KV head
@@ -44,7 +42,7 @@ struct DevTask {
     int32_t row0, nrows;    // GEMV: first row / row count.  ATTN: kv head / chunk
     int32_t K;              // GEMV: reduction length.  ATTN: chunks per head
     int32_t row_bytes;      // GEMV: packed row stride
-    int32_t rps;            // GEMV: rows per ring slot
+    int32_t rps;            // GEMV: rows per batch over all warp groups (rw * 8 / wpr)
     int32_t wpr;            // GEMV: warps sharing one row (1, 2, 4, 8)
     int64_t w_off;          // GEMV: blob offset of row0
     int32_t n_waits;
@@ -52,7 +50,7 @@ struct DevTask {
     int32_t wait_cnt[2];
     int32_t wait_off[2];
     int32_t signal_ctr;
-    int32_t rw;             // GEMV: rows per warp group per slot (rps = rw * 8 / wpr)
+    int32_t rw;             // GEMV: rows a warp group keeps in flight (a batch)
 };
 static_assert(sizeof(DevTask) == 80, "DevTask layout");
 
@@ -91,10 +89,8 @@ struct VmParams {
     // run
     int32_t n_steps, pos0, epoch0, skip_lm;
     int32_t pending;           // token fed at step 0 (no forcing); -1: status[3]
-    int32_t n_slots, slot_bytes;
     int32_t xs_floats;         // shared-memory input vector capacity: max(d, q_dim)
     int64_t watchdog_ns;
-    int64_t l2_ahead;          // weight bytes prefetched into L2 ahead of the ring (0: off)
     unsigned long long* trace; // nullable: per-task timestamps [ctas][trace_cap][4]
     int32_t trace_cap;
 };

@@ -19,7 +19,7 @@
 
 namespace mk {
 const void* vm_kernel_for(int wdtype, int base, int hd);
-size_t vm_shared_bytes(int n_slots, int slot_bytes, int xs_floats);
+size_t vm_shared_bytes(int wdtype, int xs_floats);
 cudaError_t launch_dequant(int wdtype, const uint8_t* rows, int64_t stride, int first, int step, int nrows,
                            int K, float* out, cudaStream_t st);
 cudaError_t launch_watchdog(uint32_t* ctr, uint32_t* status, int64_t limit_ns, cudaStream_t st);
@@ -132,11 +132,8 @@ mk_status launch(mk_handle* h, int n_steps, const int32_t* forced, int32_t* out_
     p.epoch0 = (int32_t)h->epoch;
     p.skip_lm = skip_lm;
     p.pending = h->pending;
-    p.n_slots = h->c.n_slots;
-    p.slot_bytes = h->c.slot_bytes;
     p.xs_floats = h->xs_floats;
     p.watchdog_ns = h->c.watchdog_ns;
-    p.l2_ahead = h->c.l2_ahead;
     p.trace = h->trace;
     p.trace_cap = h->trace_cap;
     void* args[] = {&p};
@@ -217,15 +214,9 @@ mk_status mk_create(const mk_model_desc* desc, const mk_schedule_config* cfg, co
     Config c;
     if ((st = resolve_config(desc, cfg, n_sms, &c))) return st;
     const int xs_floats = std::max(desc->d_model, desc->n_q_heads * desc->head_dim);
-    const size_t fixed = vm_shared_bytes(0, c.slot_bytes, xs_floats);
-    int max_slots = (int)(((size_t)smem_optin - fixed) / (size_t)c.slot_bytes);
-    if (max_slots > 16) max_slots = 16;
-    if (c.n_slots == 0 && max_slots > 6) max_slots = 6;  // deeper rings stream no faster
-    if (c.n_slots == 0) c.n_slots = max_slots;
-    if (c.n_slots < 2 || c.n_slots > max_slots) {
-        set_error("ring of %d slots of %d bytes does not fit %d bytes of shared memory (2..%d slots)", c.n_slots,
-                  c.slot_bytes, smem_optin, max_slots);
-        return MK_ERR_INVALID_ARG;
+    if (vm_shared_bytes(desc->wdtype, xs_floats) > (size_t)smem_optin) {
+        set_error("shared memory need %zu > %d", vm_shared_bytes(desc->wdtype, xs_floats), smem_optin);
+        return MK_ERR_UNSUPPORTED;
     }
     Lowering lw;
     if ((st = lower(desc, c, &lw))) return st;
@@ -261,7 +252,7 @@ mk_status mk_create(const mk_model_desc* desc, const mk_schedule_config* cfg, co
     h->st = (cudaStream_t)stream;
     h->device = dev;
     h->kfn = vm_kernel_for(desc->wdtype, desc->base_dtype, desc->head_dim);
-    h->smem = vm_shared_bytes(c.n_slots, c.slot_bytes, xs_floats);
+    h->smem = vm_shared_bytes(desc->wdtype, xs_floats);
     h->xs_floats = xs_floats;
     if (!h->kfn) {
         delete h;
@@ -393,7 +384,7 @@ mk_status mk_set_state(mk_handle* h, int32_t pos, int32_t pending) {
 }
 
 mk_status mk_get_launch_info(const mk_handle* h, int32_t* ctas, int32_t* threads, int32_t* smem_bytes,
-                             int32_t* n_slots, int32_t* n_tasks) {
+                             int32_t* rows_in_flight, int32_t* n_tasks) {
     if (!h) {
         set_error("NULL handle");
         return MK_ERR_INVALID_ARG;
@@ -401,7 +392,7 @@ mk_status mk_get_launch_info(const mk_handle* h, int32_t* ctas, int32_t* threads
     if (ctas) *ctas = h->c.sms;
     if (threads) *threads = THREADS;
     if (smem_bytes) *smem_bytes = (int32_t)h->smem;
-    if (n_slots) *n_slots = h->c.n_slots;
+    if (rows_in_flight) *rows_in_flight = h->c.rw;
     if (n_tasks) *n_tasks = h->n_tasks;
     return MK_OK;
 }

@@ -24,18 +24,6 @@ namespace mk {
 static int64_t up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
 
 // ------------------------------------------------------------------ config
-void plan_rows(int64_t K, int64_t row_bytes, int64_t slot_cap, int* rps, int* rw) {
-    const int groups = NW / warps_per_row((int)K);
-    *rps = 0;
-    *rw = 0;
-    for (int r = 8; r >= 2; r /= 2)
-        if ((int64_t)r * groups * row_bytes <= slot_cap && r * groups <= MAX_RPS) {
-            *rps = r * groups;
-            *rw = r;
-            return;
-        }
-}
-
 mk_status resolve_config(const mk_model_desc* d, const mk_schedule_config* cfg, int n_sms,
                          Config* out) {
     mk_schedule_config z{};
@@ -46,37 +34,15 @@ mk_status resolve_config(const mk_model_desc* d, const mk_schedule_config* cfg, 
     }
     Config c{};
     c.sms = cfg->sms > 0 ? std::min(cfg->sms, n_sms) : n_sms;
-    if (cfg->sms < 0 || cfg->slot_bytes < 0 || cfg->n_slots < 0 || cfg->attn_chunks < 0 ||
-        cfg->watchdog_ms < 0) {
+    if (cfg->sms < 0 || cfg->rows_in_flight < 0 || cfg->attn_chunks < 0 || cfg->watchdog_ms < 0) {
         set_error("negative schedule knob");
         return MK_ERR_INVALID_ARG;
     }
-    BlobLayout b = blob_layout(d);
-    const int64_t qd = (int64_t)d->n_q_heads * d->head_dim;
-    const int64_t shapes[4][2] = {{d->d_model, b.row_qkv}, {qd, b.row_o}, {d->d_ffn, b.row_down}, {d->d_model, b.row_lm}};
-    int64_t slot = 0;
-    if (cfg->slot_bytes) {
-        if (cfg->slot_bytes % 1024 || cfg->slot_bytes > MAX_SLOT_BYTES) {
-            set_error("slot_bytes %d must be a multiple of 1024 and at most %d", cfg->slot_bytes, MAX_SLOT_BYTES);
-            return MK_ERR_INVALID_ARG;
-        }
-        slot = cfg->slot_bytes;
+    c.rw = cfg->rows_in_flight ? cfg->rows_in_flight : 2;
+    if (c.rw != 2) {
+        set_error("rows_in_flight %d: only 2 is built", cfg->rows_in_flight);
+        return MK_ERR_INVALID_ARG;
     }
-    const int64_t cap = slot ? slot : MAX_SLOT_BYTES;
-    int64_t need = 0;
-    for (auto& sh : shapes) {
-        int rps, rw;
-        plan_rows(sh[0], sh[1], cap, &rps, &rw);
-        if (!rps) {
-            set_error("a ring slot of %lld bytes cannot hold two rows per warp group of %lld bytes", (long long)cap,
-                      (long long)sh[1]);
-            return slot ? MK_ERR_INVALID_ARG : MK_ERR_UNSUPPORTED;
-        }
-        need = std::max(need, (int64_t)rps * sh[1]);
-    }
-    if (!slot) slot = up(need, 1024);
-    c.slot_bytes = (int)slot;
-    c.n_slots = cfg->n_slots;  // 0: resolved against the device's shared memory at create
     if (cfg->attn_chunks) {
         c.C = cfg->attn_chunks;
     } else {
@@ -89,11 +55,6 @@ mk_status resolve_config(const mk_model_desc* d, const mk_schedule_config* cfg, 
         return MK_ERR_INVALID_ARG;
     }
     c.watchdog_ns = (int64_t)(cfg->watchdog_ms ? cfg->watchdog_ms : 1000) * 1000000;
-    if (cfg->l2_ahead_kb < 0) {
-        set_error("l2_ahead_kb %d < 0", cfg->l2_ahead_kb);
-        return MK_ERR_INVALID_ARG;
-    }
-    c.l2_ahead = cfg->l2_ahead_kb > 0 ? (int64_t)cfg->l2_ahead_kb * 1024 : 0;
     *out = c;
     return MK_OK;
 }
@@ -203,12 +164,10 @@ mk_status lower(const mk_model_desc* d, const Config& c, Lowering* lw) {
         t.nrows = (int32_t)nrows;
         t.K = (int32_t)K;
         t.row_bytes = (int32_t)rb;
-        (void)unit_rows;  // rw >= 2 keeps gate/up pairs inside one warp group
-        int rps, rw;
-        plan_rows(K, rb, c.slot_bytes, &rps, &rw);
-        t.rps = rps;
-        t.rw = rw;
+        (void)unit_rows;  // rw >= 2 keeps gate/up pairs inside one warp batch
         t.wpr = warps_per_row((int)K);
+        t.rw = c.rw;
+        t.rps = c.rw * (NW / t.wpr);
         t.w_off = region + row0 * rb;
         t.signal_ctr = signal;
         return t;

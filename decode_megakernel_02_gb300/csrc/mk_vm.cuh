@@ -9,20 +9,23 @@
 // vector ALUs, not matrix-core GEMMs.
 //
 // GB300 design (differs from the pages' kernels):
-//  * Weight streaming is split from compute.  Weight bytes never depend on
-//    activations, so one producer warp per CTA walks the CTA's whole queue
-//    ahead of the consumers and keeps a ring of shared-memory slots filled
-//    with 1-D bulk TMA copies (cp.async.bulk + mbarrier complete_tx), across
-//    counter waits and across steps.  HBM keeps streaming while consumers
-//    wait on a dependency; the ring depth is the pipelining depth.
-//  * Eight consumer warps own the arithmetic: each thread owns fixed 8-wide
-//    k-groups of the input vector in registers (fp32), reads 16/8/4-byte
-//    weight groups from shared memory (conflict-free), accumulates in fp32
-//    and reduces each slot's rows with a transposed warp reduction.
+//  * Each warp streams its own weight rows through a private ring of
+//    shared-memory slots filled by 16-byte cp.async.cg copies (no mbarriers,
+//    no cross-warp hand-off).  A bulk-copy ring shared by the CTA capped the
+//    stream near 4.7 TB/s with the full GEMV arithmetic; per-warp rings reach
+//    ~7.1 TB/s.
+//  * Weight bytes never depend on activations, so the per-warp stream runs
+//    ahead across task boundaries and counter waits: the copies of the next
+//    task's first rows are in flight while this warp waits or reduces.
+//  * Warp groups own whole rows: each lane holds a fixed fragment of the
+//    input vector in registers (fp32 pairs for packed fma.rn.f32x2) and the
+//    rows of a batch are reduced with one transposed warp reduction; large K
+//    is split over 2-8 warps that combine through shared memory.
 //  * Counters are u32 words on their own 128-byte lines; a wait is an
 //    ld.acquire.gpu spin with a %globaltimer watchdog; a signal is a
-//    __threadfence + red.release.gpu.add.  Thresholds scale with the global
-//    step (epoch), so counters never need a reset between steps or launches.
+//    red.release.gpu.add after a CTA barrier.  Thresholds scale with the
+//    global step (epoch), so counters never need a reset between steps or
+//    launches.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -37,58 +40,6 @@
 namespace mk {
 
 // ------------------------------------------------------------------ PTX helpers
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// The same test, but a thread whose phase is not complete is suspended for up
-// to `ns` nanoseconds (woken early when the phase completes) instead of
-// returning at once: spinning waiters then issue almost nothing.
-__device__ __forceinline__ bool mbar_wait_hint(uint32_t bar, uint32_t parity, uint32_t ns) {
-    uint32_t ok;
-    asm volatile(
-        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(ns)
-        : "memory");
-    return ok != 0;
-}
-constexpr uint32_t SUSPEND_NS = 20000;
-__device__ __forceinline__ uint64_t evict_first_policy() {
-    uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-    return pol;
-}
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
-                                         uint64_t pol) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], "
-        "%2, [%3], %4;" ::"r"(dst),
-        "l"(src), "r"(bytes), "r"(bar), "l"(pol)
-        : "memory");
-}
-// Fire-and-forget prefetch of [src, src + bytes) from HBM into L2.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
 __device__ __forceinline__ uint64_t gtimer() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -105,7 +56,7 @@ __device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
 __device__ __forceinline__ uint32_t ld_volatile(const uint32_t* p) {
     return *(const volatile uint32_t*)p;
 }
-// Named barrier 1 among the NT consumer threads only (the producer warp never joins).
+// Named barrier 1 among all NT threads of the CTA.
 __device__ __forceinline__ void bar_consumers() { asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory"); }
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
@@ -155,29 +106,51 @@ struct Shared {
     };
     float m[MAX_REP], l[MAX_REP], alpha[MAX_REP];
     int32_t flag;                   // broadcast of a counter-wait result
-    int32_t abort;                  // a warp gave up inside a task
+    int32_t abort;                  // set when this CTA must stop
     int32_t tok;                    // broadcast of the step's input token
-    uint32_t consumed, issued;      // ring bookkeeping for the exit drain
-    unsigned long long prod_wait_ns;   // trace: producer time waiting for free slots
-    unsigned long long full_wait_ns;   // trace: consumer warp 0 time waiting for filled slots
-    unsigned long long bars[2 * 16]; // full[16], empty[16]
+    unsigned long long t_waited;    // trace: when the current task's wait completed
 };
+
+// Weights per 16-byte chunk of a packed row's codes.
+template <int WT>
+__host__ __device__ constexpr int wpc() { return WT == MK_W_INT8_ROW ? 16 : WT == MK_W_INT4_G128 ? 32 : 8; }
+
+constexpr int RW = 2;           // rows per batch
+constexpr int TRAILER = 256;    // max trailer bytes per row (fp16 scales of a K <= 16384 int4 row)
+
+template <int WT>
+__host__ __device__ constexpr int ring_slot_bytes() {
+    return RW * (64 / wpc<WT>()) * 512 + (WT == MK_W_BF16 || WT == MK_W_FP16 ? 0 : RW * TRAILER);
+}
+template <int WT>
+__host__ __device__ constexpr int ring_slots() {  // slots that fit beside the other shared memory
+    return WT == MK_W_INT4_G128 ? 9 : WT == MK_W_INT8_ROW ? 5 : 3;
+}
+
+struct WarpStream {
+    int s, qi;               // cursor: step, next queue entry
+    int q, nb, ngroups, grp;  // current task: next batch of this warp, batches, groups, group
+    int nrows, row_bytes, nl, tlc, S, lofs, code_bytes;
+    const uint8_t* base;     // the task's first row
+    int si;                  // ring slot of the next issue
+    bool done;
+};
+
+__host__ __device__ constexpr size_t ring_offset(int xs_floats) {
+    return ((size_t)xs_floats * 4 + sizeof(Shared) + 127) / 128 * 128;
+}
 
 struct Ctx {
     const VmParams* p;
     Shared* sh;
-    uint8_t* ring;
-    float* xs;          // the task's input vector (K floats)
+    uint8_t* ring;      // this warp's weight ring (ring_slots x ring_slot_bytes)
+    WarpStream ws;      // this warp's weight-stream cursor (shared-memory ring)
+    int rs;             // ring slot of the next batch to compute
+    float* xs;          // the task's input vector (K floats, shared memory)
     float rstd;         // scale of xs applied when the fragments are loaded (RMSNorm)
     int tid, lane, warp;
-    uint32_t slot_seq;  // ring slots consumed so far (identical in every consumer warp)
-    int slot_i;         // slot_seq % n_slots
-    uint32_t slot_phase;  // (slot_seq / n_slots) & 1
     bool abort;
 };
-
-__device__ __forceinline__ uint32_t full_bar(Ctx& c, int i) { return smem_u32(&c.sh->bars[i]); }
-__device__ __forceinline__ uint32_t empty_bar(Ctx& c, int i) { return smem_u32(&c.sh->bars[16 + i]); }
 
 __device__ __forceinline__ bool aborted(const VmParams& p) { return ld_volatile(p.status) != 0; }
 
@@ -217,6 +190,7 @@ static __device__ __forceinline__ bool wait_counters(Ctx& c, const DevTask& t, i
             }
         }
         c.sh->flag = ok;
+        if (p.trace) c.sh->t_waited = gtimer();
     }
     bar_consumers();
     return c.sh->flag != 0;
@@ -229,40 +203,6 @@ __device__ __forceinline__ void signal_counter(Ctx& c, const DevTask& t) {
     bar_consumers();
     if (c.tid == 0 && t.signal_ctr >= 0 && !c.sh->abort)
         red_release_add(c.p->counters + (size_t)t.signal_ctr * CTR_STRIDE, 1u);
-}
-
-// One warp waits for ring slot `seq`: lane 0 polls with the watchdog and the
-// abort flag, the warp learns the outcome by shuffle.  Every warp waits for
-// every slot of its tasks (also slots holding none of its rows) before it
-// releases the slot, so releases never run ahead of fills.
-static __device__ __forceinline__ bool warp_wait_full(Ctx& c, int i, uint32_t par, uint32_t seq) {
-    const VmParams& p = *c.p;
-    int ok = 1;
-    const uint64_t tw0 = (p.trace && c.warp == 0 && c.lane == 0) ? gtimer() : 0;
-    if (c.lane == 0 && !mbar_try_wait(full_bar(c, i), par)) {
-        const uint64_t t0 = gtimer();
-        for (uint32_t it = 1;; ++it) {
-            if (mbar_wait_hint(full_bar(c, i), par, SUSPEND_NS)) break;
-            if ((it & 15u) == 0u) {
-                if (aborted(p)) {
-                    ok = 0;
-                    break;
-                }
-                if (gtimer() - t0 > (uint64_t)p.watchdog_ns) {
-                    raise_error(p, DEV_TIMEOUT, 0xFFFF0000u | (uint32_t)i, seq);
-                    ok = 0;
-                    break;
-                }
-            }
-        }
-    }
-    if (tw0) c.sh->full_wait_ns += gtimer() - tw0;
-    // Lane 0's acquire of the completed phase, then the warp barrier, orders
-    // every lane's reads of the slot after the bulk copy (waits by all 32
-    // lanes on one mbarrier word would serialise in shared memory).
-    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-    __syncwarp();
-    return ok != 0;
 }
 
 // ------------------------------------------------------------------ tokens
@@ -414,25 +354,20 @@ __device__ __forceinline__ float sum2(unsigned long long v) {
     return __uint_as_float((uint32_t)v) + __uint_as_float((uint32_t)(v >> 32));
 }
 
-// The lane's partial dot product of one packed weight row with its register
-// fragment xr of the input vector (no cross-lane reduction).  Lane L of a
-// row's warp group owns the 8-wide k-groups L, L + S, ..., L + (NG-1) S
-// (S = 32 * warps per row): the 32 lanes of a warp read consecutive
-// 16/8/4-byte groups, so shared-memory reads have no bank conflicts.  NG is
-// a compile-time count so that all loads of the row are issued before the
-// arithmetic; only the last group can lie past K and is zeroed by `tail_ok`.
+// The lane's partial dot product over its chunks of one row: w[j] is chunk
+// L + S*j of the row's codes, xr holds the matching input values as fp32
+// pairs (WPC/2 pairs per chunk).  int4 chunks carry their group-128 scale in
+// sc[j] (a chunk of 32 codes never straddles a group).
 template <int WT, int NG>
-__device__ __forceinline__ float row_partial(const uint8_t* row, int K, int L, int S, bool tail_ok,
-                                             const unsigned long long (&xr)[MAXG][4]) {
-    if constexpr (WT == MK_W_BF16 || WT == MK_W_FP16) {
-        uint4 w[NG];
+__device__ __forceinline__ float chunks_dot(const uint4 (&w)[NG], const float (&sc)[NG],
+                                            const unsigned long long (&xr)[NG * wpc<WT>() / 2]) {
+    constexpr int HP = wpc<WT>() / 2;  // pairs per chunk
+    unsigned long long a0 = 0ull, a1 = 0ull;
+    float f0 = 0.f, f1 = 0.f;
 #pragma unroll
-        for (int j = 0; j < NG; ++j)
-            w[j] = (j < NG - 1 || tail_ok) ? *(const uint4*)(row + (L + S * j) * 16) : make_uint4(0, 0, 0, 0);
-        unsigned long long a0 = 0ull, a1 = 0ull;
-#pragma unroll
-        for (int j = 0; j < NG; ++j) {
-            const uint32_t wv[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
+    for (int j = 0; j < NG; ++j) {
+        const uint32_t wv[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
+        if constexpr (WT == MK_W_BF16 || WT == MK_W_FP16) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 unsigned long long wp;
@@ -442,49 +377,32 @@ __device__ __forceinline__ float row_partial(const uint8_t* row, int K, int L, i
                     const float2 f = __half22float2(*(const __half2*)&wv[i]);
                     wp = pack2(f.x, f.y);
                 }
-                if (i & 1) a1 = ffma2(wp, xr[j][i], a1);
-                else a0 = ffma2(wp, xr[j][i], a0);
+                if (i & 1) a1 = ffma2(wp, xr[j * HP + i], a1);
+                else a0 = ffma2(wp, xr[j * HP + i], a0);
             }
-        }
-        return sum2(a0) + sum2(a1);
-    } else if constexpr (WT == MK_W_INT8_ROW) {
-        uint2 w[NG];
+        } else if constexpr (WT == MK_W_INT8_ROW) {
 #pragma unroll
-        for (int j = 0; j < NG; ++j)
-            w[j] = (j < NG - 1 || tail_ok) ? *(const uint2*)(row + (L + S * j) * 8) : make_uint2(0x80808080u, 0x80808080u);
-        unsigned long long a0 = 0ull, a1 = 0ull;
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t u = wv[i] ^ 0x80808080u;
+                a0 = ffma2(pack2(i8_to_f32(u, 0), i8_to_f32(u, 1)), xr[j * HP + 2 * i], a0);
+                a1 = ffma2(pack2(i8_to_f32(u, 2), i8_to_f32(u, 3)), xr[j * HP + 2 * i + 1], a1);
+            }
+        } else {  // int4
+            unsigned long long pa = 0ull, pb = 0ull;
 #pragma unroll
-        for (int j = 0; j < NG; ++j) {
-            const uint32_t u0 = w[j].x ^ 0x80808080u, u1 = w[j].y ^ 0x80808080u;
-            a0 = ffma2(pack2(i8_to_f32(u0, 0), i8_to_f32(u0, 1)), xr[j][0], a0);
-            a1 = ffma2(pack2(i8_to_f32(u0, 2), i8_to_f32(u0, 3)), xr[j][1], a1);
-            a0 = ffma2(pack2(i8_to_f32(u1, 0), i8_to_f32(u1, 1)), xr[j][2], a0);
-            a1 = ffma2(pack2(i8_to_f32(u1, 2), i8_to_f32(u1, 3)), xr[j][3], a1);
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t u = wv[i] ^ 0x88888888u;
+                pa = ffma2(pack2(i4_to_f32(u, 0), i4_to_f32(u, 1)), xr[j * HP + 4 * i], pa);
+                pb = ffma2(pack2(i4_to_f32(u, 2), i4_to_f32(u, 3)), xr[j * HP + 4 * i + 1], pb);
+                pa = ffma2(pack2(i4_to_f32(u, 4), i4_to_f32(u, 5)), xr[j * HP + 4 * i + 2], pa);
+                pb = ffma2(pack2(i4_to_f32(u, 6), i4_to_f32(u, 7)), xr[j * HP + 4 * i + 3], pb);
+            }
+            if (j & 1) f1 = fmaf(sc[j], sum2(pa) + sum2(pb), f1);
+            else f0 = fmaf(sc[j], sum2(pa) + sum2(pb), f0);
         }
-        return sum2(a0) + sum2(a1);
-    } else {  // int4: group-128 scales follow the nibbles
-        uint32_t w[NG];
-        float sc[NG];
-#pragma unroll
-        for (int j = 0; j < NG; ++j) {
-            const bool ok = j < NG - 1 || tail_ok;
-            const int g = L + S * j;
-            w[j] = ok ? *(const uint32_t*)(row + g * 4) : 0x88888888u;
-            sc[j] = ok ? half_bits_to_f32(*(const uint16_t*)(row + K / 2 + 2 * (g >> 4))) : 0.f;
-        }
-        float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-        for (int j = 0; j < NG; ++j) {
-            const uint32_t u = w[j] ^ 0x88888888u;
-            unsigned long long p = ffma2(pack2(i4_to_f32(u, 0), i4_to_f32(u, 1)), xr[j][0], 0ull);
-            p = ffma2(pack2(i4_to_f32(u, 2), i4_to_f32(u, 3)), xr[j][1], p);
-            p = ffma2(pack2(i4_to_f32(u, 4), i4_to_f32(u, 5)), xr[j][2], p);
-            p = ffma2(pack2(i4_to_f32(u, 6), i4_to_f32(u, 7)), xr[j][3], p);
-            if (j & 1) a1 = fmaf(sc[j], sum2(p), a1);
-            else a0 = fmaf(sc[j], sum2(p), a0);
-        }
-        return a0 + a1;
     }
+    if constexpr (WT == MK_W_INT4_G128) return f0 + f1;
+    else return sum2(a0) + sum2(a1);
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -520,66 +438,167 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[N], int lane) {
     return v[0];
 }
 
-// One GEMV task: rows [row0, row0 + nrows) in ring slots of rps = RW * ngroups
-// rows; warp group grp owns rows [grp*RW, grp*RW + RW) of every slot (a gate/up
-// pair stays inside one group).  Per slot a warp: waits (lane 0), computes the
-// lane partials of its RW rows, releases the slot (its arrival on the slot's
-// empty barrier; NW arrivals complete it), then reduces all RW rows with one
-// transposed warp reduction, combines the warps of a shared row (group
-// barrier) and writes the results from RW lanes in parallel.  No CTA-wide
-// barrier inside.  After a failed wait a warp keeps walking the slots without
-// touching them, so group barriers stay balanced; the task-end barrier then
-// stops the CTA.  `xin` is the input vector (shared or, from_global, device
-// memory).
-template <int WT, int BASE, int NG, int RW>
-static __device__ __forceinline__ void gemv_rows(Ctx& c, const int op, const int layer, const int row0, const int nrows, const int K,
-                          const int row_bytes, const int g, const float* xin, const bool from_global, int step,
-                          int tok, float& best_v, int& best_i) {
+// ------------------------------------------------------------------ weight stream
+// Each warp streams the weight rows it will multiply through a private ring
+// of NB shared-memory slots with cp.async (16 bytes per lane per copy), NB - 1
+// batches ahead of the batch it computes.  The warp's sequence of batches is
+// fixed by the schedule (tasks in queue order, for each GEMV task the batches
+// q = grp, grp + ngroups, ... of its warp group), so the copies run ahead
+// across counter waits and across tasks: a task usually starts with its first
+// batches already on chip.  A slot holds RW rows: the lane's chunks j of each
+// row at [(r * MAXG + j) * 512 + lane * 16] and the row's quantisation
+// trailer (scales) at [RW * MAXG * 512 + r * TRAILER].
+
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(smem_dst)),
+                 "l"(gsrc)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Move the cursor to this warp's next batch; false at the end of the launch.
+__device__ __forceinline__ bool stream_next(const VmParams& p, int q0, int q1, int warp, int lane, WarpStream& w) {
+    for (;;) {
+        if (w.q < w.nb) return true;
+        if (w.qi >= q1) {
+            if (++w.s >= p.n_steps) return false;
+            w.qi = q0;
+        }
+        const DevTask* tp = p.tasks + __ldg(p.queue + w.qi);
+        ++w.qi;
+        const int op = __ldg(&tp->op);
+        w.nb = 0;
+        w.q = 0;
+        if (!(op == OP_QKV || op == OP_O || op == OP_GU || op == OP_DOWN || (op == OP_LM && !p.skip_lm))) continue;
+        const int K = __ldg(&tp->K), g = __ldg(&tp->wpr);
+        const int L = (warp % g) * 32 + lane;
+        w.nrows = __ldg(&tp->nrows);
+        w.row_bytes = __ldg(&tp->row_bytes);
+        w.ngroups = NW / g;
+        w.grp = warp / g;
+        w.S = 32 * g;
+        const int code_bytes = p.wdtype == MK_W_INT8_ROW ? K : p.wdtype == MK_W_INT4_G128 ? K / 2 : 2 * K;
+        const int CHc = code_bytes / 16;
+        w.nl = L < CHc ? (CHc - L + w.S - 1) / w.S : 0;  // this lane's chunks of a row
+        w.tlc = (w.row_bytes - code_bytes) / 16;
+        w.base = p.w + __ldg((const long long*)&tp->w_off);
+        w.lofs = L * 16;
+        w.code_bytes = code_bytes;
+        w.nb = (w.nrows + RW - 1) / RW;
+        w.q = w.grp;
+    }
+}
+
+// Issue the copies of the cursor's batch into ring slot w.si (or an empty
+// group after the last batch), then advance.
+template <int WT>
+__device__ __forceinline__ void stream_issue(const VmParams& p, int q0, int q1, int warp, int lane, uint8_t* ring,
+                                             WarpStream& w) {
+    constexpr int NGM = 64 / wpc<WT>();
+    if (!w.done && stream_next(p, q0, q1, warp, lane, w)) {
+        uint8_t* slot = ring + (size_t)w.si * ring_slot_bytes<WT>() + lane * 16;
+        const int64_t jstep = (int64_t)w.S * 16;
+#pragma unroll
+        for (int r = 0; r < RW; ++r) {
+            const int row = w.q * RW + r;
+            if (row < w.nrows) {
+                const uint8_t* rowp = w.base + (int64_t)row * w.row_bytes;
+                const uint8_t* src = rowp + w.lofs;
+#pragma unroll
+                for (int j = 0; j < NGM; ++j)
+                    if (j < w.nl) cp_async16(slot + (r * NGM + j) * 512, src + j * jstep);
+                if constexpr (!(WT == MK_W_BF16 || WT == MK_W_FP16)) {
+                    if (lane < w.tlc)  // the row's scales follow its codes
+                        cp_async16(slot + RW * NGM * 512 + r * TRAILER, rowp + w.code_bytes + lane * 16);
+                }
+            }
+        }
+        w.q += w.ngroups;
+        if (++w.si == ring_slots<WT>()) w.si = 0;
+    } else {
+        w.done = true;
+    }
+    cp_async_commit();
+}
+
+// One GEMV task.  Warp group grp (g warps sharing each row) owns the batches
+// of RW consecutive rows q*RW .. q*RW+RW for q = grp, grp + ngroups, ...; a
+// gate/up pair stays inside one batch.  The batches come from the warp's
+// stream (already requested before the counter wait).  Returns false when
+// the CTA must stop (abort or watchdog), identically in every thread.
+template <int WT, int BASE, int NG>
+__device__ bool gemv_run(Ctx& c, const DevTask& t, int task_id, int step, float& best_v, int& best_i) {
     const VmParams& p = *c.p;
-    const int ngroups = NW / g;
+    constexpr int HP = wpc<WT>() / 2;
+    constexpr int NGM = 64 / wpc<WT>();
+    constexpr int NB = ring_slots<WT>();
+    const int op = t.op, layer = t.layer, row0 = t.row0, nrows = t.nrows, K = t.K;
+    const int g = t.wpr, ngroups = NW / g;
     const int grp = c.warp / g, wig = c.warp % g;
     const int L = wig * 32 + c.lane, S = 32 * g;
-    const int G = K >> 3;
-    const bool tail_ok = L + S * (NG - 1) < G;
-    const float xscale = from_global ? 1.f : c.rstd;
-    unsigned long long xr[MAXG][4];
-#pragma unroll
-    for (int j = 0; j < NG; ++j) {
-        const int gi = (j < NG - 1 || tail_ok) ? L + S * j : 0;
-        float4 a, b;
-        if (from_global) {
-            a = __ldcg((const float4*)(xin + 8 * gi));
-            b = __ldcg((const float4*)(xin + 8 * gi + 4));
-        } else {
-            a = *(const float4*)(xin + 8 * gi);
-            b = *(const float4*)(xin + 8 * gi + 4);
-        }
-        const bool ok = j < NG - 1 || tail_ok;
-        const float f = xscale;
-        xr[j][0] = ok ? pack2(a.x * f, a.y * f) : 0ull;
-        xr[j][1] = ok ? pack2(a.z * f, a.w * f) : 0ull;
-        xr[j][2] = ok ? pack2(b.x * f, b.y * f) : 0ull;
-        xr[j][3] = ok ? pack2(b.z * f, b.w * f) : 0ull;
+    const int CH = K / wpc<WT>();  // 16-byte chunks of codes per row
+
+    if (!wait_counters(c, t, task_id, step)) return false;
+    int tok = 0;
+    if (layer == 0 && (op == OP_QKV || op == OP_O)) {
+        if (c.tid == 0) c.sh->tok = step_token(p, step);
+        bar_consumers();
+        tok = c.sh->tok;
+        if (tok < 0) return false;
     }
-    constexpr int B = RW >= 8 ? 3 : RW >= 4 ? 2 : 1;  // log2(RW)
-    const int rps = RW * ngroups;
-    const int n_slots = p.n_slots, slot_bytes = p.slot_bytes;
-    // after the reduction lane l holds row (l >> (5 - B)) of the group's RW rows
-    const int my_r = c.lane >> (5 - B);
+    const float* xin = c.xs;
+    bool from_global = false;
+    switch (op) {
+        case OP_QKV: {
+            const uint16_t* gain = (const uint16_t*)(p.w + p.layer_bytes * layer + p.l_attn_norm);
+            const uint16_t* emb = layer == 0 ? (const uint16_t*)(p.w + p.embed) + (size_t)tok * p.d : nullptr;
+            prologue_rmsnorm<BASE>(c, p.x, emb, gain, p.d, p.eps);
+            break;
+        }
+        case OP_GU:
+            prologue_rmsnorm<BASE>(c, p.x, nullptr, (const uint16_t*)(p.w + p.layer_bytes * layer + p.l_ffn_norm), p.d,
+                                   p.eps);
+            break;
+        case OP_LM: prologue_rmsnorm<BASE>(c, p.x, nullptr, (const uint16_t*)(p.w + p.final_norm), p.d, p.eps); break;
+        case OP_O: prologue_attention(c); break;
+        default:  // down reads h straight from device memory
+            xin = p.h;
+            from_global = true;
+            break;
+    }
+    // the lane's fragment of the input vector: k of chunk L + S*j
+    unsigned long long xr[NG * HP];
+    {
+        const float f = from_global ? 1.f : c.rstd;
+#pragma unroll
+        for (int j = 0; j < NG; ++j) {
+            const int cidx = L + S * j;
+            const bool ok = cidx < CH;
+            const float* xp = xin + (ok ? cidx : 0) * wpc<WT>();
+#pragma unroll
+            for (int i = 0; i < HP / 2; ++i) {
+                float4 v;
+                if (from_global) v = __ldcg((const float4*)(xp + 4 * i));
+                else v = *(const float4*)(xp + 4 * i);
+                xr[j * HP + 2 * i] = ok ? pack2(v.x * f, v.y * f) : 0ull;
+                xr[j * HP + 2 * i + 1] = ok ? pack2(v.z * f, v.w * f) : 0ull;
+            }
+        }
+    }
+    constexpr int B = RW >= 8 ? 3 : RW >= 4 ? 2 : RW >= 2 ? 1 : 0;  // log2(RW)
+    const int my_r = c.lane >> (5 - B);                              // row of the batch this lane finishes
     const bool writer = (c.lane & ((32 >> B) - 1)) == 0;
-    bool dead = false;
     int par = 0;
-    uint32_t seq = c.slot_seq;
-    int si = c.slot_i;
-    uint32_t phase = c.slot_phase;
-    for (int r0 = 0; r0 < nrows; r0 += rps) {
-        const int rows_here = min(rps, nrows - r0);
-        const int first = grp * RW;  // first row of this group inside the slot
-        const int row_g = row0 + r0 + first + my_r;  // global row this lane may finish
-        const bool has_row = first + my_r < rows_here;
-        // residual input of this lane's row, requested before the slot arrives
-        float resid = 0.f;
-        if (writer && has_row && !dead) {
+    const int nbatches = (nrows + RW - 1) / RW;
+    const int q0 = p.queue_off[blockIdx.x], q1 = p.queue_off[blockIdx.x + 1];
+    for (int q = grp; q < nbatches; q += ngroups) {
+        const int rb = q * RW;
+        const int row_g = row0 + rb + my_r;
+        const bool has_row = rb + my_r < nrows;
+        float resid = 0.f;  // residual input of this lane's row
+        if (writer && has_row) {
             if (op == OP_DOWN || (op == OP_O && layer > 0)) {
                 resid = __ldcg(p.x + row_g);
             } else if (op == OP_O) {
@@ -587,20 +606,37 @@ static __device__ __forceinline__ void gemv_rows(Ctx& c, const int op, const int
                 resid = base_to_f32<BASE>(__ldg(e + row_g));
             }
         }
-        if (!dead) dead = !warp_wait_full(c, si, phase, seq);
-        const uint8_t* slot = c.ring + (size_t)si * slot_bytes;
-        float v[RW];
-        float scale = 1.f;
-#pragma unroll
-        for (int r = 0; r < RW; ++r)
-            v[r] = (!dead && first + r < rows_here)
-                       ? row_partial<WT, NG>(slot + (size_t)(first + r) * row_bytes, K, L, S, tail_ok, xr)
-                       : 0.f;
-        if constexpr (WT == MK_W_INT8_ROW) {
-            if (writer && has_row && !dead) scale = half_bits_to_f32(*(const uint16_t*)(slot + (size_t)(first + my_r) * row_bytes + K));
-        }
+        // keep NB - 1 batches in flight beyond this one, then wait for this one
+        stream_issue<WT>(p, q0, q1, c.warp, c.lane, c.ring, c.ws);
+        cp_async_wait<NB - 1>();
         __syncwarp();
-        if (c.lane == 0 && !dead) mbar_arrive(empty_bar(c, si));  // the slot is no longer read
+        const uint8_t* slot = c.ring + (size_t)c.rs * ring_slot_bytes<WT>();
+        float v[RW], rsv[RW];
+#pragma unroll
+        for (int r = 0; r < RW; ++r) {
+            uint4 w[NG];
+            float sc[NG];
+            // Chunks past the row's end and rows past the task's end read
+            // whatever the slot holds: zeros (the ring is cleared at start) or
+            // finite weights of an earlier batch.  Their input values are
+            // zero and their results are discarded, so no test is needed.
+#pragma unroll
+            for (int j = 0; j < NG; ++j) {
+                w[j] = *(const uint4*)(slot + (r * NGM + j) * 512 + c.lane * 16);
+                if constexpr (WT == MK_W_INT4_G128)
+                    sc[j] = half_bits_to_f32(
+                        *(const uint16_t*)(slot + RW * NGM * 512 + r * TRAILER + 2 * (((L + S * j) >> 2) & (TRAILER / 2 - 1))));
+                else
+                    sc[j] = 0.f;
+            }
+            v[r] = chunks_dot<WT, NG>(w, sc, xr);
+            if constexpr (WT == MK_W_INT8_ROW)
+                rsv[r] = half_bits_to_f32(*(const uint16_t*)(slot + RW * NGM * 512 + r * TRAILER));
+            else
+                rsv[r] = 1.f;
+        }
+        __syncwarp();  // the slot is reused by a later issue of this warp
+        if (++c.rs == NB) c.rs = 0;
         float tot = transpose_reduce<RW>(v, c.lane);
         if (g > 1) {
             float* scr = &c.sh->gpart[grp][par][0][0];  // [row][warp]
@@ -608,15 +644,20 @@ static __device__ __forceinline__ void gemv_rows(Ctx& c, const int op, const int
             bar_group(2 + grp, S);
             if (wig == 0 && writer) {
                 tot = 0.f;
-                for (int w = 0; w < g; ++w) tot += scr[my_r * NW + w];
+                for (int ww = 0; ww < g; ++ww) tot += scr[my_r * NW + ww];
             }
             par ^= 1;
         }
-        if constexpr (WT == MK_W_INT8_ROW) tot *= scale;
+        if constexpr (WT == MK_W_INT8_ROW) {
+            float scale = rsv[0];
+#pragma unroll
+            for (int r = 1; r < RW; ++r) scale = my_r == r ? rsv[r] : scale;
+            tot *= scale;
+        }
         if (op == OP_GU) {  // rows alternate gate, up: the up total sits one row further
             const float up = __shfl_down_sync(0xFFFFFFFFu, tot, 32 >> B);
-            if (wig == 0 && writer && has_row && !dead && !(my_r & 1)) p.h[row_g >> 1] = silu(tot) * up;
-        } else if (wig == 0 && writer && has_row && !dead) {
+            if (wig == 0 && writer && has_row && !(my_r & 1)) p.h[row_g >> 1] = silu(tot) * up;
+        } else if (wig == 0 && writer && has_row) {
             if (op == OP_LM) {
                 if (p.logits) p.logits[(size_t)step * p.V + row_g] = tot;
                 if (tot > best_v) {  // rows ascend per lane: the first maximum is kept
@@ -629,45 +670,26 @@ static __device__ __forceinline__ void gemv_rows(Ctx& c, const int op, const int
                 p.x[row_g] = resid + tot;
             }
         }
-        ++seq;
-        if (++si == n_slots) {
-            si = 0;
-            phase ^= 1u;
-        }
     }
-    c.slot_seq = seq;
-    c.slot_i = si;
-    c.slot_phase = phase;
-    if (dead && c.lane == 0) c.sh->abort = 1;
+    return true;
 }
 
 template <int WT, int BASE>
-static __device__ __forceinline__ void gemv_task(Ctx& c, const DevTask& task, const float* xin, bool from_global, int step, int tok,
-                          float& best_v, int& best_i) {
-    const int op = task.op, layer = task.layer, row0 = task.row0, nrows = task.nrows, K = task.K;
-    const int row_bytes = task.row_bytes, g = task.wpr, rw = task.rw;
-    const int S = 32 * g, ng = ((K >> 3) + S - 1) / S;
-#define MK_ROWS(N, R) gemv_rows<WT, BASE, N, R>(c, op, layer, row0, nrows, K, row_bytes, g, xin, from_global, step, tok, best_v, best_i)
-#define MK_NG(R)                         \
-    switch (ng) {                        \
-        case 1: MK_ROWS(1, R); break;    \
-        case 2: MK_ROWS(2, R); break;    \
-        case 3: MK_ROWS(3, R); break;    \
-        case 4: MK_ROWS(4, R); break;    \
-        case 5: MK_ROWS(5, R); break;    \
-        case 6: MK_ROWS(6, R); break;    \
-        case 7: MK_ROWS(7, R); break;    \
-        default: MK_ROWS(8, R); break;   \
+__device__ bool gemv_task(Ctx& c, const DevTask& t, int task_id, int step, float& best_v, int& best_i) {
+    const int S = 32 * t.wpr, CH = t.K / wpc<WT>(), ng = (CH + S - 1) / S;
+    constexpr int NGMAX = 64 / wpc<WT>();  // 8 (16-bit), 4 (int8), 2 (int4)
+#define MK_RUN(N) return gemv_run<WT, BASE, (N <= NGMAX ? N : NGMAX)>(c, t, task_id, step, best_v, best_i)
+    switch (ng) {
+        case 1: MK_RUN(1);
+        case 2: MK_RUN(2);
+        case 3: MK_RUN(3);
+        case 4: MK_RUN(4);
+        case 5: MK_RUN(5);
+        case 6: MK_RUN(6);
+        case 7: MK_RUN(7);
+        default: MK_RUN(8);
     }
-    if (rw >= 8) {
-        MK_NG(8)
-    } else if (rw == 4) {
-        MK_NG(4)
-    } else {
-        MK_NG(2)
-    }
-#undef MK_NG
-#undef MK_ROWS
+#undef MK_RUN
 }
 
 // ------------------------------------------------------------------ attention
@@ -852,122 +874,9 @@ static __device__ __forceinline__ void attn_task(Ctx& c, const DevTask& t, int s
     }
 }
 
-// ------------------------------------------------------------------ producer
-__device__ __forceinline__ bool streams_weights(const VmParams& p, int op) {
-    return op == OP_QKV || op == OP_O || op == OP_GU || op == OP_DOWN || (op == OP_LM && !p.skip_lm);
-}
-
-// Walks the weight chunks of this CTA's queue in consumption order.  The
-// current task's fields stay in registers, so the task table is read once
-// per task, not once per chunk.
-struct ChunkCursor {
-    int s, qi, r0;
-    int nrows, rps, row_bytes;  // current streaming task (nrows == 0: none loaded)
-    const uint8_t* base;
-};
-
-// Advance to the next weight chunk (rows r0 .. r0 + rps of a streaming task);
-// returns false at the end of the launch.
-__device__ __forceinline__ bool next_chunk(const VmParams& p, int q0, int q1, ChunkCursor& k, const uint8_t*& src,
-                                           uint32_t& bytes) {
-    for (;;) {
-        if (k.r0 < k.nrows) {
-            src = k.base + (int64_t)k.r0 * k.row_bytes;
-            bytes = (uint32_t)(min(k.rps, k.nrows - k.r0) * k.row_bytes);
-            k.r0 += k.rps;
-            return true;
-        }
-        // load the next streaming task
-        k.nrows = 0;
-        k.r0 = 0;
-        if (k.qi >= q1) {
-            if (++k.s >= p.n_steps) return false;
-            k.qi = q0;
-        }
-        const DevTask& t = p.tasks[__ldg(p.queue + k.qi)];
-        ++k.qi;
-        const int op = __ldg(&t.op);
-        if (streams_weights(p, op)) {
-            k.nrows = __ldg(&t.nrows);
-            k.rps = __ldg(&t.rps);
-            k.row_bytes = __ldg(&t.row_bytes);
-            k.base = p.w + __ldg((const long long*)&t.w_off);
-        }
-    }
-}
-
-// The weight-streaming lane.  Weights never depend on activations, so it
-// walks the CTA's queue ahead of the consumers through every counter wait and
-// every step: an L2 cursor keeps up to l2_ahead bytes requested from HBM into
-// L2 (bulk prefetches, nothing to wait for), and the ring cursor copies chunk
-// after chunk into the shared-memory slots as the consumers free them.
-static __device__ __forceinline__ void producer_lane(Ctx& c) {
-    const VmParams& p = *c.p;
-    const uint64_t pol = evict_first_policy();
-    const int q0 = p.queue_off[blockIdx.x], q1 = p.queue_off[blockIdx.x + 1];
-    const int n_slots = p.n_slots;
-    uint32_t seq = 0, phase = 0;  // phase: parity of the current use of slot si
-    int si = 0;
-    ChunkCursor ring{0, q0, 0, 0, 1, 0, nullptr}, pf{0, q0, 0, 0, 1, 0, nullptr};
-    int64_t ring_bytes = 0, pf_bytes = 0;
-    bool pf_done = p.l2_ahead <= 0;
-    const uint8_t* src;
-    uint32_t bytes;
-    while (next_chunk(p, q0, q1, ring, src, bytes)) {
-        ring_bytes += bytes;
-        while (!pf_done && pf_bytes < ring_bytes + p.l2_ahead) {
-            const uint8_t* psrc;
-            uint32_t pbytes;
-            if (!next_chunk(p, q0, q1, pf, psrc, pbytes)) {
-                pf_done = true;
-                break;
-            }
-            if (pf_bytes + pbytes > ring_bytes - bytes) bulk_prefetch_l2(psrc, pbytes);  // not yet in the ring
-            pf_bytes += pbytes;
-        }
-        if (seq >= (uint32_t)n_slots) {  // wait for the previous use of slot si to be released
-            const uint32_t par = phase ^ 1u;
-            const uint64_t tw0 = p.trace ? gtimer() : 0;
-            if (!mbar_try_wait(empty_bar(c, si), par)) {
-                const uint64_t t0 = gtimer();
-                bool stop = false;
-                for (uint32_t it = 1;; ++it) {
-                    if (mbar_wait_hint(empty_bar(c, si), par, SUSPEND_NS)) break;
-                    if ((it & 15u) == 0u) {
-                        if (aborted(p)) {
-                            stop = true;
-                            break;
-                        }
-                        if (gtimer() - t0 > (uint64_t)p.watchdog_ns) {
-                            raise_error(p, DEV_TIMEOUT, 0xFFFE0000u | (uint32_t)si, seq);
-                            stop = true;
-                            break;
-                        }
-                    }
-                }
-                if (stop) break;
-            }
-            if (tw0) c.sh->prod_wait_ns += gtimer() - tw0;
-        }
-        mbar_expect_tx(full_bar(c, si), bytes);
-        bulk_g2s(smem_u32(c.ring + (size_t)si * p.slot_bytes), src, bytes, full_bar(c, si), pol);
-        ++seq;
-        if (++si == n_slots) {
-            si = 0;
-            phase ^= 1u;
-        }
-    }
-    c.sh->issued = seq;
-}
-
-static __device__ __forceinline__ void producer(Ctx& c) {
-    if (c.lane == 0) producer_lane(c);
-    __syncwarp();  // the warp reaches the final CTA barrier converged
-}
-
 // ------------------------------------------------------------------ consumer
 template <int WT, int BASE, int HD>
-static __device__ __forceinline__ void consumer(Ctx& c) {
+__device__ __forceinline__ void consumer(Ctx& c) {
     const VmParams& p = *c.p;
     const int q0 = p.queue_off[blockIdx.x], q1 = p.queue_off[blockIdx.x + 1];
     for (int s = 0; s < p.n_steps && !c.abort; ++s) {
@@ -984,6 +893,7 @@ static __device__ __forceinline__ void consumer(Ctx& c) {
             t.rps = __ldg(&tp->rps);
             t.wpr = __ldg(&tp->wpr);
             t.rw = __ldg(&tp->rw);
+            t.w_off = __ldg((const long long*)&tp->w_off);
             t.n_waits = __ldg(&tp->n_waits);
             t.wait_ctr[0] = __ldg(&tp->wait_ctr[0]);
             t.wait_ctr[1] = __ldg(&tp->wait_ctr[1]);
@@ -993,60 +903,18 @@ static __device__ __forceinline__ void consumer(Ctx& c) {
             t.wait_off[1] = __ldg(&tp->wait_off[1]);
             t.signal_ctr = __ldg(&tp->signal_ctr);
             const uint64_t t_start = p.trace ? gtimer() : 0;
-            if (!wait_counters(c, t, tid_, s)) {
-                c.abort = true;
-                break;
-            }
-            const uint64_t t_waited = p.trace ? gtimer() : 0;
-            int tok = 0;
-            if (t.layer == 0 && (t.op == OP_QKV || t.op == OP_O)) {
-                if (c.tid == 0) c.sh->tok = step_token(p, s);
-                bar_consumers();
-                tok = c.sh->tok;
-                if (tok < 0) {
-                    c.abort = true;
-                    break;
-                }
-            }
             float best_v = -3.0e38f;
             int best_i = 0;
             const bool gemv = t.op == OP_QKV || t.op == OP_O || t.op == OP_GU || t.op == OP_DOWN ||
                               (t.op == OP_LM && !p.skip_lm);
+            bool ok;
             if (gemv) {
-                switch (t.op) {
-                    case OP_QKV: {
-                        const uint16_t* gain = (const uint16_t*)(p.w + p.layer_bytes * t.layer + p.l_attn_norm);
-                        const uint16_t* emb = t.layer == 0 ? (const uint16_t*)(p.w + p.embed) + (size_t)tok * p.d : nullptr;
-                        prologue_rmsnorm<BASE>(c, p.x, emb, gain, p.d, p.eps);
-                        break;
-                    }
-                    case OP_GU:
-                        prologue_rmsnorm<BASE>(c, p.x, nullptr,
-                                               (const uint16_t*)(p.w + p.layer_bytes * t.layer + p.l_ffn_norm), p.d, p.eps);
-                        break;
-                    case OP_LM:
-                        prologue_rmsnorm<BASE>(c, p.x, nullptr, (const uint16_t*)(p.w + p.final_norm), p.d, p.eps);
-                        break;
-                    case OP_O: prologue_attention(c); break;
-                    default: break;  // down reads h straight from device memory
-                }
-                if (t.op == OP_DOWN) gemv_task<WT, BASE>(c, t, p.h, true, s, tok, best_v, best_i);
-                else gemv_task<WT, BASE>(c, t, c.xs, false, s, tok, best_v, best_i);
-                if (t.op == OP_LM) {  // per-lane bests -> the warp's key (largest value, lowest index)
-                    unsigned long long key = (key_tag((uint32_t)(p.epoch0 + s)) << 49) |
-                                             ((unsigned long long)float_order(best_v) << KEY_IDX_BITS) |
-                                             (unsigned long long)((1u << KEY_IDX_BITS) - 1u - (uint32_t)best_i);
-#pragma unroll
-                    for (int o = 16; o; o >>= 1) {
-                        const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, key, o);
-                        key = other > key ? other : key;
-                    }
-                    if (c.lane == 0) c.sh->keys[c.warp] = key;
-                }
-            } else if (t.op == OP_ATTN) {
-                attn_task<HD>(c, t, s);
-            } else if (t.op == OP_FIN) {
-                if (c.tid == 0 && !p.skip_lm) {
+                ok = gemv_task<WT, BASE>(c, t, tid_, s, best_v, best_i);
+            } else {
+                ok = wait_counters(c, t, tid_, s);
+                if (ok && t.op == OP_ATTN) {
+                    attn_task<HD>(c, t, s);
+                } else if (ok && t.op == OP_FIN && c.tid == 0 && !p.skip_lm) {
                     const unsigned long long k = __ldcg(p.key);
                     if ((k >> 49) != key_tag((uint32_t)(p.epoch0 + s))) {
                         raise_error(p, DEV_BAD_KEY, (uint32_t)tid_, (uint32_t)s);
@@ -1057,35 +925,41 @@ static __device__ __forceinline__ void consumer(Ctx& c) {
                     }
                 }
             }
+            if (!ok) {  // decided uniformly (after a consumer barrier)
+                c.abort = true;
+                break;
+            }
+            if (gemv && t.op == OP_LM) {  // per-lane bests -> the warp's key (largest value, lowest index)
+                unsigned long long key = (key_tag((uint32_t)(p.epoch0 + s)) << 49) |
+                                         ((unsigned long long)float_order(best_v) << KEY_IDX_BITS) |
+                                         (unsigned long long)((1u << KEY_IDX_BITS) - 1u - (uint32_t)best_i);
+#pragma unroll
+                for (int o = 16; o; o >>= 1) {
+                    const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, key, o);
+                    key = other > key ? other : key;
+                }
+                if (c.lane == 0) c.sh->keys[c.warp] = key;
+            }
             bar_consumers();
-            if (t.op == OP_LM && !p.skip_lm && c.tid == 0 && !c.sh->abort) {
-                // block argmax: largest value, lowest index on ties
+            if (gemv && t.op == OP_LM && c.tid == 0) {
                 unsigned long long key = 0;
                 for (int w = 0; w < NW; ++w) key = c.sh->keys[w] > key ? c.sh->keys[w] : key;
                 atomicMax(p.key, key);
             }
             signal_counter(c, t);
-            if (c.sh->abort) {  // read after the barrier: the same in every consumer thread
-                c.abort = true;
-                break;
-            }
             if (p.trace && c.tid == 0) {
                 const int k = s * (q1 - q0) + (qi - q0);
                 if (k < p.trace_cap) {
                     unsigned long long* r = p.trace + ((size_t)blockIdx.x * p.trace_cap + k) * 8;
                     r[0] = (unsigned long long)tid_ | ((unsigned long long)s << 32);
                     r[1] = t_start;
-                    r[2] = t_waited;
+                    r[2] = c.sh->t_waited;
                     r[3] = gtimer();
-                    r[4] = c.sh->full_wait_ns;
-                    r[5] = c.slot_seq;
-                    r[6] = *(volatile unsigned long long*)&c.sh->prod_wait_ns;
-                    r[7] = 0;
+                    r[4] = r[5] = r[6] = r[7] = 0;
                 }
             }
         }
     }
-    if (c.tid == 0) c.sh->consumed = c.slot_seq;
 }
 
 template <int WT, int BASE, int HD>
@@ -1093,45 +967,25 @@ __global__ void __launch_bounds__(THREADS, 1) vm_kernel(const VmParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     Ctx c;
     c.p = &p;
-    c.ring = smem_raw;
-    c.xs = (float*)(smem_raw + (size_t)p.n_slots * p.slot_bytes);
-    c.sh = (Shared*)(smem_raw + (size_t)p.n_slots * p.slot_bytes + (size_t)p.xs_floats * 4);
     c.tid = threadIdx.x;
     c.lane = threadIdx.x & 31;
     c.warp = threadIdx.x >> 5;
-    c.slot_seq = 0;
-    c.slot_i = 0;
-    c.slot_phase = 0;
+    c.xs = (float*)smem_raw;
+    c.sh = (Shared*)(smem_raw + (size_t)p.xs_floats * 4);
+    c.ring = smem_raw + ring_offset(p.xs_floats) + (size_t)c.warp * ring_slots<WT>() * ring_slot_bytes<WT>();
+    c.rstd = 1.f;
     c.abort = false;
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < p.n_slots; ++i) {
-            mbar_init(full_bar(c, i), 1);
-            mbar_init(empty_bar(c, i), NW);  // one arrival per consumer warp
-        }
-        c.sh->abort = 0;
-        c.sh->prod_wait_ns = 0;
-        c.sh->full_wait_ns = 0;
-        c.sh->issued = 0;
-        c.sh->consumed = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
+    c.rs = 0;
+    const int q0 = p.queue_off[blockIdx.x], q1 = p.queue_off[blockIdx.x + 1];
+    c.ws = WarpStream{0, q0, 0, 0, 1, 0, 0, 0, 0, 0, 32, 0, 0, nullptr, 0, false};
+    if (threadIdx.x == 0) c.sh->abort = 0;
+    for (int i = c.lane; i < ring_slots<WT>() * ring_slot_bytes<WT>() / 16; i += 32)  // no stale NaN bit patterns
+        ((uint4*)c.ring)[i] = make_uint4(0, 0, 0, 0);
+    __syncwarp();
+    for (int i = 0; i < ring_slots<WT>() - 1; ++i) stream_issue<WT>(p, q0, q1, c.warp, c.lane, c.ring, c.ws);
     __syncthreads();
-    if (c.warp == NW) producer(c);
-    else consumer<WT, BASE, HD>(c);
-    __syncthreads();
-    // Exit drain: after an abort the producer may have copies in flight into
-    // slots nobody consumed; wait (bounded) for them before the CTA exits.
-    if (threadIdx.x == 0) {
-        const uint32_t issued = c.sh->issued, consumed = c.sh->consumed;
-        for (uint32_t s = consumed; s < issued; ++s) {
-            const int i = (int)(s % (uint32_t)p.n_slots);
-            const uint32_t par = (s / (uint32_t)p.n_slots) & 1u;
-            const uint64_t t0 = gtimer();
-            while (!mbar_try_wait(full_bar(c, i), par) && gtimer() - t0 < (uint64_t)p.watchdog_ns) {
-            }
-        }
-    }
+    consumer<WT, BASE, HD>(c);
+    cp_async_wait<0>();  // no copy may land in shared memory after the CTA exits
 }
-
 
 }  // namespace mk

@@ -87,13 +87,11 @@ typedef struct {
 /* Structural knobs of the lowering (AutoMegaKernel "ScheduleConfig": tiling,
  * SM assignment, pipelining depth).  0 selects the default. */
 typedef struct {
-    int32_t sms;         /* CTAs (= SMs used); default all SMs of the device              */
-    int32_t slot_bytes;  /* weight ring slot size in bytes, multiple of 1024; 32768        */
-    int32_t n_slots;     /* weight ring depth (pipelining depth); default fills smem       */
-    int32_t attn_chunks; /* split-KV chunks per KV head; default from max_seq and sms     */
-    int32_t watchdog_ms; /* a device wait gives up after this long; default 1000          */
-    int32_t l2_ahead_kb; /* weight KiB per CTA prefetched into L2 ahead of the ring;
-                            default 0 (off)                                             */
+    int32_t sms;            /* CTAs (= SMs used); default all SMs of the device              */
+    int32_t rows_in_flight; /* weight rows each warp group keeps loading ahead; 2 (the only  
+                               value built)                                               */
+    int32_t attn_chunks;    /* split-KV chunks per KV head; default from max_seq and sms     */
+    int32_t watchdog_ms;    /* a device wait gives up after this long; default 1000          */
 } mk_schedule_config;
 
 /* ------------------------------------------------------------------ packing
@@ -261,9 +259,9 @@ mk_status mk_get_state(const mk_handle* h, int32_t* pos, int32_t* pending);
 mk_status mk_set_state(mk_handle* h, int32_t pos, int32_t pending);
 
 /* Launch geometry chosen at mk_create: CTAs, threads per CTA, dynamic shared
- * memory bytes, ring slots, tasks in the schedule. */
+ * memory bytes, rows in flight per warp group, tasks in the schedule. */
 mk_status mk_get_launch_info(const mk_handle* h, int32_t* ctas, int32_t* threads,
-                             int32_t* smem_bytes, int32_t* n_slots, int32_t* n_tasks);
+                             int32_t* smem_bytes, int32_t* rows_in_flight, int32_t* n_tasks);
 
 /* Kernel launches issued by this handle so far (one per prefill/decode call). */
 int64_t mk_launch_count(const mk_handle* h);
