@@ -24,6 +24,7 @@ MK_FLAG_PROJ_BIAS, MK_FLAG_TIED_HEAD, MK_FLAG_ROPE_SCALING = 1, 2, 4
 MK_ACC_READ, MK_ACC_WRITE, MK_ACC_ATOMIC = 1, 2, 3
 MK_BUF_OUTPUT = 1
 MK_IR_MAX_WAITS = 2
+MK_STATIC_SCRATCH_BYTES = 8 << 20
 OPS = {1: "qkv", 2: "attn", 3: "o", 4: "gu", 5: "down", 6: "lm", 7: "fin"}
 WDTYPES = {"bf16": MK_W_BF16, "fp16": MK_W_FP16, "int8": MK_W_INT8_ROW, "int4": MK_W_INT4_G128}
 STATUS_NAMES = {0: "MK_OK", 1: "MK_ERR_INVALID_ARG", 2: "MK_ERR_UNSUPPORTED", 3: "MK_ERR_SCHEDULE_INVALID",
@@ -98,6 +99,7 @@ SIGNATURES = {
     "mk_launch_count": (_I64, [_P]),
     "mk_last_error": (ctypes.c_char_p, [_P]),
     "mk_destroy": (None, [_P]),
+    "mk_decode_static": (_I32, [_DESC, _CFG, _P, _SZ, _P, _SZ, _I32, _I32, _I32, _P, _P, _P]),
     "mk_debug_dequant": (_I32, [_DESC, _P, _I32, _I32, _P, _P]),
     "mk_debug_set_trace": (_I32, [_P, _P, _I32]),
     "mk_debug_watchdog": (_I32, [_I32, _P, _P]),
@@ -375,6 +377,21 @@ class Decoder:
         self.decode_async(n, forced=f, out_ids=ids, logits=lg)
         self.finish()
         return lg.cpu().numpy(), ids.cpu().numpy()
+
+
+def decode_static(desc, weights, kv, pos, token, n_steps, cfg=None, logits=None, stream=None, out=None):
+    """``mk_decode_static``: greedy decode from (pos, token) into the caller's
+    KV cache with the library's static device scratch (no allocation on the
+    device).  weights/kv/logits are caller-owned device tensors; returns the
+    int32 ids (numpy, host)."""
+    import torch
+    out = np.empty(n_steps, np.int32) if out is None else out
+    st = stream or torch.cuda.current_stream()
+    _check(load().mk_decode_static(ctypes.byref(desc), ctypes.byref(cfg) if cfg else None, weights.data_ptr(),
+                                   weights.numel() * weights.element_size(), kv.data_ptr(),
+                                   kv.numel() * kv.element_size(), pos, token, n_steps, out.ctypes.data,
+                                   logits.data_ptr() if logits is not None else None, _P(st.cuda_stream)))
+    return out
 
 
 def debug_dequant(desc, weights_dev, tensor, layer, rows, cols, stream=None):

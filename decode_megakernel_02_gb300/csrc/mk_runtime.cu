@@ -12,6 +12,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -23,6 +24,7 @@ size_t vm_shared_bytes(int wdtype, int xs_floats);
 cudaError_t launch_dequant(int wdtype, const uint8_t* rows, int64_t stride, int first, int step, int nrows,
                            int K, float* out, cudaStream_t st);
 cudaError_t launch_watchdog(uint32_t* ctr, uint32_t* status, int64_t limit_ns, cudaStream_t st);
+cudaError_t static_scratch_address(void** ptr);
 }  // namespace mk
 
 using namespace mk;
@@ -402,6 +404,204 @@ int64_t mk_launch_count(const mk_handle* h) { return h ? h->launches : 0; }
 const char* mk_last_error(const mk_handle* h) { return h ? h->err.c_str() : thread_error(); }
 
 void mk_destroy(mk_handle* h) { delete h; }
+
+}  // extern "C"
+
+namespace {
+
+// Per-device state of mk_decode_static: the scratch array's address and the
+// schedule currently uploaded into it.
+struct StaticSlot {
+    uint8_t* base = nullptr;  // set once per device
+    bool ready = false;       // tables below match the uploaded schedule
+    mk_model_desc d{};
+    Config c{};
+    WsLayout ws{};
+    int32_t n_tasks = 0, n_counters = 0;
+    const void* kfn = nullptr;
+    size_t smem = 0;
+    int32_t xs_floats = 0;
+};
+constexpr int MAX_STATIC_DEVICES = 64;
+std::mutex g_static_mu;
+StaticSlot g_static[MAX_STATIC_DEVICES];
+
+bool same_config(const Config& a, const Config& b) {
+    return a.sms == b.sms && a.rw == b.rw && a.C == b.C && a.watchdog_ns == b.watchdog_ns;
+}
+
+// Lower, validate and upload the schedule for (desc, c) into the slot's scratch.
+mk_status static_setup(StaticSlot& s, const mk_model_desc* desc, const Config& c, int n_sms, int smem_optin,
+                       cudaStream_t stream) {
+    s.ready = false;
+    Lowering lw;
+    mk_status st = lower(desc, c, &lw);
+    if (st) return st;
+    const WsLayout ws = ws_layout(desc, c, (int64_t)lw.tasks.size(), lw.n_counters);
+    if ((uint64_t)ws.total > (uint64_t)MK_STATIC_SCRATCH_BYTES) {
+        set_error("this model needs %lld bytes of scratch; the static scratch holds %u (MK_STATIC_SCRATCH_BYTES)",
+                  (long long)ws.total, (unsigned)MK_STATIC_SCRATCH_BYTES);
+        return MK_ERR_CAPACITY;
+    }
+    {
+        mk_ir* ir = to_ir(lw, c.sms);
+        std::string why;
+        st = validate_ir(ir, &why);
+        mk_free_ir(ir);
+        if (st) {
+            set_error("schedule rejected before launch: %s", why.c_str());
+            return MK_ERR_SCHEDULE_INVALID;
+        }
+    }
+    const int xs_floats = std::max(desc->d_model, desc->n_q_heads * desc->head_dim);
+    const size_t smem = vm_shared_bytes(desc->wdtype, xs_floats);
+    const void* kfn = vm_kernel_for(desc->wdtype, desc->base_dtype, desc->head_dim);
+    if (!kfn) {
+        set_error("no kernel for wdtype %d / base %d", desc->wdtype, desc->base_dtype);
+        return MK_ERR_UNSUPPORTED;
+    }
+    if (smem > (size_t)smem_optin) {
+        set_error("shared memory need %zu > %d", smem, smem_optin);
+        return MK_ERR_UNSUPPORTED;
+    }
+    cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    int per_sm = 0;
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kfn, THREADS, smem);
+    if (e != cudaSuccess) {
+        set_error("kernel set-up: %s", cudaGetErrorString(e));
+        return MK_ERR_CUDA;
+    }
+    if (per_sm < 1 || (int64_t)per_sm * n_sms < c.sms) {
+        set_error("%d CTAs cannot be co-resident (%d per SM)", c.sms, per_sm);
+        return MK_ERR_UNSUPPORTED;
+    }
+    std::vector<int32_t> queue, qoff(c.sms + 1);
+    for (int q = 0; q < c.sms; ++q) {
+        qoff[q] = (int32_t)queue.size();
+        for (int id : lw.queues[q]) queue.push_back(id);
+    }
+    qoff[c.sms] = (int32_t)queue.size();
+    std::vector<float> inv(desc->head_dim / 2);
+    for (int i = 0; i < desc->head_dim / 2; ++i)
+        inv[i] = (float)std::pow((double)desc->rope_theta, -2.0 * i / (double)desc->head_dim);
+    e = cudaMemcpyAsync(s.base + ws.tasks, lw.dev.data(), lw.dev.size() * sizeof(DevTask), cudaMemcpyHostToDevice,
+                        stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(s.base + ws.queue, queue.data(), queue.size() * 4, cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(s.base + ws.queue_off, qoff.data(), qoff.size() * 4, cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(s.base + ws.inv_freq, inv.data(), inv.size() * 4, cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);  // the host vectors die on return
+    if (e != cudaSuccess) {
+        set_error("uploading the schedule: %s", cudaGetErrorString(e));
+        return MK_ERR_CUDA;
+    }
+    s.d = *desc;
+    s.c = c;
+    s.ws = ws;
+    s.n_tasks = (int32_t)lw.tasks.size();
+    s.n_counters = lw.n_counters;
+    s.kfn = kfn;
+    s.smem = smem;
+    s.xs_floats = xs_floats;
+    s.ready = true;
+    return MK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mk_status mk_decode_static(const mk_model_desc* desc, const mk_schedule_config* cfg, const void* weights_dev,
+                           size_t weights_bytes, void* kv_dev, size_t kv_bytes, int32_t pos, int32_t token,
+                           int32_t n_steps, int32_t* out_ids_host, float* logits_dev, mk_stream_t stream) {
+    mk_status st = check_desc(desc);
+    if (st) return st;
+    if (!weights_dev || !kv_dev || !out_ids_host) {
+        set_error("NULL argument");
+        return MK_ERR_INVALID_ARG;
+    }
+    if (((uintptr_t)weights_dev & 255) || ((uintptr_t)kv_dev & 15)) {
+        set_error("misaligned buffer: weights need 256-byte, the KV cache 16-byte alignment");
+        return MK_ERR_INVALID_ARG;
+    }
+    if (token < 0 || token >= desc->vocab) {
+        set_error("token %d out of range", token);
+        return MK_ERR_INVALID_ARG;
+    }
+    if (pos < 0 || n_steps < 1 || n_steps >= KEY_TAG_MAX - 1) {
+        set_error("pos %d / n_steps %d out of range", pos, n_steps);
+        return MK_ERR_INVALID_ARG;
+    }
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    int dev = 0, n_sms = 0, smem_optin = 0, coop = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+    if (e != cudaSuccess) {
+        set_error("CUDA device query failed: %s", cudaGetErrorString(e));
+        return MK_ERR_CUDA;
+    }
+    if (!coop || dev >= MAX_STATIC_DEVICES) {
+        set_error("device %d: no cooperative launch or index above %d", dev, MAX_STATIC_DEVICES - 1);
+        return MK_ERR_UNSUPPORTED;
+    }
+    StaticSlot& s = g_static[dev];
+    if (!s.base) {
+        void* p = nullptr;
+        e = static_scratch_address(&p);
+        if (e != cudaSuccess || !p) {
+            set_error("cudaGetSymbolAddress of the static scratch: %s", cudaGetErrorString(e));
+            return MK_ERR_CUDA;
+        }
+        s.base = (uint8_t*)p;
+    }
+    Config c;
+    if ((st = resolve_config(desc, cfg, n_sms, &c))) return st;
+    const cudaStream_t cs = (cudaStream_t)stream;
+    if (!s.ready || std::memcmp(&s.d, desc, sizeof s.d) != 0 || !same_config(s.c, c)) {
+        if ((st = static_setup(s, desc, c, n_sms, smem_optin, cs))) return st;
+    }
+    size_t need_w = 0, need_kv = 0;
+    mk_packed_size(desc, &need_w);
+    mk_kv_cache_size(desc, &need_kv);
+    if (weights_bytes < need_w || kv_bytes < need_kv) {
+        set_error("buffer too small: weights %zu/%zu, kv %zu/%zu", weights_bytes, need_w, kv_bytes, need_kv);
+        return MK_ERR_CAPACITY;
+    }
+    if ((int64_t)pos + n_steps > desc->max_seq) {
+        set_error("pos %d + %d steps > max_seq %d", pos, n_steps, desc->max_seq);
+        return MK_ERR_CAPACITY;
+    }
+    // A handle on the stack over the static scratch: nothing is allocated.
+    mk_handle h;
+    h.d = *desc;
+    h.c = c;
+    h.ws = s.ws;
+    h.bl = blob_layout(desc);
+    h.n_tasks = s.n_tasks;
+    h.n_counters = s.n_counters;
+    h.w = (const uint8_t*)weights_dev;
+    h.kv = (uint16_t*)kv_dev;
+    h.wsp = s.base;
+    h.st = cs;
+    h.device = dev;
+    h.kfn = s.kfn;
+    h.smem = s.smem;
+    h.xs_floats = s.xs_floats;
+    h.pos = pos;
+    h.pending = token;
+    h.has_seq = true;
+    // status words, sync counters and the argmax key must start at zero
+    if ((st = reset_sync_state(&h))) return st;
+    int32_t* ids_dev = (int32_t*)(s.base + s.ws.out_ids);
+    if ((st = launch(&h, n_steps, nullptr, ids_dev, logits_dev, 0))) return st;
+    e = cudaMemcpyAsync(out_ids_host, ids_dev, (size_t)n_steps * 4, cudaMemcpyDeviceToHost, cs);
+    if (e != cudaSuccess) {
+        set_error("reading the ids: %s", cudaGetErrorString(e));
+        return MK_ERR_CUDA;
+    }
+    return read_status(&h);
+}
 
 mk_status mk_debug_dequant(const mk_model_desc* desc, const void* weights_dev, int32_t tensor, int32_t layer,
                            float* out_dev, mk_stream_t stream) {

@@ -269,6 +269,44 @@ int64_t mk_launch_count(const mk_handle* h);
 const char* mk_last_error(const mk_handle* h);
 void mk_destroy(mk_handle* h);
 
+/* ------------------------------------------------------------------ allocation-free decode */
+/* Largest scratch mk_decode_static accepts (8 MiB; a Llama-3-8B layout with an
+ * 8k context needs about 2.5 MiB). */
+#define MK_STATIC_SCRATCH_BYTES (8u << 20)
+
+/* Greedy decode of n_steps tokens from position pos feeding `token`, without a
+ * handle or a caller workspace.  The design sources have no counterpart: this
+ * is an extra entry point of this library for callers that may not allocate.
+ * It runs the same kernel and schedule as mk_create + mk_decode, but the
+ * kernel's scratch (schedule tables, sync counters, activations, split-KV
+ * partials, token ids) lives in one file-scope device array of
+ * MK_STATIC_SCRATCH_BYTES per device; no device memory is allocated.
+ *
+ * weights_dev: packed blob (mk_packed_size bytes, 256-byte aligned).
+ * kv_dev: KV cache (mk_kv_cache_size bytes, 16-byte aligned) whose positions
+ *   0..pos-1 already hold the sequence (e.g. written by a handle's mk_prefill);
+ *   positions pos..pos+n_steps-1 are written.
+ * out_ids_host: int32 [n_steps], the argmax ids (lowest index on ties).
+ * logits_dev (nullable): float32 [n_steps][vocab].
+ * Synchronous on `stream`.
+ *
+ * Set-up: the first call on a device looks up the array's address (once per
+ * device) and, like every call whose desc or resolved config differs from the
+ * previous call's on that device, lowers, validates and uploads the schedule;
+ * make that first call before any stream capture.  Every call zeroes the
+ * status words, sync counters and argmax key before its launch; all other
+ * scratch is written before it is read.
+ * Calls share the one array per device: calls that overlap (other host
+ * threads, other streams) race on it.  Calls of this library are serialised
+ * by a host lock, and each returns only after its launch has finished.
+ * Errors: INVALID_ARG, UNSUPPORTED, CAPACITY (scratch above
+ * MK_STATIC_SCRATCH_BYTES, checked first; then buffers too small or
+ * pos + n_steps > max_seq), SCHEDULE_INVALID, CUDA, TIMEOUT, DEVICE. */
+mk_status mk_decode_static(const mk_model_desc* desc, const mk_schedule_config* cfg,
+                           const void* weights_dev, size_t weights_bytes, void* kv_dev,
+                           size_t kv_bytes, int32_t pos, int32_t token, int32_t n_steps,
+                           int32_t* out_ids_host, float* logits_dev, mk_stream_t stream);
+
 /* ------------------------------------------------------------------ test support */
 /* Dequantise one packed GEMV tensor on the device with the same device
  * function the decode kernel uses: out_dev float32 [rows][cols] row-major.
