@@ -174,12 +174,13 @@ def main():
     ap.add_argument("--sms", type=int, default=0)
     ap.add_argument("--rows-in-flight", type=int, default=0)
     ap.add_argument("--chunks", type=int, default=0)
+    ap.add_argument("--tokens", type=int, default=0, help="decode tokens per step (default: the workload's)")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     w = synthetic.get_workload(args.workload)
-    n_tok = w.decode_steps
+    n_tok = args.tokens or w.decode_steps
     pos0 = w.prompt_len - 1
     config = {"workload": w.name, "prompt_len": w.prompt_len, "decode_tokens": n_tok, "batch": 1,
               "weights": w.wdtype, "l2": "inputs larger than L2 (weights streamed every token)",

@@ -42,6 +42,11 @@ struct Lowering {
 };
 mk_status lower(const mk_model_desc* d, const Config& c, Lowering* out);
 
+// The device tables of a lowering: records in queue order and queue offsets.
+// Fails (INVALID_ARG) if a field does not fit its record width.
+mk_status device_tables(const Lowering& lw, int n_sms, std::vector<TaskRec>* recs, std::vector<int32_t>* queue,
+                        std::vector<int32_t>* queue_off, int32_t* tab_cap);
+
 // Flatten a lowering into a library-owned mk_ir.
 mk_ir* to_ir(const Lowering& lw, int n_sms);
 
@@ -50,7 +55,7 @@ mk_status validate_ir(const mk_ir* ir, std::string* why);
 
 // Workspace layout (byte offsets).
 struct WsLayout {
-    int64_t status, counters, key, tasks, queue, queue_off, inv_freq, x, qkv, part_ml, part_acc,
+    int64_t status, counters, key, recs, queue_off, inv_freq, x, qkv, part_ml, part_acc,
         h, tok, out_ids, total;
 };
 WsLayout ws_layout(const mk_model_desc* d, const Config& c, int64_t n_tasks, int32_t n_counters);

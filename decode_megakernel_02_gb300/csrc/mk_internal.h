@@ -54,6 +54,23 @@ struct DevTask {
 };
 static_assert(sizeof(DevTask) == 80, "DevTask layout");
 
+// The device's compact copy of a DevTask.  Each CTA keeps the records of its
+// own queue (in queue order) in shared memory for the whole launch.
+struct TaskRec {
+    uint8_t op, n_waits;
+    uint16_t layer;
+    int32_t row0, nrows;    // as in DevTask
+    uint32_t w_off16;       // GEMV: blob offset of row0 / 16
+    uint16_t row_bytes16;   // GEMV: packed row stride / 16
+    uint16_t K;             // GEMV: reduction length.  ATTN: chunks per head
+    uint16_t wait_ctr[2];
+    uint16_t wait_cnt[2];
+    int16_t signal_ctr;     // -1: none
+    uint8_t wpr;
+    uint8_t wait_prev;      // bit i: wait i targets the previous step (epoch offset -1)
+};
+static_assert(sizeof(TaskRec) == 32, "TaskRec layout");
+
 // Byte offsets of the packed weight blob.
 struct BlobLayout {
     int64_t row_qkv, row_o, row_gu, row_down, row_lm;   // row strides
@@ -67,12 +84,11 @@ struct BlobLayout {
 struct VmParams {
     const uint8_t* w;          // packed blob
     uint16_t* kv;              // bf16 KV cache [L][2][Hkv][max_seq][hd]
-    uint32_t* status;          // [0] status, [1] task id, [2] detail, [3] last token
+    uint32_t* status;          // [0] status, [1] queue index, [2] detail, [3] last token
     uint32_t* counters;        // n_counters lines of CTR_STRIDE words
     unsigned long long* key;   // the step's packed argmax key
-    const DevTask* tasks;
-    const int32_t* queue;
-    const int32_t* queue_off;  // [n_sms + 1]
+    const TaskRec* recs;       // every CTA's queue, concatenated in queue order
+    const int32_t* queue_off;  // [n_sms + 1]: CTA b owns recs[queue_off[b] .. queue_off[b+1])
     const float* inv_freq;     // [hd/2]
     float* x;                  // residual stream [d]
     float* qkv;                // [q_dim + 2 kv_dim]
@@ -90,6 +106,7 @@ struct VmParams {
     int32_t n_steps, pos0, epoch0, skip_lm;
     int32_t pending;           // token fed at step 0 (no forcing); -1: status[3]
     int32_t xs_floats;         // shared-memory input vector capacity: max(d, q_dim)
+    int32_t tab_cap;           // task records a CTA's shared-memory table holds (longest queue)
     int64_t watchdog_ns;
     unsigned long long* trace; // nullable: per-task timestamps [ctas][trace_cap][4]
     int32_t trace_cap;

@@ -20,7 +20,7 @@
 
 namespace mk {
 const void* vm_kernel_for(int wdtype, int base, int hd);
-size_t vm_shared_bytes(int wdtype, int xs_floats);
+size_t vm_shared_bytes(int wdtype, int xs_floats, int tab_cap);
 cudaError_t launch_dequant(int wdtype, const uint8_t* rows, int64_t stride, int first, int step, int nrows,
                            int K, float* out, cudaStream_t st);
 cudaError_t launch_watchdog(uint32_t* ctr, uint32_t* status, int64_t limit_ns, cudaStream_t st);
@@ -48,6 +48,9 @@ struct mk_handle {
     bool dirty = false;
     int64_t launches = 0;
     int32_t xs_floats = 0;
+    int32_t tab_cap = 0;                 // longest per-CTA queue (shared-memory task table)
+    const int32_t* queue = nullptr;      // task id of each queue index (host copy, for errors)
+    std::vector<int32_t> queue_store;    // owns `queue` for handles made by mk_create
     unsigned long long* trace = nullptr;
     int32_t trace_cap = 0;
     std::string err;
@@ -97,8 +100,7 @@ mk_status launch(mk_handle* h, int n_steps, const int32_t* forced, int32_t* out_
     p.status = (uint32_t*)(h->wsp + h->ws.status);
     p.counters = (uint32_t*)(h->wsp + h->ws.counters);
     p.key = (unsigned long long*)(h->wsp + h->ws.key);
-    p.tasks = (const DevTask*)(h->wsp + h->ws.tasks);
-    p.queue = (const int32_t*)(h->wsp + h->ws.queue);
+    p.recs = (const TaskRec*)(h->wsp + h->ws.recs);
     p.queue_off = (const int32_t*)(h->wsp + h->ws.queue_off);
     p.inv_freq = (const float*)(h->wsp + h->ws.inv_freq);
     p.x = (float*)(h->wsp + h->ws.x);
@@ -135,6 +137,7 @@ mk_status launch(mk_handle* h, int n_steps, const int32_t* forced, int32_t* out_
     p.skip_lm = skip_lm;
     p.pending = h->pending;
     p.xs_floats = h->xs_floats;
+    p.tab_cap = h->tab_cap;
     p.watchdog_ns = h->c.watchdog_ns;
     p.trace = h->trace;
     p.trace_cap = h->trace_cap;
@@ -151,10 +154,11 @@ mk_status read_status(mk_handle* h) {
     CK(h, cudaStreamSynchronize(h->st));
     if (s[0] == DEV_OK) return MK_OK;
     h->dirty = true;
+    const int task = h->queue && s[1] < (uint32_t)h->n_tasks ? h->queue[s[1]] : -1;
     if (s[0] == DEV_TIMEOUT)
-        return herr(h, MK_ERR_TIMEOUT, "device wait gave up (task %u, detail %u); counters are reset on the next launch",
-                    s[1], s[2]);
-    return herr(h, MK_ERR_DEVICE, "device reported error %u (task 0x%x, step %u)", s[0], s[1], s[2]);
+        return herr(h, MK_ERR_TIMEOUT, "device wait gave up (task %d, step %u); counters are reset on the next launch",
+                    task, s[2]);
+    return herr(h, MK_ERR_DEVICE, "device reported error %u (task %d, step %u)", s[0], task, s[2]);
 }
 
 }  // namespace
@@ -216,12 +220,17 @@ mk_status mk_create(const mk_model_desc* desc, const mk_schedule_config* cfg, co
     Config c;
     if ((st = resolve_config(desc, cfg, n_sms, &c))) return st;
     const int xs_floats = std::max(desc->d_model, desc->n_q_heads * desc->head_dim);
-    if (vm_shared_bytes(desc->wdtype, xs_floats) > (size_t)smem_optin) {
-        set_error("shared memory need %zu > %d", vm_shared_bytes(desc->wdtype, xs_floats), smem_optin);
-        return MK_ERR_UNSUPPORTED;
-    }
     Lowering lw;
     if ((st = lower(desc, c, &lw))) return st;
+    std::vector<TaskRec> recs;
+    std::vector<int32_t> queue, qoff;
+    int32_t tab_cap = 0;
+    if ((st = device_tables(lw, c.sms, &recs, &queue, &qoff, &tab_cap))) return st;
+    if (vm_shared_bytes(desc->wdtype, xs_floats, tab_cap) > (size_t)smem_optin) {
+        set_error("shared memory need %zu > %d (%d tasks per CTA)", vm_shared_bytes(desc->wdtype, xs_floats, tab_cap),
+                  smem_optin, tab_cap);
+        return MK_ERR_UNSUPPORTED;
+    }
     {
         mk_ir* ir = to_ir(lw, c.sms);
         std::string why;
@@ -254,8 +263,11 @@ mk_status mk_create(const mk_model_desc* desc, const mk_schedule_config* cfg, co
     h->st = (cudaStream_t)stream;
     h->device = dev;
     h->kfn = vm_kernel_for(desc->wdtype, desc->base_dtype, desc->head_dim);
-    h->smem = vm_shared_bytes(desc->wdtype, xs_floats);
+    h->smem = vm_shared_bytes(desc->wdtype, xs_floats, tab_cap);
     h->xs_floats = xs_floats;
+    h->tab_cap = tab_cap;
+    h->queue_store = queue;
+    h->queue = h->queue_store.data();
     if (!h->kfn) {
         delete h;
         set_error("no kernel for wdtype %d / base %d", desc->wdtype, desc->base_dtype);
@@ -274,18 +286,11 @@ mk_status mk_create(const mk_model_desc* desc, const mk_schedule_config* cfg, co
     if (per_sm < 1 || (int64_t)per_sm * n_sms < c.sms)
         return fail(herr(h, MK_ERR_UNSUPPORTED, "%d CTAs cannot be co-resident (%d per SM)", c.sms, per_sm));
 
-    // device tables: tasks, queues, RoPE inverse frequencies
-    std::vector<int32_t> queue, qoff(c.sms + 1);
-    for (int s = 0; s < c.sms; ++s) {
-        qoff[s] = (int32_t)queue.size();
-        for (int id : lw.queues[s]) queue.push_back(id);
-    }
-    qoff[c.sms] = (int32_t)queue.size();
+    // device tables: task records, queue offsets, RoPE inverse frequencies
     std::vector<float> inv(desc->head_dim / 2);
     for (int i = 0; i < desc->head_dim / 2; ++i)
         inv[i] = (float)std::pow((double)desc->rope_theta, -2.0 * i / (double)desc->head_dim);
-    e = cudaMemcpyAsync(h->wsp + ws.tasks, lw.dev.data(), lw.dev.size() * sizeof(DevTask), cudaMemcpyHostToDevice, h->st);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(h->wsp + ws.queue, queue.data(), queue.size() * 4, cudaMemcpyHostToDevice, h->st);
+    e = cudaMemcpyAsync(h->wsp + ws.recs, recs.data(), recs.size() * sizeof(TaskRec), cudaMemcpyHostToDevice, h->st);
     if (e == cudaSuccess) e = cudaMemcpyAsync(h->wsp + ws.queue_off, qoff.data(), qoff.size() * 4, cudaMemcpyHostToDevice, h->st);
     if (e == cudaSuccess) e = cudaMemcpyAsync(h->wsp + ws.inv_freq, inv.data(), inv.size() * 4, cudaMemcpyHostToDevice, h->st);
     if (e != cudaSuccess) return fail(cuda_fail(h, e, "uploading the schedule"));
@@ -420,7 +425,8 @@ struct StaticSlot {
     int32_t n_tasks = 0, n_counters = 0;
     const void* kfn = nullptr;
     size_t smem = 0;
-    int32_t xs_floats = 0;
+    int32_t xs_floats = 0, tab_cap = 0;
+    std::vector<int32_t> queue;
 };
 constexpr int MAX_STATIC_DEVICES = 64;
 std::mutex g_static_mu;
@@ -453,8 +459,12 @@ mk_status static_setup(StaticSlot& s, const mk_model_desc* desc, const Config& c
             return MK_ERR_SCHEDULE_INVALID;
         }
     }
+    std::vector<TaskRec> recs;
+    std::vector<int32_t> queue, qoff;
+    int32_t tab_cap = 0;
+    if ((st = device_tables(lw, c.sms, &recs, &queue, &qoff, &tab_cap))) return st;
     const int xs_floats = std::max(desc->d_model, desc->n_q_heads * desc->head_dim);
-    const size_t smem = vm_shared_bytes(desc->wdtype, xs_floats);
+    const size_t smem = vm_shared_bytes(desc->wdtype, xs_floats, tab_cap);
     const void* kfn = vm_kernel_for(desc->wdtype, desc->base_dtype, desc->head_dim);
     if (!kfn) {
         set_error("no kernel for wdtype %d / base %d", desc->wdtype, desc->base_dtype);
@@ -475,18 +485,10 @@ mk_status static_setup(StaticSlot& s, const mk_model_desc* desc, const Config& c
         set_error("%d CTAs cannot be co-resident (%d per SM)", c.sms, per_sm);
         return MK_ERR_UNSUPPORTED;
     }
-    std::vector<int32_t> queue, qoff(c.sms + 1);
-    for (int q = 0; q < c.sms; ++q) {
-        qoff[q] = (int32_t)queue.size();
-        for (int id : lw.queues[q]) queue.push_back(id);
-    }
-    qoff[c.sms] = (int32_t)queue.size();
     std::vector<float> inv(desc->head_dim / 2);
     for (int i = 0; i < desc->head_dim / 2; ++i)
         inv[i] = (float)std::pow((double)desc->rope_theta, -2.0 * i / (double)desc->head_dim);
-    e = cudaMemcpyAsync(s.base + ws.tasks, lw.dev.data(), lw.dev.size() * sizeof(DevTask), cudaMemcpyHostToDevice,
-                        stream);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(s.base + ws.queue, queue.data(), queue.size() * 4, cudaMemcpyHostToDevice, stream);
+    e = cudaMemcpyAsync(s.base + ws.recs, recs.data(), recs.size() * sizeof(TaskRec), cudaMemcpyHostToDevice, stream);
     if (e == cudaSuccess) e = cudaMemcpyAsync(s.base + ws.queue_off, qoff.data(), qoff.size() * 4, cudaMemcpyHostToDevice, stream);
     if (e == cudaSuccess) e = cudaMemcpyAsync(s.base + ws.inv_freq, inv.data(), inv.size() * 4, cudaMemcpyHostToDevice, stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(stream);  // the host vectors die on return
@@ -502,6 +504,8 @@ mk_status static_setup(StaticSlot& s, const mk_model_desc* desc, const Config& c
     s.kfn = kfn;
     s.smem = smem;
     s.xs_floats = xs_floats;
+    s.tab_cap = tab_cap;
+    s.queue = std::move(queue);
     s.ready = true;
     return MK_OK;
 }
@@ -588,6 +592,8 @@ mk_status mk_decode_static(const mk_model_desc* desc, const mk_schedule_config* 
     h.kfn = s.kfn;
     h.smem = s.smem;
     h.xs_floats = s.xs_floats;
+    h.tab_cap = s.tab_cap;
+    h.queue = s.queue.data();
     h.pos = pos;
     h.pending = token;
     h.has_seq = true;

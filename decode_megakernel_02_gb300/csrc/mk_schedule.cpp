@@ -314,6 +314,54 @@ mk_status lower(const mk_model_desc* d, const Config& c, Lowering* lw) {
     return MK_OK;
 }
 
+mk_status device_tables(const Lowering& lw, int n_sms, std::vector<TaskRec>* recs, std::vector<int32_t>* queue,
+                        std::vector<int32_t>* queue_off, int32_t* tab_cap) {
+    recs->clear();
+    queue->clear();
+    queue_off->assign(n_sms + 1, 0);
+    *tab_cap = 0;
+    for (int s = 0; s < n_sms; ++s) {
+        (*queue_off)[s] = (int32_t)queue->size();
+        if (s < (int)lw.queues.size()) {
+            *tab_cap = std::max(*tab_cap, (int32_t)lw.queues[s].size());
+            for (int id : lw.queues[s]) queue->push_back(id);
+        }
+    }
+    (*queue_off)[n_sms] = (int32_t)queue->size();
+    for (int id : *queue) {
+        const DevTask& t = lw.dev[id];
+        TaskRec r{};
+        bool fits = t.op >= 0 && t.op < 256 && t.layer >= 0 && t.layer < 65536 && t.n_waits >= 0 && t.n_waits <= 2 &&
+                    t.w_off >= 0 && (t.w_off & 15) == 0 && (t.w_off >> 4) <= 0xFFFFFFFFll && t.row_bytes >= 0 &&
+                    (t.row_bytes & 15) == 0 && (t.row_bytes >> 4) < 65536 && t.K >= 0 && t.K < 65536 &&
+                    t.signal_ctr >= -1 && t.signal_ctr < 32768 && t.wpr >= 0 && t.wpr < 256;
+        for (int w = 0; w < t.n_waits && fits; ++w)
+            fits = t.wait_ctr[w] >= 0 && t.wait_ctr[w] < 65536 && t.wait_cnt[w] >= 0 && t.wait_cnt[w] < 65536 &&
+                   (t.wait_off[w] == 0 || t.wait_off[w] == -1);
+        if (!fits) {
+            set_error("task %d does not fit the device record (blob offset above 64 GiB or a field out of range)", id);
+            return MK_ERR_INVALID_ARG;
+        }
+        r.op = (uint8_t)t.op;
+        r.n_waits = (uint8_t)t.n_waits;
+        r.layer = (uint16_t)t.layer;
+        r.row0 = t.row0;
+        r.nrows = t.nrows;
+        r.w_off16 = (uint32_t)(t.w_off >> 4);
+        r.row_bytes16 = (uint16_t)(t.row_bytes >> 4);
+        r.K = (uint16_t)t.K;
+        for (int w = 0; w < t.n_waits; ++w) {
+            r.wait_ctr[w] = (uint16_t)t.wait_ctr[w];
+            r.wait_cnt[w] = (uint16_t)t.wait_cnt[w];
+            if (t.wait_off[w] == -1) r.wait_prev |= (uint8_t)(1u << w);
+        }
+        r.signal_ctr = (int16_t)t.signal_ctr;
+        r.wpr = (uint8_t)t.wpr;
+        recs->push_back(r);
+    }
+    return MK_OK;
+}
+
 mk_ir* to_ir(const Lowering& lw, int n_sms) {
     mk_ir* ir = new mk_ir{};
     ir->n_sms = n_sms;
@@ -627,8 +675,7 @@ WsLayout ws_layout(const mk_model_desc* d, const Config& c, int64_t n_tasks, int
     w.status = take(256);
     w.counters = take((int64_t)n_counters * CTR_STRIDE * 4);
     w.key = take(128);
-    w.tasks = take(n_tasks * (int64_t)sizeof(DevTask));
-    w.queue = take(n_tasks * 4);
+    w.recs = take(n_tasks * (int64_t)sizeof(TaskRec));
     w.queue_off = take((int64_t)(c.sms + 1) * 4);
     w.inv_freq = take((int64_t)d->head_dim / 2 * 4);
     w.x = take((int64_t)d->d_model * 4);

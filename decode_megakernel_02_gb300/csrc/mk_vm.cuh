@@ -83,8 +83,10 @@ __device__ __forceinline__ float i4_to_f32(uint32_t word_xor88, int n) {
 }
 
 // ------------------------------------------------------------------ shared memory
-// Scratch of one attention task; its space is reused by the split-KV merge of
-// the O prologue (a CTA never runs both at once).
+// Layout: [input vector of a GEMV task | attention scratch] (one region: a
+// CTA runs one task at a time and a GEMV task reads its input vector into
+// registers before it ends) [Shared] [task records] [weight rings].
+// Scratch of one attention task.
 struct AttnScratch {
     float q[MAX_REP * 128];         // roped, scaled queries of one KV group
     float kcur[128], vcur[128];     // this step's K and V (bf16-rounded)
@@ -100,10 +102,7 @@ struct Shared {
     float norm[NW];                 // RMSNorm sum of squares
     float gpart[NW][2][8][NW];      // [group][parity][row][warp]: partial sums of shared rows
     unsigned long long keys[NW];    // per-warp LM argmax keys
-    union {
-        AttnScratch at;
-        MergeScratch mg;
-    };
+    MergeScratch mg;
     float m[MAX_REP], l[MAX_REP], alpha[MAX_REP];
     int32_t flag;                   // broadcast of a counter-wait result
     int32_t abort;                  // set when this CTA must stop
@@ -128,7 +127,7 @@ __host__ __device__ constexpr int ring_slots() {  // slots that fit beside the o
 }
 
 struct WarpStream {
-    int s, qi;               // cursor: step, next queue entry
+    int s, qi;               // cursor: step, next record of the CTA's table
     int q, nb, ngroups, grp;  // current task: next batch of this warp, batches, groups, group
     int nrows, row_bytes, nl, tlc, S, lofs, code_bytes;
     const uint8_t* base;     // the task's first row
@@ -136,13 +135,21 @@ struct WarpStream {
     bool done;
 };
 
-__host__ __device__ constexpr size_t ring_offset(int xs_floats) {
-    return ((size_t)xs_floats * 4 + sizeof(Shared) + 127) / 128 * 128;
+__host__ __device__ constexpr size_t up128(size_t v) { return (v + 127) / 128 * 128; }
+__host__ __device__ constexpr size_t region0_bytes(int xs_floats) {
+    return up128((size_t)xs_floats * 4 > sizeof(AttnScratch) ? (size_t)xs_floats * 4 : sizeof(AttnScratch));
+}
+__host__ __device__ constexpr size_t table_offset(int xs_floats) { return region0_bytes(xs_floats) + up128(sizeof(Shared)); }
+__host__ __device__ constexpr size_t ring_offset(int xs_floats, int tab_cap) {
+    return table_offset(xs_floats) + up128((size_t)tab_cap * sizeof(TaskRec));
 }
 
 struct Ctx {
     const VmParams* p;
     Shared* sh;
+    AttnScratch* at;    // overlaps xs
+    const TaskRec* tab; // this CTA's task records (shared memory)
+    int nrec, q0;       // records in the table; queue index of the first
     uint8_t* ring;      // this warp's weight ring (ring_slots x ring_slot_bytes)
     WarpStream ws;      // this warp's weight-stream cursor (shared-memory ring)
     int rs;             // ring slot of the next batch to compute
@@ -164,14 +171,14 @@ static __device__ void raise_error(const VmParams& p, uint32_t code, uint32_t ta
 // Consumer wait on a counter: thread 0 spins, the rest learn the outcome at
 // the named barrier.  An abort raised anywhere (another CTA, or one of this
 // CTA's warps inside the previous task) stops every consumer warp here.
-static __device__ __forceinline__ bool wait_counters(Ctx& c, const DevTask& t, int task_id, int step) {
+static __device__ __forceinline__ bool wait_counters(Ctx& c, const TaskRec& t, int task_id, int step) {
     const VmParams& p = *c.p;
     if (c.tid == 0) {
         int ok = c.sh->abort ? 0 : 1;
         const uint32_t e = (uint32_t)(p.epoch0 + step);
         for (int w = 0; w < t.n_waits && ok; ++w) {
             const uint32_t* ctr = p.counters + (size_t)t.wait_ctr[w] * CTR_STRIDE;
-            const uint32_t target = (uint32_t)t.wait_cnt[w] * (e + 1u + (uint32_t)t.wait_off[w]);
+            const uint32_t target = (uint32_t)t.wait_cnt[w] * (e + 1u - ((t.wait_prev >> w) & 1u));
             if ((int32_t)(ld_acquire(ctr) - target) >= 0) continue;
             const uint64_t t0 = gtimer();
             for (uint32_t it = 1;; ++it) {
@@ -199,7 +206,7 @@ static __device__ __forceinline__ bool wait_counters(Ctx& c, const DevTask& t, i
 // The consumer barrier orders every consumer thread's writes of the task
 // before thread 0's release-add; a gpu-scope release is cumulative over
 // writes that happen before it, so the waiting CTA's acquire sees them all.
-__device__ __forceinline__ void signal_counter(Ctx& c, const DevTask& t) {
+__device__ __forceinline__ void signal_counter(Ctx& c, const TaskRec& t) {
     bar_consumers();
     if (c.tid == 0 && t.signal_ctr >= 0 && !c.sh->abort)
         red_release_add(c.p->counters + (size_t)t.signal_ctr * CTR_STRIDE, 1u);
@@ -459,31 +466,31 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 // Move the cursor to this warp's next batch; false at the end of the launch.
-__device__ __forceinline__ bool stream_next(const VmParams& p, int q0, int q1, int warp, int lane, WarpStream& w) {
+__device__ __forceinline__ bool stream_next(const Ctx& c, WarpStream& w) {
+    const VmParams& p = *c.p;
     for (;;) {
         if (w.q < w.nb) return true;
-        if (w.qi >= q1) {
+        if (w.qi >= c.nrec) {
             if (++w.s >= p.n_steps) return false;
-            w.qi = q0;
+            w.qi = 0;
         }
-        const DevTask* tp = p.tasks + __ldg(p.queue + w.qi);
-        ++w.qi;
-        const int op = __ldg(&tp->op);
+        const TaskRec& t = c.tab[w.qi++];
+        const int op = t.op;
         w.nb = 0;
         w.q = 0;
         if (!(op == OP_QKV || op == OP_O || op == OP_GU || op == OP_DOWN || (op == OP_LM && !p.skip_lm))) continue;
-        const int K = __ldg(&tp->K), g = __ldg(&tp->wpr);
-        const int L = (warp % g) * 32 + lane;
-        w.nrows = __ldg(&tp->nrows);
-        w.row_bytes = __ldg(&tp->row_bytes);
+        const int K = t.K, g = t.wpr;
+        const int L = (c.warp % g) * 32 + c.lane;
+        w.nrows = t.nrows;
+        w.row_bytes = (int)t.row_bytes16 * 16;
         w.ngroups = NW / g;
-        w.grp = warp / g;
+        w.grp = c.warp / g;
         w.S = 32 * g;
         const int code_bytes = p.wdtype == MK_W_INT8_ROW ? K : p.wdtype == MK_W_INT4_G128 ? K / 2 : 2 * K;
         const int CHc = code_bytes / 16;
         w.nl = L < CHc ? (CHc - L + w.S - 1) / w.S : 0;  // this lane's chunks of a row
         w.tlc = (w.row_bytes - code_bytes) / 16;
-        w.base = p.w + __ldg((const long long*)&tp->w_off);
+        w.base = p.w + (size_t)t.w_off16 * 16;
         w.lofs = L * 16;
         w.code_bytes = code_bytes;
         w.nb = (w.nrows + RW - 1) / RW;
@@ -494,11 +501,12 @@ __device__ __forceinline__ bool stream_next(const VmParams& p, int q0, int q1, i
 // Issue the copies of the cursor's batch into ring slot w.si (or an empty
 // group after the last batch), then advance.
 template <int WT>
-__device__ __forceinline__ void stream_issue(const VmParams& p, int q0, int q1, int warp, int lane, uint8_t* ring,
-                                             WarpStream& w) {
+__device__ __forceinline__ void stream_issue(Ctx& c) {
     constexpr int NGM = 64 / wpc<WT>();
-    if (!w.done && stream_next(p, q0, q1, warp, lane, w)) {
-        uint8_t* slot = ring + (size_t)w.si * ring_slot_bytes<WT>() + lane * 16;
+    WarpStream& w = c.ws;
+    const int lane = c.lane;
+    if (!w.done && stream_next(c, w)) {
+        uint8_t* slot = c.ring + (size_t)w.si * ring_slot_bytes<WT>() + lane * 16;
         const int64_t jstep = (int64_t)w.S * 16;
 #pragma unroll
         for (int r = 0; r < RW; ++r) {
@@ -529,7 +537,7 @@ __device__ __forceinline__ void stream_issue(const VmParams& p, int q0, int q1, 
 // stream (already requested before the counter wait).  Returns false when
 // the CTA must stop (abort or watchdog), identically in every thread.
 template <int WT, int BASE, int NG>
-__device__ bool gemv_run(Ctx& c, const DevTask& t, int task_id, int step, float& best_v, int& best_i) {
+__device__ bool gemv_run(Ctx& c, const TaskRec& t, int task_id, int step, float& best_v, int& best_i) {
     const VmParams& p = *c.p;
     constexpr int HP = wpc<WT>() / 2;
     constexpr int NGM = 64 / wpc<WT>();
@@ -592,7 +600,6 @@ __device__ bool gemv_run(Ctx& c, const DevTask& t, int task_id, int step, float&
     const bool writer = (c.lane & ((32 >> B) - 1)) == 0;
     int par = 0;
     const int nbatches = (nrows + RW - 1) / RW;
-    const int q0 = p.queue_off[blockIdx.x], q1 = p.queue_off[blockIdx.x + 1];
     for (int q = grp; q < nbatches; q += ngroups) {
         const int rb = q * RW;
         const int row_g = row0 + rb + my_r;
@@ -607,7 +614,7 @@ __device__ bool gemv_run(Ctx& c, const DevTask& t, int task_id, int step, float&
             }
         }
         // keep NB - 1 batches in flight beyond this one, then wait for this one
-        stream_issue<WT>(p, q0, q1, c.warp, c.lane, c.ring, c.ws);
+        stream_issue<WT>(c);
         cp_async_wait<NB - 1>();
         __syncwarp();
         const uint8_t* slot = c.ring + (size_t)c.rs * ring_slot_bytes<WT>();
@@ -675,7 +682,7 @@ __device__ bool gemv_run(Ctx& c, const DevTask& t, int task_id, int step, float&
 }
 
 template <int WT, int BASE>
-__device__ bool gemv_task(Ctx& c, const DevTask& t, int task_id, int step, float& best_v, int& best_i) {
+__device__ bool gemv_task(Ctx& c, const TaskRec& t, int task_id, int step, float& best_v, int& best_i) {
     const int S = 32 * t.wpr, CH = t.K / wpc<WT>(), ng = (CH + S - 1) / S;
     constexpr int NGMAX = 64 / wpc<WT>();  // 8 (16-bit), 4 (int8), 2 (int4)
 #define MK_RUN(N) return gemv_run<WT, BASE, (N <= NGMAX ? N : NGMAX)>(c, t, task_id, step, best_v, best_i)
@@ -717,9 +724,10 @@ __device__ __forceinline__ void load_kv_row(const uint16_t* rowp, int lane, floa
 // queries are rotated, so cache reads overlap the qkv reads.  Writes
 // (max, sum, unnormalised output) per query head.
 template <int HD>
-static __device__ __forceinline__ void attn_task(Ctx& c, const DevTask& t, int step) {
+static __device__ __forceinline__ void attn_task(Ctx& c, const TaskRec& t, int step) {
     const VmParams& p = *c.p;
     Shared& sh = *c.sh;
+    AttnScratch& at = *c.at;
     constexpr int DPL = HD / 32;            // dims per lane
     constexpr int PPW = ATTN_TILE / NW;     // positions per warp per tile
     constexpr int OPT = MAX_REP * HD / NT;  // output elements per thread (upper bound)
@@ -755,19 +763,19 @@ static __device__ __forceinline__ void attn_task(Ctx& c, const DevTask& t, int s
         for (int k = 0; k < PPW; ++k) {
             const int jj = c.warp + NW * k, j = jt + jj;
             if (jj < n) {
-                uint32_t* dst = (uint32_t*)(sh.at.sv + jj * HD + c.lane * DPL);
+                uint32_t* dst = (uint32_t*)(at.sv + jj * HD + c.lane * DPL);
 #pragma unroll
                 for (int i = 0; i < DPL / 2; ++i) {
                     if (j == pos) {
-                        dst[i] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(sh.at.vcur[c.lane * DPL + 2 * i])) |
-                                 ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(sh.at.vcur[c.lane * DPL + 2 * i + 1])) << 16);
+                        dst[i] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(at.vcur[c.lane * DPL + 2 * i])) |
+                                 ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(at.vcur[c.lane * DPL + 2 * i + 1])) << 16);
                     } else {
                         dst[i] = vraw[k][i];
                     }
                 }
                 if (j == pos) {
 #pragma unroll
-                    for (int i = 0; i < DPL; ++i) kf[k][i] = sh.at.kcur[c.lane * DPL + i];
+                    for (int i = 0; i < DPL; ++i) kf[k][i] = at.kcur[c.lane * DPL + i];
                 }
             }
         }
@@ -783,15 +791,15 @@ static __device__ __forceinline__ void attn_task(Ctx& c, const DevTask& t, int s
         sincosf(ang, &sn, &cs);
         const float o1 = x1 * cs - x2 * sn, o2 = x2 * cs + x1 * sn;
         if (hh < rep) {
-            sh.at.q[hh * HD + dd] = o1 * scale;
-            sh.at.q[hh * HD + dd + half] = o2 * scale;
+            at.q[hh * HD + dd] = o1 * scale;
+            at.q[hh * HD + dd + half] = o2 * scale;
         } else {
-            sh.at.kcur[dd] = round_bf16(o1);
-            sh.at.kcur[dd + half] = round_bf16(o2);
+            at.kcur[dd] = round_bf16(o1);
+            at.kcur[dd + half] = round_bf16(o2);
         }
     }
     for (int i = c.tid; i < HD; i += NT)
-        sh.at.vcur[i] = round_bf16(__ldcg(p.qkv + p.q_dim + p.kv_dim + (size_t)g * HD + i));
+        at.vcur[i] = round_bf16(__ldcg(p.qkv + p.q_dim + p.kv_dim + (size_t)g * HD + i));
     if (c.tid < rep) {
         sh.m[c.tid] = -1.0e30f;
         sh.l[c.tid] = 0.f;
@@ -799,8 +807,8 @@ static __device__ __forceinline__ void attn_task(Ctx& c, const DevTask& t, int s
     bar_consumers();
     if (ch == C - 1) {
         for (int i = c.tid; i < HD; i += NT) {
-            kbase[(size_t)pos * HD + i] = __bfloat16_as_ushort(__float2bfloat16_rn(sh.at.kcur[i]));
-            vbase[(size_t)pos * HD + i] = __bfloat16_as_ushort(__float2bfloat16_rn(sh.at.vcur[i]));
+            kbase[(size_t)pos * HD + i] = __bfloat16_as_ushort(__float2bfloat16_rn(at.kcur[i]));
+            vbase[(size_t)pos * HD + i] = __bfloat16_as_ushort(__float2bfloat16_rn(at.vcur[i]));
         }
     }
     float acc[OPT];
@@ -822,25 +830,25 @@ static __device__ __forceinline__ void attn_task(Ctx& c, const DevTask& t, int s
                     float sacc = 0.f;
                     if (h0 + hh < rep) {
 #pragma unroll
-                        for (int i = 0; i < DPL; ++i) sacc = fmaf(sh.at.q[(h0 + hh) * HD + c.lane * DPL + i], kf[k][i], sacc);
+                        for (int i = 0; i < DPL; ++i) sacc = fmaf(at.q[(h0 + hh) * HD + c.lane * DPL + i], kf[k][i], sacc);
                     }
                     v[k * 4 + hh] = sacc;
                 }
             const float sc = transpose_reduce<PPW * 4>(v, c.lane);
             constexpr int SH = PPW * 4 >= 32 ? 0 : PPW * 4 >= 16 ? 1 : 2;
             const int idx = c.lane >> SH, k = idx >> 2, hh = idx & 3, jj = c.warp + NW * k;
-            if ((c.lane & ((1 << SH) - 1)) == 0 && h0 + hh < rep && jj < n) sh.at.sc[(h0 + hh) * ATTN_TILE + jj] = sc;
+            if ((c.lane & ((1 << SH) - 1)) == 0 && h0 + hh < rep && jj < n) at.sc[(h0 + hh) * ATTN_TILE + jj] = sc;
         }
         bar_consumers();
         if (c.warp < rep) {  // online softmax statistics: warp h owns query head h
             const int h = c.warp;
-            const float a = c.lane < n ? sh.at.sc[h * ATTN_TILE + c.lane] : -3.0e38f;
+            const float a = c.lane < n ? at.sc[h * ATTN_TILE + c.lane] : -3.0e38f;
             float mt = a;
 #pragma unroll
             for (int o = 16; o; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, o));
             const float m_old = sh.m[h], m_new = fmaxf(m_old, mt);
             const float pa = c.lane < n ? expf(a - m_new) : 0.f;
-            if (c.lane < n) sh.at.sc[h * ATTN_TILE + c.lane] = pa;
+            if (c.lane < n) at.sc[h * ATTN_TILE + c.lane] = pa;
             const float ls = warp_sum(pa);
             if (c.lane == 0) {
                 const float al = expf(m_old - m_new);
@@ -855,8 +863,8 @@ static __device__ __forceinline__ void attn_task(Ctx& c, const DevTask& t, int s
             const int oe = c.tid + NT * e, h = oe / HD, dd = oe % HD;
             if (h < rep) {
                 float a = acc[e] * sh.alpha[h];
-                const float* pr = sh.at.sc + h * ATTN_TILE;
-                for (int jj = 0; jj < n; ++jj) a = fmaf(pr[jj], bf16_bits_to_f32(sh.at.sv[jj * HD + dd]), a);
+                const float* pr = at.sc + h * ATTN_TILE;
+                for (int jj = 0; jj < n; ++jj) a = fmaf(pr[jj], bf16_bits_to_f32(at.sv[jj * HD + dd]), a);
                 acc[e] = a;
             }
         }
@@ -878,30 +886,10 @@ static __device__ __forceinline__ void attn_task(Ctx& c, const DevTask& t, int s
 template <int WT, int BASE, int HD>
 __device__ __forceinline__ void consumer(Ctx& c) {
     const VmParams& p = *c.p;
-    const int q0 = p.queue_off[blockIdx.x], q1 = p.queue_off[blockIdx.x + 1];
     for (int s = 0; s < p.n_steps && !c.abort; ++s) {
-        for (int qi = q0; qi < q1 && !c.abort; ++qi) {
-            const int tid_ = __ldg(p.queue + qi);
-            const DevTask* tp = p.tasks + tid_;
-            DevTask t;  // fields read once into registers (read-only data path)
-            t.op = __ldg(&tp->op);
-            t.layer = __ldg(&tp->layer);
-            t.row0 = __ldg(&tp->row0);
-            t.nrows = __ldg(&tp->nrows);
-            t.K = __ldg(&tp->K);
-            t.row_bytes = __ldg(&tp->row_bytes);
-            t.rps = __ldg(&tp->rps);
-            t.wpr = __ldg(&tp->wpr);
-            t.rw = __ldg(&tp->rw);
-            t.w_off = __ldg((const long long*)&tp->w_off);
-            t.n_waits = __ldg(&tp->n_waits);
-            t.wait_ctr[0] = __ldg(&tp->wait_ctr[0]);
-            t.wait_ctr[1] = __ldg(&tp->wait_ctr[1]);
-            t.wait_cnt[0] = __ldg(&tp->wait_cnt[0]);
-            t.wait_cnt[1] = __ldg(&tp->wait_cnt[1]);
-            t.wait_off[0] = __ldg(&tp->wait_off[0]);
-            t.wait_off[1] = __ldg(&tp->wait_off[1]);
-            t.signal_ctr = __ldg(&tp->signal_ctr);
+        for (int qi = 0; qi < c.nrec && !c.abort; ++qi) {
+            const TaskRec& t = c.tab[qi];
+            const int tid_ = c.q0 + qi;  // queue index: identifies the task in errors and traces
             const uint64_t t_start = p.trace ? gtimer() : 0;
             float best_v = -3.0e38f;
             int best_i = 0;
@@ -948,7 +936,7 @@ __device__ __forceinline__ void consumer(Ctx& c) {
             }
             signal_counter(c, t);
             if (p.trace && c.tid == 0) {
-                const int k = s * (q1 - q0) + (qi - q0);
+                const int k = s * c.nrec + qi;
                 if (k < p.trace_cap) {
                     unsigned long long* r = p.trace + ((size_t)blockIdx.x * p.trace_cap + k) * 8;
                     r[0] = (unsigned long long)tid_ | ((unsigned long long)s << 32);
@@ -971,19 +959,24 @@ __global__ void __launch_bounds__(THREADS, 1) vm_kernel(const VmParams p) {
     c.lane = threadIdx.x & 31;
     c.warp = threadIdx.x >> 5;
     c.xs = (float*)smem_raw;
-    c.sh = (Shared*)(smem_raw + (size_t)p.xs_floats * 4);
-    c.ring = smem_raw + ring_offset(p.xs_floats) + (size_t)c.warp * ring_slots<WT>() * ring_slot_bytes<WT>();
+    c.at = (AttnScratch*)smem_raw;
+    c.sh = (Shared*)(smem_raw + region0_bytes(p.xs_floats));
+    TaskRec* tab = (TaskRec*)(smem_raw + table_offset(p.xs_floats));
+    c.tab = tab;
+    c.ring = smem_raw + ring_offset(p.xs_floats, p.tab_cap) + (size_t)c.warp * ring_slots<WT>() * ring_slot_bytes<WT>();
     c.rstd = 1.f;
     c.abort = false;
     c.rs = 0;
-    const int q0 = p.queue_off[blockIdx.x], q1 = p.queue_off[blockIdx.x + 1];
-    c.ws = WarpStream{0, q0, 0, 0, 1, 0, 0, 0, 0, 0, 32, 0, 0, nullptr, 0, false};
+    c.q0 = p.queue_off[blockIdx.x];
+    c.nrec = min(p.queue_off[blockIdx.x + 1] - c.q0, p.tab_cap);  // the host sizes tab_cap to the longest queue
+    for (int i = threadIdx.x; i < c.nrec * (int)(sizeof(TaskRec) / 16); i += NT)
+        ((uint4*)tab)[i] = __ldg((const uint4*)(p.recs + c.q0) + i);
+    c.ws = WarpStream{0, 0, 0, 0, 1, 0, 0, 0, 0, 0, 32, 0, 0, nullptr, 0, false};
     if (threadIdx.x == 0) c.sh->abort = 0;
     for (int i = c.lane; i < ring_slots<WT>() * ring_slot_bytes<WT>() / 16; i += 32)  // no stale NaN bit patterns
         ((uint4*)c.ring)[i] = make_uint4(0, 0, 0, 0);
-    __syncwarp();
-    for (int i = 0; i < ring_slots<WT>() - 1; ++i) stream_issue<WT>(p, q0, q1, c.warp, c.lane, c.ring, c.ws);
-    __syncthreads();
+    __syncthreads();  // the task table is complete
+    for (int i = 0; i < ring_slots<WT>() - 1; ++i) stream_issue<WT>(c);
     consumer<WT, BASE, HD>(c);
     cp_async_wait<0>();  // no copy may land in shared memory after the CTA exits
 }

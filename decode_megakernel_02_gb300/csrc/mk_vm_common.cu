@@ -20,14 +20,14 @@ const void* vm_kernel_for(int wdtype, int base, int hd) {
     }
 }
 
-size_t vm_shared_bytes(int wdtype, int xs_floats) {
+size_t vm_shared_bytes(int wdtype, int xs_floats, int tab_cap) {
     size_t ring = 0;
     switch (wdtype) {
         case MK_W_INT8_ROW: ring = (size_t)NW * ring_slots<MK_W_INT8_ROW>() * ring_slot_bytes<MK_W_INT8_ROW>(); break;
         case MK_W_INT4_G128: ring = (size_t)NW * ring_slots<MK_W_INT4_G128>() * ring_slot_bytes<MK_W_INT4_G128>(); break;
         default: ring = (size_t)NW * ring_slots<MK_W_BF16>() * ring_slot_bytes<MK_W_BF16>(); break;
     }
-    return ring_offset(xs_floats) + ring;
+    return ring_offset(xs_floats, tab_cap) + ring;
 }
 
 // ------------------------------------------------------------------ test kernels

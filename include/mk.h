@@ -315,13 +315,12 @@ mk_status mk_debug_dequant(const mk_model_desc* desc, const void* weights_dev, i
                            int32_t layer, float* out_dev, mk_stream_t stream);
 
 /* Record %globaltimer stamps of every task of later launches into trace_dev,
- * uint64 [ctas][records_per_cta][8] = {task id | step << 32, wait start,
- * wait done, after signal, ns consumer warp 0 waited for filled ring slots
- * (cumulative), ring slots consumed (cumulative), ns the weight-streaming
- * warp waited for free slots (cumulative), 0}; record k of a CTA is
- * step * queue_len + queue slot, and records past the capacity are dropped.
- * NULL disables tracing.  The buffer is caller-owned and must outlive the
- * launches. */
+ * uint64 [ctas][records_per_cta][8] = {queue index | step << 32, task start,
+ * wait done, after signal, 0, 0, 0, 0}.  The queue index is the task's
+ * position in the concatenated per-CTA queues (mk_ir.queue holds the task id
+ * at each index).  Record k of a CTA is step * queue_len + queue slot, and
+ * records past the capacity are dropped.  NULL disables tracing.  The buffer
+ * is caller-owned and must outlive the launches. */
 mk_status mk_debug_set_trace(mk_handle* h, void* trace_dev, int32_t records_per_cta);
 
 /* Launch a one-CTA kernel that waits on a counter nothing ever signals, with
