@@ -204,12 +204,25 @@ static __device__ __forceinline__ bool wait_counters(Ctx& c, const TaskRec& t, i
 }
 
 // The consumer barrier orders every consumer thread's writes of the task
-// before thread 0's release-add; a gpu-scope release is cumulative over
-// writes that happen before it, so the waiting CTA's acquire sees them all.
-__device__ __forceinline__ void signal_counter(Ctx& c, const TaskRec& t) {
+// before the release-add by lane 0 of warp sw; a gpu-scope release is
+// cumulative over writes that happen before it, so the waiting CTA's acquire
+// sees them all.
+__device__ __forceinline__ void signal_counter(Ctx& c, const TaskRec& t, int sw) {
     bar_consumers();
-    if (c.tid == 0 && t.signal_ctr >= 0 && !c.sh->abort)
+    if (c.warp == sw && c.lane == 0 && t.signal_ctr >= 0 && !c.sh->abort)
         red_release_add(c.p->counters + (size_t)t.signal_ctr * CTR_STRIDE, 1u);
+}
+
+// The warp that releases a task's signal.  A gpu-scope release waits for
+// every weight copy its warp still has in flight (about one HBM latency
+// right after the warp has run ahead into the next task), so the signal
+// goes to the first warp of the last warp group: with batches dealt out
+// round-robin that group has the fewest, and its copies usually land while
+// the other groups finish.
+__device__ __forceinline__ int signal_warp(const TaskRec& t, bool gemv) {
+    if (!gemv) return NW - 1;
+    const int g = t.wpr;
+    return NW - g;
 }
 
 // ------------------------------------------------------------------ tokens
@@ -244,6 +257,15 @@ static __device__ __forceinline__ int step_token(const VmParams& p, int step) {
 }
 
 // ------------------------------------------------------------------ GEMV inputs
+// Position (in floats) of float4 unit u of a K-float input vector in c.xs.
+// Unit u belongs to the 16-byte weight chunk u >> lq4 of a row (2^lq4 units
+// per chunk); the units of equal rank in their chunk form one plane, so the
+// 32 lanes of a warp, which read the same rank of 32 consecutive chunks,
+// touch 512 consecutive bytes (no bank conflicts).
+__device__ __forceinline__ int xs_pos(int u, int K, int lq4) {
+    const int nch = K >> (lq4 + 2);
+    return ((u & ((1 << lq4) - 1)) * nch + (u >> lq4)) * 4;
+}
 // Each prologue writes the task's input vector (K floats) into c.xs with all
 // consumer threads and ends with a consumer barrier.
 
@@ -251,7 +273,7 @@ static __device__ __forceinline__ int step_token(const VmParams& p, int step) {
 // The gain loads are issued together with the x loads (one memory round trip).
 template <int BASE>
 static __device__ __forceinline__ void prologue_rmsnorm(Ctx& c, const float* x, const uint16_t* emb_row, const uint16_t* gain, int K,
-                                 float eps) {
+                                 float eps, int lq4) {
     float ss = 0.f;
     for (int g = c.tid; g < (K >> 3); g += NT) {
         const uint4 graw = __ldg((const uint4*)(gain + 8 * g));
@@ -278,8 +300,8 @@ static __device__ __forceinline__ void prologue_rmsnorm(Ctx& c, const float* x, 
             v[2 * i] *= base_to_f32<BASE>(gv[i] & 0xFFFFu);
             v[2 * i + 1] *= base_to_f32<BASE>(gv[i] >> 16);
         }
-        *(float4*)(c.xs + 8 * g) = make_float4(v[0], v[1], v[2], v[3]);
-        *(float4*)(c.xs + 8 * g + 4) = make_float4(v[4], v[5], v[6], v[7]);
+        *(float4*)(c.xs + xs_pos(2 * g, K, lq4)) = make_float4(v[0], v[1], v[2], v[3]);
+        *(float4*)(c.xs + xs_pos(2 * g + 1, K, lq4)) = make_float4(v[4], v[5], v[6], v[7]);
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
@@ -296,7 +318,7 @@ static __device__ __forceinline__ void prologue_rmsnorm(Ctx& c, const float* x, 
 // all heads are read cooperatively and turned into per-chunk weights in
 // shared memory; each thread then reads its chunk accumulators with batches
 // of independent loads.
-static __device__ __forceinline__ void prologue_attention(Ctx& c) {
+static __device__ __forceinline__ void prologue_attention(Ctx& c, int lq4) {
     const VmParams& p = *c.p;
     const int C = p.C, HC = p.Hq * C;
     float* wgt = c.sh->mg.mw;  // [Hq][C]
@@ -339,8 +361,8 @@ static __device__ __forceinline__ void prologue_attention(Ctx& c) {
                 o[6] = fmaf(w, a[k][1].z, o[6]); o[7] = fmaf(w, a[k][1].w, o[7]);
             }
         }
-        *(float4*)(c.xs + 8 * g) = make_float4(o[0], o[1], o[2], o[3]);
-        *(float4*)(c.xs + 8 * g + 4) = make_float4(o[4], o[5], o[6], o[7]);
+        *(float4*)(c.xs + xs_pos(2 * g, p.q_dim, lq4)) = make_float4(o[0], o[1], o[2], o[3]);
+        *(float4*)(c.xs + xs_pos(2 * g + 1, p.q_dim, lq4)) = make_float4(o[4], o[5], o[6], o[7]);
     }
     c.rstd = 1.f;
     bar_consumers();
@@ -547,6 +569,7 @@ __device__ bool gemv_run(Ctx& c, const TaskRec& t, int task_id, int step, float&
     const int grp = c.warp / g, wig = c.warp % g;
     const int L = wig * 32 + c.lane, S = 32 * g;
     const int CH = K / wpc<WT>();  // 16-byte chunks of codes per row
+    constexpr int LQ4 = wpc<WT>() == 8 ? 1 : wpc<WT>() == 16 ? 2 : 3;  // log2(float4 units per chunk)
 
     if (!wait_counters(c, t, task_id, step)) return false;
     int tok = 0;
@@ -562,15 +585,15 @@ __device__ bool gemv_run(Ctx& c, const TaskRec& t, int task_id, int step, float&
         case OP_QKV: {
             const uint16_t* gain = (const uint16_t*)(p.w + p.layer_bytes * layer + p.l_attn_norm);
             const uint16_t* emb = layer == 0 ? (const uint16_t*)(p.w + p.embed) + (size_t)tok * p.d : nullptr;
-            prologue_rmsnorm<BASE>(c, p.x, emb, gain, p.d, p.eps);
+            prologue_rmsnorm<BASE>(c, p.x, emb, gain, p.d, p.eps, LQ4);
             break;
         }
         case OP_GU:
             prologue_rmsnorm<BASE>(c, p.x, nullptr, (const uint16_t*)(p.w + p.layer_bytes * layer + p.l_ffn_norm), p.d,
-                                   p.eps);
+                                   p.eps, LQ4);
             break;
-        case OP_LM: prologue_rmsnorm<BASE>(c, p.x, nullptr, (const uint16_t*)(p.w + p.final_norm), p.d, p.eps); break;
-        case OP_O: prologue_attention(c); break;
+        case OP_LM: prologue_rmsnorm<BASE>(c, p.x, nullptr, (const uint16_t*)(p.w + p.final_norm), p.d, p.eps, LQ4); break;
+        case OP_O: prologue_attention(c, LQ4); break;
         default:  // down reads h straight from device memory
             xin = p.h;
             from_global = true;
@@ -584,12 +607,12 @@ __device__ bool gemv_run(Ctx& c, const TaskRec& t, int task_id, int step, float&
         for (int j = 0; j < NG; ++j) {
             const int cidx = L + S * j;
             const bool ok = cidx < CH;
-            const float* xp = xin + (ok ? cidx : 0) * wpc<WT>();
+            const int cc = ok ? cidx : 0;
 #pragma unroll
             for (int i = 0; i < HP / 2; ++i) {
                 float4 v;
-                if (from_global) v = __ldcg((const float4*)(xp + 4 * i));
-                else v = *(const float4*)(xp + 4 * i);
+                if (from_global) v = __ldcg((const float4*)(xin + cc * wpc<WT>() + 4 * i));  // natural layout
+                else v = *(const float4*)(xin + (i * CH + cc) * 4);                         // planes (xs_pos)
                 xr[j * HP + 2 * i] = ok ? pack2(v.x * f, v.y * f) : 0ull;
                 xr[j * HP + 2 * i + 1] = ok ? pack2(v.z * f, v.w * f) : 0ull;
             }
@@ -928,13 +951,15 @@ __device__ __forceinline__ void consumer(Ctx& c) {
                 }
                 if (c.lane == 0) c.sh->keys[c.warp] = key;
             }
+            const int sw = signal_warp(t, gemv);
+            if (c.warp == sw) cp_async_wait<0>();  // its release then has no copies to wait for
             bar_consumers();
             if (gemv && t.op == OP_LM && c.tid == 0) {
                 unsigned long long key = 0;
                 for (int w = 0; w < NW; ++w) key = c.sh->keys[w] > key ? c.sh->keys[w] : key;
                 atomicMax(p.key, key);
             }
-            signal_counter(c, t);
+            signal_counter(c, t, sw);
             if (p.trace && c.tid == 0) {
                 const int k = s * c.nrec + qi;
                 if (k < p.trace_cap) {
