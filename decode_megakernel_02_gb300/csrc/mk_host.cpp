@@ -198,6 +198,7 @@ int64_t row_stride(int64_t K, int wdtype) {
 BlobLayout blob_layout(const mk_model_desc* d) {
     BlobLayout b{};
     int64_t qd = (int64_t)d->n_q_heads * d->head_dim, kd = (int64_t)d->n_kv_heads * d->head_dim;
+    b.down_cols = ffn_fused(d->wdtype, d->base_dtype, d->d_model);
     b.row_qkv = row_stride(d->d_model, d->wdtype);
     b.row_o = row_stride(qd, d->wdtype);
     b.row_gu = row_stride(d->d_model, d->wdtype);
@@ -248,7 +249,7 @@ static bool place(const mk_model_desc* d, int tensor, int layer, Place* p) {
         case MK_T_WO: *p = {lb + b.l_o, b.row_o, 0, 1, d->d_model, qd, true}; break;
         case MK_T_WGATE: *p = {lb + b.l_gu, b.row_gu, 0, 2, d->d_ffn, d->d_model, true}; break;
         case MK_T_WUP: *p = {lb + b.l_gu, b.row_gu, 1, 2, d->d_ffn, d->d_model, true}; break;
-        case MK_T_WDOWN: *p = {lb + b.l_down, b.row_down, 0, 1, d->d_model, d->d_ffn, true}; break;
+        case MK_T_WDOWN: *p = {lb + b.l_down, b.down_cols ? 0 : b.row_down, 0, 1, d->d_model, d->d_ffn, true}; break;
         default: return false;
     }
     return true;
@@ -319,6 +320,11 @@ mk_status mk_pack_tensor(const mk_model_desc* desc, int32_t tensor, int32_t laye
     for (int32_t r = 0; r < p.rows; ++r) {
         uint8_t* dst = blob + p.off + (int64_t)(p.first + (int64_t)r * p.step) * p.stride;
         const uint16_t* row = src + (int64_t)r * K;
+        if (p.stride == 0) {  // W_down in column blocks: row r of block c at (c * rows + r) * 16 bytes
+            for (int64_t c = 0; c < K / FFN_BLOCK; ++c)
+                std::memcpy(blob + p.off + (c * p.rows + r) * 16, row + c * FFN_BLOCK, 16);
+            continue;
+        }
         std::memset(dst, 0, (size_t)p.stride);
         if (desc->wdtype == desc->base_dtype) {
             std::memcpy(dst, row, (size_t)K * 2);

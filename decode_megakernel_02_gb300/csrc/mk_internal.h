@@ -16,7 +16,9 @@ enum Op : int32_t {
     OP_GU = 4,    // RMSNorm prologue + interleaved gate/up rows + SwiGLU -> h
     OP_DOWN = 5,  // Wdown GEMV rows + residual add -> x
     OP_LM = 6,    // final RMSNorm + LM-head rows + block argmax -> logits, key
-    OP_FIN = 7    // read the step's argmax key -> out id
+    OP_FIN = 7,   // read the step's argmax key -> out id
+    OP_FFN = 8    // RMSNorm prologue + gate/up rows + SwiGLU (kept on chip) + the down
+                  // projection's columns of those units, red.add into the next residual
 };
 
 constexpr int NT = 256;                 // threads per CTA (eight warps)
@@ -28,6 +30,21 @@ constexpr int MAX_REP = 8;              // query heads per KV head
 constexpr int ATTN_TILE = 32;           // positions per online-softmax tile
 constexpr int CTR_STRIDE = 32;          // u32 words between counters (128 B lines)
 constexpr int MAX_HC = 1024;            // query heads x split-KV chunks (merge scratch)
+constexpr int FFN_BLOCK = 8;            // hidden units per 16-byte column block of a fused down projection
+constexpr int FFN_MAX_UNITS = 2 * MAX_HC;  // hidden units of one OP_FFN task (its SwiGLU outputs reuse the merge scratch)
+
+// The FFN runs fused (OP_FFN) for 16-bit weights when every warp's share of
+// the d_model output rows is a whole number of 32-row lines (d_model % 256
+// == 0), a column block of a warp's rows fits one 16-line ring slot, and the
+// lines per block (d_model / 256) is one the kernel is built for.
+#ifdef __CUDACC__
+__host__ __device__
+#endif
+constexpr bool ffn_fused(int wdtype, int base_dtype, int d_model) {
+    return wdtype == base_dtype && d_model % 256 == 0 &&
+           (d_model / 256 == 1 || d_model / 256 == 2 || d_model / 256 == 4 || d_model / 256 == 8 ||
+            d_model / 256 == 10 || d_model / 256 == 12 || d_model / 256 == 16);
+}
 
 // Warps that share one weight row: enough that each lane holds at most
 // MAXG 8-wide k-groups of the input vector in registers (K <= 2048 * wpr).
@@ -73,6 +90,7 @@ static_assert(sizeof(TaskRec) == 32, "TaskRec layout");
 
 // Byte offsets of the packed weight blob.
 struct BlobLayout {
+    bool down_cols;     // W_down stored as FFN_BLOCK-column blocks (fused FFN) instead of rows
     int64_t row_qkv, row_o, row_gu, row_down, row_lm;   // row strides
     int64_t norm_bytes;                                 // bytes per norm-gain vector (padded)
     int64_t layer_bytes;                                // one layer block
@@ -90,7 +108,7 @@ struct VmParams {
     const TaskRec* recs;       // every CTA's queue, concatenated in queue order
     const int32_t* queue_off;  // [n_sms + 1]: CTA b owns recs[queue_off[b] .. queue_off[b+1])
     const float* inv_freq;     // [hd/2]
-    float* x;                  // residual stream [d]
+    float* x;                  // residual stream [2][d]
     float* qkv;                // [q_dim + 2 kv_dim]
     float* part_ml;            // [Hq][C][2]  (running max, sum)
     float* part_acc;           // [Hq][C][hd]
@@ -100,8 +118,9 @@ struct VmParams {
     float* logits;             // nullable: [n_steps][V]
     // model
     int32_t L, d, Hq, Hkv, hd, F, V, max_seq, wdtype, base_dtype, q_dim, kv_dim, C;
+    int32_t fused;             // FFN as OP_FFN: residual buffers alternate by layer (x + (layer & 1) * d)
     float eps;
-    int64_t layer_bytes, l_attn_norm, l_ffn_norm, final_norm, embed;
+    int64_t layer_bytes, l_attn_norm, l_ffn_norm, l_down, final_norm, embed;
     // run
     int32_t n_steps, pos0, epoch0, skip_lm;
     int32_t pending;           // token fed at step 0 (no forcing); -1: status[3]

@@ -125,10 +125,12 @@ mk_status launch(mk_handle* h, int n_steps, const int32_t* forced, int32_t* out_
     p.q_dim = d.n_q_heads * d.head_dim;
     p.kv_dim = d.n_kv_heads * d.head_dim;
     p.C = h->c.C;
+    p.fused = h->bl.down_cols ? 1 : 0;
     p.eps = d.rms_eps;
     p.layer_bytes = h->bl.layer_bytes;
     p.l_attn_norm = h->bl.l_attn_norm;
     p.l_ffn_norm = h->bl.l_ffn_norm;
+    p.l_down = h->bl.l_down;
     p.final_norm = h->bl.final_norm;
     p.embed = h->bl.embed;
     p.n_steps = n_steps;

@@ -154,6 +154,11 @@ mk_status lower(const mk_model_desc* d, const Config& c, Lowering* lw) {
     lw->n_counters = 5 * L + 1;
     auto ctr = [&](int l, int k) { return 5 * l + k; };
     const int64_t ML_BYTES = (int64_t)Hq * C * 2 * 4;
+    // Residual buffers: x[2][d].  With the fused FFN the layer-l input lives in
+    // x[l & 1]; O(l) writes x_mid into x[l & 1] and x[(l + 1) & 1], and the
+    // OP_FFN tasks add their down-projection partials into x[(l + 1) & 1].
+    const bool fused = bl.down_cols;
+    auto xb = [&](int l) -> int64_t { return fused ? (int64_t)(l & 1) * 4 * dm : 0; };
 
     auto gemv_task = [&](int op, int l, int64_t row0, int64_t nrows, int64_t K, int64_t rb,
                          int64_t region, int unit_rows, int signal) {
@@ -187,7 +192,7 @@ mk_status lower(const mk_model_desc* d, const Config& c, Lowering* lw) {
             int64_t r0 = p.second.first, r1 = p.second.second;
             DevTask t = gemv_task(OP_QKV, l, r0, r1 - r0, dm, bl.row_qkv, lb + bl.l_qkv, 1, ctr(l, 0));
             std::vector<mk_ir_access> acc;
-            acc.push_back(l == 0 ? A(B_KEY, MK_ACC_READ, 0, 8) : A(B_X, MK_ACC_READ, 0, 4 * dm));
+            acc.push_back(l == 0 ? A(B_KEY, MK_ACC_READ, 0, 8) : A(B_X, MK_ACC_READ, xb(l), xb(l) + 4 * dm));
             acc.push_back(A(B_QKV, MK_ACC_WRITE, 4 * r0, 4 * r1));
             ids.push_back(B.add_task(p.first, t, acc));
         }
@@ -200,12 +205,23 @@ mk_status lower(const mk_model_desc* d, const Config& c, Lowering* lw) {
         prev = ids;
         prev_ctr = ctr(l, 0);
 
-        // ---- attention: one task per (kv head, chunk), placed on the least-loaded CTAs
+        // ---- attention: one task per (kv head, chunk), placed on the least-loaded
+        // CTAs, no two on one CTA while free CTAs remain (they run in parallel)
         ids.clear();
         const int64_t est = std::max<int64_t>(1, d->max_seq / 2 / C) * hd * 2 * 2;
+        std::vector<char> has_attn(c.sms, 0);
+        int attn_placed = 0;
         for (int g = 0; g < Hkv; ++g) {
             for (int ch = 0; ch < C; ++ch) {
-                int sm = (int)(std::min_element(B.load.begin(), B.load.end()) - B.load.begin());
+                if (attn_placed == c.sms) {
+                    std::fill(has_attn.begin(), has_attn.end(), 0);
+                    attn_placed = 0;
+                }
+                int sm = -1;
+                for (int q = 0; q < c.sms; ++q)
+                    if (!has_attn[q] && (sm < 0 || B.load[q] < B.load[sm])) sm = q;
+                has_attn[sm] = 1;
+                ++attn_placed;
                 B.load[sm] += est;
                 DevTask t{};
                 t.op = OP_ATTN;
@@ -245,12 +261,37 @@ mk_status lower(const mk_model_desc* d, const Config& c, Lowering* lw) {
             std::vector<mk_ir_access> acc;
             acc.push_back(A(B_PART, MK_ACC_READ, 0, ML_BYTES + (int64_t)Hq * C * hd * 4));
             if (l == 0) acc.push_back(A(B_KEY, MK_ACC_READ, 0, 8));
-            acc.push_back(A(B_X, MK_ACC_WRITE, 4 * r0, 4 * r1));
+            acc.push_back(A(B_X, MK_ACC_WRITE, xb(l) + 4 * r0, xb(l) + 4 * r1));
+            if (fused) acc.push_back(A(B_X, MK_ACC_WRITE, xb(l + 1) + 4 * r0, xb(l + 1) + 4 * r1));
             ids.push_back(B.add_task(p.first, t, acc));
         }
         B.set_wait(ids, prev_ctr, (int)prev.size(), 0);
         prev = ids;
         prev_ctr = ctr(l, 2);
+
+        if (fused) {
+            // ---- fused FFN: each CTA owns blocks of FFN_BLOCK hidden units: their
+            // gate/up rows, SwiGLU in shared memory, and their down-projection
+            // column block, added into the next residual buffer
+            ids.clear();
+            const int64_t blocks = F / FFN_BLOCK, max_blocks = FFN_MAX_UNITS / FFN_BLOCK;
+            const int64_t block_bytes = FFN_BLOCK * (2 * bl.row_gu + 2 * dm);
+            for (auto& p : B.split(blocks, block_bytes)) {
+                for (int64_t b0 = p.second.first; b0 < p.second.second; b0 += max_blocks) {
+                    const int64_t b1 = std::min(p.second.second, b0 + max_blocks);
+                    const int64_t u0 = b0 * FFN_BLOCK, u1 = b1 * FFN_BLOCK;
+                    DevTask t = gemv_task(OP_FFN, l, 2 * u0, 2 * (u1 - u0), dm, bl.row_gu, lb + bl.l_gu, 2, ctr(l, 3));
+                    std::vector<mk_ir_access> acc;
+                    acc.push_back(A(B_X, MK_ACC_READ, xb(l), xb(l) + 4 * dm));
+                    acc.push_back(A(B_X, MK_ACC_ATOMIC, xb(l + 1), xb(l + 1) + 4 * dm));
+                    ids.push_back(B.add_task(p.first, t, acc));
+                }
+            }
+            B.set_wait(ids, prev_ctr, (int)prev.size(), 0);
+            prev = ids;
+            prev_ctr = ctr(l, 3);
+            continue;
+        }
 
         // ---- gate/up (interleaved pairs) + SwiGLU
         ids.clear();
@@ -286,7 +327,7 @@ mk_status lower(const mk_model_desc* d, const Config& c, Lowering* lw) {
         int64_t r0 = p.second.first, r1 = p.second.second;
         DevTask t = gemv_task(OP_LM, L, r0, r1 - r0, dm, bl.row_lm, bl.lm, 1, CTR_LM);
         std::vector<mk_ir_access> acc;
-        acc.push_back(A(B_X, MK_ACC_READ, 0, 4 * dm));
+        acc.push_back(A(B_X, MK_ACC_READ, xb(L), xb(L) + 4 * dm));
         acc.push_back(A(B_LOGITS, MK_ACC_WRITE, 4 * r0, 4 * r1, 4 * V, 0));
         acc.push_back(A(B_KEY, MK_ACC_ATOMIC, 0, 8));
         lm_ids.push_back(B.add_task(p.first, t, acc));
@@ -678,7 +719,7 @@ WsLayout ws_layout(const mk_model_desc* d, const Config& c, int64_t n_tasks, int
     w.recs = take(n_tasks * (int64_t)sizeof(TaskRec));
     w.queue_off = take((int64_t)(c.sms + 1) * 4);
     w.inv_freq = take((int64_t)d->head_dim / 2 * 4);
-    w.x = take((int64_t)d->d_model * 4);
+    w.x = take((int64_t)d->d_model * 2 * 4);
     w.qkv = take((qd + 2 * kd) * 4);
     w.part_ml = take((int64_t)d->n_q_heads * c.C * 2 * 4);
     w.part_acc = take((int64_t)d->n_q_heads * c.C * d->head_dim * 4);

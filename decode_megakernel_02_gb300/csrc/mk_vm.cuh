@@ -128,10 +128,16 @@ __host__ __device__ constexpr int ring_slots() {  // slots that fit beside the o
 
 struct WarpStream {
     int s, qi;               // cursor: step, next record of the CTA's table
-    int q, nb, ngroups, grp;  // current task: next batch of this warp, batches, groups, group
+    int q, nb, ngroups, grp;  // current phase: next batch of this warp, batches, batch step, first batch
+    // row phase: rows, row stride, chunks per lane per row, trailer chunks, lane stride, lane offset, code bytes.
+    // column phase (OP_FFN down projection): nrows = column blocks, row_bytes = block stride,
+    // nl = 512-byte lines per block of this warp's rows, tlc = blocks per batch.
     int nrows, row_bytes, nl, tlc, S, lofs, code_bytes;
-    const uint8_t* base;     // the task's first row
+    const uint8_t* base;     // the task's first row (column phase: this warp's part of the first block)
     int si;                  // ring slot of the next issue
+    int cols;                // 1 in a column phase
+    int ffn_blocks;          // column blocks of the OP_FFN task whose row phase is current (0: none)
+    const uint8_t* base2;    // that task's first down-projection column block
     bool done;
 };
 
@@ -492,6 +498,21 @@ __device__ __forceinline__ bool stream_next(const Ctx& c, WarpStream& w) {
     const VmParams& p = *c.p;
     for (;;) {
         if (w.q < w.nb) return true;
+        if (w.ffn_blocks) {  // the row phase of an OP_FFN task is done: its column blocks follow
+            const int R = p.d / NW;  // output rows of this warp
+            w.cols = 1;
+            w.nl = R / 32;
+            w.tlc = 16 / w.nl;
+            w.nrows = w.ffn_blocks;
+            w.row_bytes = p.d * 16;
+            w.base = w.base2 + (size_t)c.warp * R * 16;
+            w.lofs = c.lane * 16;
+            w.nb = (w.ffn_blocks + w.tlc - 1) / w.tlc;
+            w.q = 0;
+            w.ngroups = 1;
+            w.ffn_blocks = 0;
+            continue;
+        }
         if (w.qi >= c.nrec) {
             if (++w.s >= p.n_steps) return false;
             w.qi = 0;
@@ -500,7 +521,14 @@ __device__ __forceinline__ bool stream_next(const Ctx& c, WarpStream& w) {
         const int op = t.op;
         w.nb = 0;
         w.q = 0;
-        if (!(op == OP_QKV || op == OP_O || op == OP_GU || op == OP_DOWN || (op == OP_LM && !p.skip_lm))) continue;
+        w.cols = 0;
+        if (!(op == OP_QKV || op == OP_O || op == OP_GU || op == OP_DOWN || op == OP_FFN ||
+              (op == OP_LM && !p.skip_lm)))
+            continue;
+        if (op == OP_FFN) {
+            w.ffn_blocks = t.nrows / (2 * FFN_BLOCK);
+            w.base2 = p.w + p.layer_bytes * t.layer + p.l_down + (size_t)(t.row0 / (2 * FFN_BLOCK)) * p.d * 16;
+        }
         const int K = t.K, g = t.wpr;
         const int L = (c.warp % g) * 32 + c.lane;
         w.nrows = t.nrows;
@@ -530,8 +558,22 @@ __device__ __forceinline__ void stream_issue(Ctx& c) {
     if (!w.done && stream_next(c, w)) {
         uint8_t* slot = c.ring + (size_t)w.si * ring_slot_bytes<WT>() + lane * 16;
         const int64_t jstep = (int64_t)w.S * 16;
+        if (w.cols) {  // tlc blocks of nl lines: line k of the slot <- line m of block seg
+            int seg = w.q * w.tlc, m = 0;
+            const int lines = w.tlc * w.nl;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                if (k < lines && seg < w.nrows)
+                    cp_async16(slot + k * 512, w.base + (size_t)seg * w.row_bytes + m * 512 + w.lofs);
+                if (++m == w.nl) {
+                    m = 0;
+                    ++seg;
+                }
+            }
+        }
 #pragma unroll
         for (int r = 0; r < RW; ++r) {
+            if (w.cols) break;
             const int row = w.q * RW + r;
             if (row < w.nrows) {
                 const uint8_t* rowp = w.base + (int64_t)row * w.row_bytes;
@@ -551,6 +593,91 @@ __device__ __forceinline__ void stream_issue(Ctx& c) {
         w.done = true;
     }
     cp_async_commit();
+}
+
+// ------------------------------------------------------------------ fused FFN
+// Residual buffer holding the input of `layer` (with the fused FFN the two
+// buffers alternate by layer; otherwise there is one).
+__device__ __forceinline__ float* xbuf(const VmParams& p, int layer) {
+    return p.x + (p.fused ? (size_t)(layer & 1) * p.d : 0);
+}
+// SwiGLU outputs of the running OP_FFN task (the merge scratch is idle then).
+static_assert(sizeof(MergeScratch) >= FFN_MAX_UNITS * sizeof(float), "OP_FFN SwiGLU outputs");
+__device__ __forceinline__ float* ffn_h(Ctx& c) { return reinterpret_cast<float*>(&c.sh->mg); }
+
+__device__ __forceinline__ void red_add_f32(float* p, float v) {
+    asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+
+// Down projection of an OP_FFN task: y[r] = sum over the task's hidden units
+// u of Wdown[r][u] * h[u], for every output row r, added into the next
+// layer's residual buffer (which O initialised to x_mid).  W_down is packed in
+// column blocks of FFN_BLOCK units: block b holds, for r = 0..d-1, the 16
+// bytes Wdown[r][8b .. 8b+8).  Warp w owns rows [w*R, (w+1)*R), R = d/8, so a
+// block gives it NL = R/32 lines of 512 bytes: lane l of line m holds row
+// w*R + 32m + l.  The lane keeps NL packed accumulators and ends with one
+// red.add per row; the ring batches hold 16/NL blocks each.
+template <int WT, int NL>
+__device__ __forceinline__ void ffn_cols(Ctx& c, const TaskRec& t, int layer) {
+    const VmParams& p = *c.p;
+    constexpr int NB = ring_slots<WT>();
+    constexpr int SEGB = 16 / NL;
+    const int kc = t.nrows / (2 * FFN_BLOCK);
+    const int nb2 = (kc + SEGB - 1) / SEGB;
+    const float* hs = ffn_h(c);
+    unsigned long long acc[NL];
+#pragma unroll
+    for (int m = 0; m < NL; ++m) acc[m] = 0ull;
+    for (int b = 0; b < nb2; ++b) {
+        stream_issue<WT>(c);
+        cp_async_wait<NB - 1>();
+        __syncwarp();
+        const uint8_t* slot = c.ring + (size_t)c.rs * ring_slot_bytes<WT>() + c.lane * 16;
+#pragma unroll
+        for (int sg = 0; sg < SEGB; ++sg) {
+            const int seg = b * SEGB + sg;
+            if (seg < kc) {
+                const float4 h0 = *(const float4*)(hs + seg * FFN_BLOCK);
+                const float4 h1 = *(const float4*)(hs + seg * FFN_BLOCK + 4);
+                const unsigned long long hx[4] = {pack2(h0.x, h0.y), pack2(h0.z, h0.w), pack2(h1.x, h1.y),
+                                                  pack2(h1.z, h1.w)};
+#pragma unroll
+                for (int m = 0; m < NL; ++m) {
+                    const uint4 w = *(const uint4*)(slot + (sg * NL + m) * 512);
+                    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        unsigned long long wp;
+                        if constexpr (WT == MK_W_BF16) {
+                            wp = pack2(__uint_as_float(wv[i] << 16), __uint_as_float(wv[i] & 0xFFFF0000u));
+                        } else {
+                            const float2 f = __half22float2(*(const __half2*)&wv[i]);
+                            wp = pack2(f.x, f.y);
+                        }
+                        acc[m] = ffma2(wp, hx[i], acc[m]);
+                    }
+                }
+            }
+        }
+        __syncwarp();  // the slot is reused by a later issue of this warp
+        if (++c.rs == NB) c.rs = 0;
+    }
+    float* xo = xbuf(p, layer + 1) + (size_t)c.warp * (p.d / NW) + c.lane;
+#pragma unroll
+    for (int m = 0; m < NL; ++m) red_add_f32(xo + 32 * m, sum2(acc[m]));
+}
+
+template <int WT>
+__device__ __forceinline__ void ffn_down(Ctx& c, const TaskRec& t, int layer) {
+    switch (c.p->d / 256) {  // lines per block; the host only fuses these shapes
+        case 1: ffn_cols<WT, 1>(c, t, layer); break;
+        case 2: ffn_cols<WT, 2>(c, t, layer); break;
+        case 4: ffn_cols<WT, 4>(c, t, layer); break;
+        case 8: ffn_cols<WT, 8>(c, t, layer); break;
+        case 10: ffn_cols<WT, 10>(c, t, layer); break;
+        case 12: ffn_cols<WT, 12>(c, t, layer); break;
+        default: ffn_cols<WT, 16>(c, t, layer); break;
+    }
 }
 
 // One GEMV task.  Warp group grp (g warps sharing each row) owns the batches
@@ -585,14 +712,17 @@ __device__ bool gemv_run(Ctx& c, const TaskRec& t, int task_id, int step, float&
         case OP_QKV: {
             const uint16_t* gain = (const uint16_t*)(p.w + p.layer_bytes * layer + p.l_attn_norm);
             const uint16_t* emb = layer == 0 ? (const uint16_t*)(p.w + p.embed) + (size_t)tok * p.d : nullptr;
-            prologue_rmsnorm<BASE>(c, p.x, emb, gain, p.d, p.eps, LQ4);
+            prologue_rmsnorm<BASE>(c, xbuf(p, layer), emb, gain, p.d, p.eps, LQ4);
             break;
         }
         case OP_GU:
-            prologue_rmsnorm<BASE>(c, p.x, nullptr, (const uint16_t*)(p.w + p.layer_bytes * layer + p.l_ffn_norm), p.d,
-                                   p.eps, LQ4);
+        case OP_FFN:
+            prologue_rmsnorm<BASE>(c, xbuf(p, layer), nullptr,
+                                   (const uint16_t*)(p.w + p.layer_bytes * layer + p.l_ffn_norm), p.d, p.eps, LQ4);
             break;
-        case OP_LM: prologue_rmsnorm<BASE>(c, p.x, nullptr, (const uint16_t*)(p.w + p.final_norm), p.d, p.eps, LQ4); break;
+        case OP_LM:
+            prologue_rmsnorm<BASE>(c, xbuf(p, p.L), nullptr, (const uint16_t*)(p.w + p.final_norm), p.d, p.eps, LQ4);
+            break;
         case OP_O: prologue_attention(c, LQ4); break;
         default:  // down reads h straight from device memory
             xin = p.h;
@@ -630,7 +760,7 @@ __device__ bool gemv_run(Ctx& c, const TaskRec& t, int task_id, int step, float&
         float resid = 0.f;  // residual input of this lane's row
         if (writer && has_row) {
             if (op == OP_DOWN || (op == OP_O && layer > 0)) {
-                resid = __ldcg(p.x + row_g);
+                resid = __ldcg(xbuf(p, layer) + row_g);
             } else if (op == OP_O) {
                 const uint16_t* e = (const uint16_t*)(p.w + p.embed) + (size_t)tok * p.d;
                 resid = base_to_f32<BASE>(__ldg(e + row_g));
@@ -684,9 +814,12 @@ __device__ bool gemv_run(Ctx& c, const TaskRec& t, int task_id, int step, float&
             for (int r = 1; r < RW; ++r) scale = my_r == r ? rsv[r] : scale;
             tot *= scale;
         }
-        if (op == OP_GU) {  // rows alternate gate, up: the up total sits one row further
+        if (op == OP_GU || op == OP_FFN) {  // rows alternate gate, up: the up total sits one row further
             const float up = __shfl_down_sync(0xFFFFFFFFu, tot, 32 >> B);
-            if (wig == 0 && writer && has_row && !(my_r & 1)) p.h[row_g >> 1] = silu(tot) * up;
+            if (wig == 0 && writer && has_row && !(my_r & 1)) {
+                if (op == OP_GU) p.h[row_g >> 1] = silu(tot) * up;
+                else ffn_h(c)[(rb + my_r) >> 1] = silu(tot) * up;
+            }
         } else if (wig == 0 && writer && has_row) {
             if (op == OP_LM) {
                 if (p.logits) p.logits[(size_t)step * p.V + row_g] = tot;
@@ -697,7 +830,9 @@ __device__ bool gemv_run(Ctx& c, const TaskRec& t, int task_id, int step, float&
             } else if (op == OP_QKV) {
                 p.qkv[row_g] = tot;
             } else {  // O and down: residual add
-                p.x[row_g] = resid + tot;
+                float* xo = xbuf(p, layer);
+                xo[row_g] = resid + tot;
+                if (op == OP_O && p.fused) xbuf(p, layer + 1)[row_g] = resid + tot;  // the FFN adds into this copy
             }
         }
     }
@@ -916,11 +1051,17 @@ __device__ __forceinline__ void consumer(Ctx& c) {
             const uint64_t t_start = p.trace ? gtimer() : 0;
             float best_v = -3.0e38f;
             int best_i = 0;
-            const bool gemv = t.op == OP_QKV || t.op == OP_O || t.op == OP_GU || t.op == OP_DOWN ||
+            const bool gemv = t.op == OP_QKV || t.op == OP_O || t.op == OP_GU || t.op == OP_DOWN || t.op == OP_FFN ||
                               (t.op == OP_LM && !p.skip_lm);
             bool ok;
             if (gemv) {
                 ok = gemv_task<WT, BASE>(c, t, tid_, s, best_v, best_i);
+                if constexpr (WT == MK_W_BF16 || WT == MK_W_FP16) {
+                    if (ok && t.op == OP_FFN) {
+                        bar_consumers();  // every SwiGLU output of the task is in shared memory
+                        ffn_down<WT>(c, t, t.layer);
+                    }
+                }
             } else {
                 ok = wait_counters(c, t, tid_, s);
                 if (ok && t.op == OP_ATTN) {
@@ -996,7 +1137,7 @@ __global__ void __launch_bounds__(THREADS, 1) vm_kernel(const VmParams p) {
     c.nrec = min(p.queue_off[blockIdx.x + 1] - c.q0, p.tab_cap);  // the host sizes tab_cap to the longest queue
     for (int i = threadIdx.x; i < c.nrec * (int)(sizeof(TaskRec) / 16); i += NT)
         ((uint4*)tab)[i] = __ldg((const uint4*)(p.recs + c.q0) + i);
-    c.ws = WarpStream{0, 0, 0, 0, 1, 0, 0, 0, 0, 0, 32, 0, 0, nullptr, 0, false};
+    c.ws = WarpStream{0, 0, 0, 0, 1, 0, 0, 0, 0, 0, 32, 0, 0, nullptr, 0, 0, 0, nullptr, false};
     if (threadIdx.x == 0) c.sh->abort = 0;
     for (int i = c.lane; i < ring_slots<WT>() * ring_slot_bytes<WT>() / 16; i += 32)  // no stale NaN bit patterns
         ((uint4*)c.ring)[i] = make_uint4(0, 0, 0, 0);

@@ -97,9 +97,13 @@ typedef struct {
 /* ------------------------------------------------------------------ packing
  * The packer lays every GEMV weight out as contiguous rows in one blob, in
  * the order the device streams them: per layer [QKV rows (Wq;Wk;Wv)] [O rows]
- * [gate/up rows interleaved: gate_j, up_j] [down rows], then the LM head, the
+ * [gate/up rows interleaved: gate_j, up_j] [down], then the LM head, the
  * norm gains and the embedding.  Quantised rows carry their fp16 scales after
- * the codes; every row starts on a 16-byte boundary. */
+ * the codes; every row starts on a 16-byte boundary.
+ * Down projection: rows [d_model][d_ffn] for quantised weights; for 16-bit
+ * weights with d_model / 256 in {1, 2, 4, 8, 10, 12, 16} (the fused FFN) it is
+ * stored in column blocks of 8: block b holds, for r = 0 .. d_model-1, the
+ * 16 bytes Wdown[r][8b .. 8b+8), at offset (b * d_model + r) * 16. */
 enum {
     MK_T_EMBED = 0, MK_T_LM_HEAD = 1, MK_T_FINAL_NORM = 2, MK_T_ATTN_NORM = 3, MK_T_FFN_NORM = 4,
     MK_T_WQ = 5, MK_T_WK = 6, MK_T_WV = 7, MK_T_WO = 8, MK_T_WGATE = 9, MK_T_WUP = 10,
@@ -122,7 +126,8 @@ mk_status mk_pack_tensor(const mk_model_desc* desc, int32_t tensor, int32_t laye
 
 /* Byte offset, row stride and row count of a packed tensor inside the blob
  * (rows of Wq/Wk/Wv/Wgate/Wup are interleaved with their siblings: use the
- * stride and first_row to locate them).  Errors: INVALID_ARG. */
+ * stride and first_row to locate them).  A down projection stored in column
+ * blocks reports row_stride 0 (layout above).  Errors: INVALID_ARG. */
 mk_status mk_tensor_layout(const mk_model_desc* desc, int32_t tensor, int32_t layer,
                            size_t* offset, size_t* row_stride, int32_t* first_row,
                            int32_t* row_step, int32_t* rows);
