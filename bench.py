@@ -49,6 +49,22 @@ def algorithmic_bytes(w, pos0, n_steps):
     return total, gemv
 
 
+def max_over_ranks(value, device):
+    """The largest value over all ranks of the default process group (every
+    rank gets it): the job's time is its slowest replica's."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world, units_per_rank, seconds):
+    """Whole-job throughput of `world` replicas that each processed
+    units_per_rank units, over the slowest replica's time."""
+    return world * units_per_rank / seconds
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -260,12 +276,10 @@ def main():
     total_ms = ev0.elapsed_time(ev1)
     per_launch = [a.elapsed_time(b) for a, b in evs]
     if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+        total_ms = max_over_ranks(total_ms, "cuda")
         dist.barrier()
     ms_per_step = total_ms / args.steps
-    value = world * n_tok * args.steps / (total_ms / 1000.0)
+    value = job_rate(world, n_tok * args.steps, total_ms / 1000.0)
 
     # end to end through the host-buffer call (ids copied to host, stream synced)
     host_ids = np.empty(n_tok, np.int32)

@@ -1,0 +1,186 @@
+"""Host-side checks of the C ABI (no GPU): the library loads and exports every
+function include/mk.h declares; the packer and its quantisers produce the
+oracle's bytes; the static validator accepts every real lowering and never
+accepts a schedule the brute-force simulator finds unsafe."""
+import ctypes
+import os
+import random
+import re
+
+import numpy as np
+import pytest
+
+import synthetic
+from oracle import quant as Q
+from oracle import schedule_sim as S
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def mk():
+    from decode_megakernel_02_gb300 import build
+    build.build()
+    import decode_megakernel_02_gb300 as m
+    m.load()
+    return m
+
+
+# ------------------------------------------------------------------ exports
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "mk.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:mk_status|int64_t|const char\s*\*|void)\s*\*?\s*(mk_\w+)\s*\(",
+                                 text, flags=re.M)))
+
+
+def test_library_exports_every_declared_function(mk):
+    names = declared_functions()
+    assert len(names) >= 25
+    lib = ctypes.CDLL(os.path.join(ROOT, "decode_megakernel_02_gb300", "libmk.so"))
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+    # the binding declares a signature for every exported entry point
+    assert set(names) == set(mk.SIGNATURES), set(names) ^ set(mk.SIGNATURES)
+
+
+def test_errors_without_a_device(mk):
+    # contract violations are reported before any CUDA call
+    w = synthetic.get_workload("tiny")
+    d = mk.make_desc(w, flags=mk.MK_FLAG_TIED_HEAD)
+    with pytest.raises(mk.MKError) as e:
+        mk.mk_packed_size(d)
+    assert e.value.status == mk.MK_ERR_UNSUPPORTED
+    d = mk.make_desc(w)
+    d.head_dim = 96
+    with pytest.raises(mk.MKError) as e:
+        mk.mk_packed_size(d)
+    assert e.value.status == mk.MK_ERR_UNSUPPORTED
+
+
+# ------------------------------------------------------------------ packer
+def test_quantisers_match_oracle_bytes(mk):
+    rng = np.random.default_rng(5)
+    w = synthetic.bits_to_f32(
+        (rng.standard_normal((37, 256), np.float32) * 0.02).astype(np.float32).view(np.uint32) >> 16, "bf16")
+    w[3] = 0.0  # an all-zero row: scale 0, codes 0
+    q, s = mk.mk_quantize_int8(w)
+    qo, so = Q.quantize_int8_rows(w)
+    assert np.array_equal(q, qo) and np.array_equal(s.view(np.uint16), so.view(np.uint16))
+    q, s = mk.mk_quantize_int4(w)
+    qo, so = Q.quantize_int4_g128(w)
+    assert np.array_equal(q, qo) and np.array_equal(s.view(np.uint16), so.view(np.uint16))
+
+
+@pytest.mark.parametrize("wd", ["int8", "int4"])
+def test_packed_quantised_rows_match_oracle(mk, wd):
+    w = synthetic.get_workload("tiny").with_(wdtype=wd)
+    weights = synthetic.generate_weights(w)
+    desc = mk.make_desc(w)
+    blob = mk.pack_model(desc, weights)
+    for name, tid in (("wq", mk.MK_T_WQ), ("wup", mk.MK_T_WUP), ("wdown", mk.MK_T_WDOWN)):
+        src = synthetic.bits_to_f32(weights[f"l1.{name}"], "bf16")
+        lay = mk.mk_tensor_layout(desc, tid, 1)
+        K = src.shape[1]
+        for r in (0, 1, src.shape[0] - 1):
+            row = blob[lay["offset"] + (lay["first_row"] + r * lay["row_step"]) * lay["stride"]:][:lay["stride"]]
+            if wd == "int8":
+                q, s = Q.quantize_int8_rows(src[r:r + 1])
+                want = np.concatenate([q.view(np.uint8)[0], s.view(np.uint8)])
+            else:
+                q, s = Q.quantize_int4_g128(src[r:r + 1])
+                want = np.concatenate([Q.pack_int4_nibbles(q)[0], s.view(np.uint8)[0]])
+            assert np.array_equal(row[:len(want)], want), (name, r)
+            assert not row[len(want):].any()
+        assert lay["stride"] % 16 == 0 and K > 0
+
+
+def test_packed_down_column_blocks(mk):
+    w = synthetic.get_workload("tiny")
+    weights = synthetic.generate_weights(w)
+    desc = mk.make_desc(w)
+    blob = mk.pack_model(desc, weights)
+    lay = mk.mk_tensor_layout(desc, mk.MK_T_WDOWN, 0)
+    assert lay["stride"] == 0  # 16-bit weights with the fused FFN: column blocks of 8
+    down = np.asarray(weights["l0.wdown"], np.uint16)  # [d][F]
+    d, F = down.shape
+    region = blob[lay["offset"]:lay["offset"] + d * F * 2].view(np.uint16).reshape(F // 8, d, 8)
+    assert np.array_equal(region, down.reshape(d, F // 8, 8).transpose(1, 0, 2))
+
+
+# ------------------------------------------------------------------ validator
+@pytest.mark.parametrize("name,sms,chunks", [("tiny", 152, 0), ("tiny", 7, 3), ("tiny", 1, 1), ("tiny", 2, 4),
+                                             ("llama-1b", 152, 0), ("llama-1b-int8", 152, 0),
+                                             ("llama-1b-int4", 64, 2), ("llama-2b-fp16", 152, 0)])
+def test_validator_accepts_real_lowerings(mk, name, sms, chunks):
+    w = synthetic.get_workload(name)
+    st, why = mk.mk_validate_schedule(mk.make_desc(w), mk.make_config(sms=sms, attn_chunks=chunks), sms)
+    assert st == mk.MK_OK, why
+
+
+def _small_ir(mk, sms, chunks, wdtype=None):
+    w = synthetic.get_workload("tiny").with_(n_layers=1)
+    if wdtype:
+        w = w.with_(wdtype=wdtype)
+    return mk.mk_build_ir(mk.make_desc(w, max_seq=16), mk.make_config(sms=sms, attn_chunks=chunks), sms)
+
+
+def _mutants(ir, rng, n):
+    """Structural mutations of a real schedule (thresholds, waits, epoch offsets,
+    queue order, task placement, signals, accesses, outputs)."""
+    import copy
+    out = []
+    T = len(ir["tasks"])
+    for _ in range(n):
+        m = copy.deepcopy(ir)
+        kind = rng.randrange(9)
+        t = m["tasks"][rng.randrange(T)]
+        if kind == 0 and t["waits"]:
+            c, k, o = t["waits"][0]
+            t["waits"][0] = (c, k + rng.choice([1, 2]), o)
+        elif kind == 1 and t["waits"]:
+            c, k, o = t["waits"][0]
+            t["waits"][0] = (c, max(1, k - 1), o)
+        elif kind == 2 and t["waits"]:
+            t["waits"].pop(rng.randrange(len(t["waits"])))
+        elif kind == 3 and t["waits"]:
+            c, k, o = t["waits"][0]
+            t["waits"][0] = (c, k, -1 - o)
+        elif kind == 4:
+            q = m["queues"][rng.randrange(len(m["queues"]))]
+            if len(q) >= 2:
+                i = rng.randrange(len(q) - 1)
+                q[i], q[i + 1] = q[i + 1], q[i]
+        elif kind == 5 and len(m["queues"]) > 1:
+            s0 = rng.randrange(len(m["queues"]))
+            s1 = (s0 + 1) % len(m["queues"])
+            if m["queues"][s0]:
+                j = m["queues"][s0].pop(rng.randrange(len(m["queues"][s0])))
+                m["queues"][s1].insert(rng.randrange(len(m["queues"][s1]) + 1), j)
+                m["tasks"][j]["sm"] = s1
+        elif kind == 6 and t["signal"] >= 0:
+            t["signal"] = rng.randrange(m["n_counters"])
+        elif kind == 7 and t["acc"]:
+            b, k, lo, hi, st, gr = t["acc"][rng.randrange(len(t["acc"]))]
+            t["acc"].append((b, S.WRITE, lo, hi, st, gr))
+        elif kind == 8:
+            m["outputs"] = []
+        out.append(m)
+    return out
+
+
+@pytest.mark.parametrize("sms,chunks,wd", [(2, 1, None), (3, 2, None), (2, 1, "int8")])
+def test_validator_never_accepts_what_the_simulator_rejects(mk, sms, chunks, wd):
+    ir = _small_ir(mk, sms, chunks, wd)
+    assert S.verdict(ir)[0], S.verdict(ir)[1]
+    assert mk.mk_validate_ir(ir)[0] == mk.MK_OK
+    rng = random.Random(1000 * sms + chunks)
+    false_accepts, rejected = [], 0
+    for m in _mutants(ir, rng, 60):
+        safe, why = S.verdict(m)
+        st, vwhy = mk.mk_validate_ir(m)
+        if st == mk.MK_OK and not safe:
+            false_accepts.append(why)
+        rejected += st != mk.MK_OK
+    assert not false_accepts, false_accepts[:3]
+    assert rejected > 10  # the corpus does exercise the validator
