@@ -68,6 +68,7 @@ struct Builder {
     Lowering* lw;
     std::vector<int64_t> load;
     int S;
+    std::vector<std::vector<mk_ir_access>> tacc;  // accesses per task (flattened at the end)
 
     // Split `units` (of unit_rows rows, unit_bytes bytes) across the CTAs: every
     // CTA gets units/S, and the remainder goes to the CTAs with the least
@@ -102,9 +103,7 @@ struct Builder {
             it.wait_epoch_off[i] = t.wait_off[i];
         }
         it.signal_ctr = t.signal_ctr;
-        it.acc_begin = (int32_t)lw->acc.size();
-        it.n_acc = (int32_t)acc.size();
-        lw->acc.insert(lw->acc.end(), acc.begin(), acc.end());
+        tacc.push_back(std::move(acc));
         int id = (int)lw->tasks.size();
         lw->tasks.push_back(it);
         lw->dev.push_back(t);
@@ -235,9 +234,15 @@ mk_status lower(const mk_model_desc* d, const Config& c, Lowering* lw) {
                 acc.push_back(A(B_QKV, MK_ACC_READ, 4 * (qd + (int64_t)g * hd), 4 * (qd + (int64_t)(g + 1) * hd)));
                 acc.push_back(A(B_QKV, MK_ACC_READ, 4 * (qd + kd + (int64_t)g * hd),
                                 4 * (qd + kd + (int64_t)(g + 1) * hd)));
+                // The cache rows of earlier positions are read from before the
+                // task's own wait (their writers precede this CTA's previous
+                // task), so the read belongs to that previous task.
+                const int prev_task = lw->queues[sm].empty() ? -1 : lw->queues[sm].back();
                 for (int kv = 0; kv < 2; ++kv) {
                     int64_t base = (((int64_t)l * 2 + kv) * Hkv + g) * d->max_seq * hd * 2;
-                    acc.push_back(A(B_KV, MK_ACC_READ, base, base + P0 * hd * 2, 0, hd * 2));
+                    const mk_ir_access hist = A(B_KV, MK_ACC_READ, base, base + P0 * hd * 2, 0, hd * 2);
+                    if (prev_task >= 0) B.tacc[prev_task].push_back(hist);
+                    else acc.push_back(hist);
                     if (ch == C - 1)  // the chunk holding the newest position appends it
                         acc.push_back(A(B_KV, MK_ACC_WRITE, base + P0 * hd * 2, base + (P0 + 1) * hd * 2, hd * 2, 0));
                 }
@@ -349,6 +354,11 @@ mk_status lower(const mk_model_desc* d, const Config& c, Lowering* lw) {
     // The first layer of step e waits for the LM head of step e-1 (the token).
     B.set_wait(first_qkv, CTR_LM, (int)lm_ids.size(), -1);
 
+    for (size_t i = 0; i < lw->tasks.size(); ++i) {
+        lw->tasks[i].acc_begin = (int32_t)lw->acc.size();
+        lw->tasks[i].n_acc = (int32_t)B.tacc[i].size();
+        lw->acc.insert(lw->acc.end(), B.tacc[i].begin(), B.tacc[i].end());
+    }
     auto mm = std::minmax_element(B.load.begin(), B.load.end());
     lw->bytes_per_sm_min = *mm.first;
     lw->bytes_per_sm_max = *mm.second;

@@ -163,6 +163,7 @@ struct Ctx {
     float rstd;         // scale of xs applied when the fragments are loaded (RMSNorm)
     int tid, lane, warp;
     bool abort;
+    bool deferred;      // the last batch of the task issued no copy: issue it after the signal
 };
 
 __device__ __forceinline__ bool aborted(const VmParams& p) { return ld_volatile(p.status) != 0; }
@@ -595,6 +596,22 @@ __device__ __forceinline__ void stream_issue(Ctx& c) {
     cp_async_commit();
 }
 
+// Wait for the ring slot of the batch about to be computed.  NB - 1 batches
+// run ahead; a task's last batch (last = true) defers its issue until after
+// the task's signal, so the copy's back-pressure stays off the signal's path.
+template <int WT>
+__device__ __forceinline__ void ring_acquire(Ctx& c, bool last) {
+    constexpr int NB = ring_slots<WT>();
+    if (last) {
+        c.deferred = true;
+        cp_async_wait<NB - 2>();
+    } else {
+        stream_issue<WT>(c);
+        cp_async_wait<NB - 1>();
+    }
+    __syncwarp();
+}
+
 // ------------------------------------------------------------------ fused FFN
 // Residual buffer holding the input of `layer` (with the fused FFN the two
 // buffers alternate by layer; otherwise there is one).
@@ -629,9 +646,7 @@ __device__ __forceinline__ void ffn_cols(Ctx& c, const TaskRec& t, int layer) {
 #pragma unroll
     for (int m = 0; m < NL; ++m) acc[m] = 0ull;
     for (int b = 0; b < nb2; ++b) {
-        stream_issue<WT>(c);
-        cp_async_wait<NB - 1>();
-        __syncwarp();
+        ring_acquire<WT>(c, b == nb2 - 1);
         const uint8_t* slot = c.ring + (size_t)c.rs * ring_slot_bytes<WT>() + c.lane * 16;
 #pragma unroll
         for (int sg = 0; sg < SEGB; ++sg) {
@@ -767,9 +782,7 @@ __device__ bool gemv_run(Ctx& c, const TaskRec& t, int task_id, int step, float&
             }
         }
         // keep NB - 1 batches in flight beyond this one, then wait for this one
-        stream_issue<WT>(c);
-        cp_async_wait<NB - 1>();
-        __syncwarp();
+        ring_acquire<WT>(c, q + ngroups >= nbatches && op != OP_FFN);
         const uint8_t* slot = c.ring + (size_t)c.rs * ring_slot_bytes<WT>();
         float v[RW], rsv[RW];
 #pragma unroll
@@ -882,7 +895,7 @@ __device__ __forceinline__ void load_kv_row(const uint16_t* rowp, int lane, floa
 // queries are rotated, so cache reads overlap the qkv reads.  Writes
 // (max, sum, unnormalised output) per query head.
 template <int HD>
-static __device__ __forceinline__ void attn_task(Ctx& c, const TaskRec& t, int step) {
+static __device__ __forceinline__ bool attn_task(Ctx& c, const TaskRec& t, int task_id, int step) {
     const VmParams& p = *c.p;
     Shared& sh = *c.sh;
     AttnScratch& at = *c.at;
@@ -938,7 +951,11 @@ static __device__ __forceinline__ void attn_task(Ctx& c, const TaskRec& t, int s
             }
         }
     };
+    // The chunk's first cache rows are requested before the counter wait: rows
+    // of earlier positions were written by earlier steps, whose writers the
+    // wait of this CTA's previous task already ordered before us.
     if (j1 > j0) load_tile(j0, min(ATTN_TILE, j1 - j0));
+    if (!wait_counters(c, t, task_id, step)) return false;
 
     for (int i = c.tid; i < (rep + 1) * half; i += NT) {
         const int hh = i / half, dd = i % half;
@@ -1038,6 +1055,7 @@ static __device__ __forceinline__ void attn_task(Ctx& c, const TaskRec& t, int s
         ml[0] = sh.m[c.tid];
         ml[1] = sh.l[c.tid];
     }
+    return true;
 }
 
 // ------------------------------------------------------------------ consumer
@@ -1063,10 +1081,8 @@ __device__ __forceinline__ void consumer(Ctx& c) {
                     }
                 }
             } else {
-                ok = wait_counters(c, t, tid_, s);
-                if (ok && t.op == OP_ATTN) {
-                    attn_task<HD>(c, t, s);
-                } else if (ok && t.op == OP_FIN && c.tid == 0 && !p.skip_lm) {
+                ok = t.op == OP_ATTN ? attn_task<HD>(c, t, tid_, s) : wait_counters(c, t, tid_, s);
+                if (ok && t.op == OP_FIN && c.tid == 0 && !p.skip_lm) {
                     const unsigned long long k = __ldcg(p.key);
                     if ((k >> 49) != key_tag((uint32_t)(p.epoch0 + s))) {
                         raise_error(p, DEV_BAD_KEY, (uint32_t)tid_, (uint32_t)s);
@@ -1101,6 +1117,10 @@ __device__ __forceinline__ void consumer(Ctx& c) {
                 atomicMax(p.key, key);
             }
             signal_counter(c, t, sw);
+            if (c.deferred) {  // the copy the task's last batch skipped
+                stream_issue<WT>(c);
+                c.deferred = false;
+            }
             if (p.trace && c.tid == 0) {
                 const int k = s * c.nrec + qi;
                 if (k < p.trace_cap) {
@@ -1132,6 +1152,7 @@ __global__ void __launch_bounds__(THREADS, 1) vm_kernel(const VmParams p) {
     c.ring = smem_raw + ring_offset(p.xs_floats, p.tab_cap) + (size_t)c.warp * ring_slots<WT>() * ring_slot_bytes<WT>();
     c.rstd = 1.f;
     c.abort = false;
+    c.deferred = false;
     c.rs = 0;
     c.q0 = p.queue_off[blockIdx.x];
     c.nrec = min(p.queue_off[blockIdx.x + 1] - c.q0, p.tab_cap);  // the host sizes tab_cap to the longest queue
