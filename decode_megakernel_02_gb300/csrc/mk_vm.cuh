@@ -321,55 +321,48 @@ static __device__ __forceinline__ void prologue_rmsnorm(Ctx& c, const float* x, 
 }
 
 // Merge the split-KV partials of every query head into the attention output:
-// o = sum_c e^(m_c - M) acc_c / sum_c e^(m_c - M) l_c.  The (max, sum) pairs of
-// all heads are read cooperatively and turned into per-chunk weights in
-// shared memory; each thread then reads its chunk accumulators with batches
-// of independent loads.
+// o = sum_c e^(m_c - M) acc_c / sum_c e^(m_c - M) l_c, M = max_c m_c.
 static __device__ __forceinline__ void prologue_attention(Ctx& c, int lq4) {
     const VmParams& p = *c.p;
-    const int C = p.C, HC = p.Hq * C;
-    float* wgt = c.sh->mg.mw;  // [Hq][C]
-    for (int i = c.tid; i < HC; i += NT) wgt[i] = __ldcg(p.part_ml + 2 * i);        // m
-    for (int i = c.tid; i < HC; i += NT) c.sh->mg.ml[i] = __ldcg(p.part_ml + 2 * i + 1);  // l
-    bar_consumers();
-    if (c.tid < p.Hq) {
-        float* wh = wgt + c.tid * C;
-        const float* lh = c.sh->mg.ml + c.tid * C;
-        float M = -3.0e38f;
-        for (int ch = 0; ch < C; ++ch) M = fmaxf(M, wh[ch]);
-        float den = 0.f;
-        for (int ch = 0; ch < C; ++ch) {
-            wh[ch] = expf(wh[ch] - M);
-            den = fmaf(wh[ch], lh[ch], den);
-        }
-        const float inv = 1.f / den;
-        for (int ch = 0; ch < C; ++ch) wh[ch] *= inv;
-    }
-    bar_consumers();
+    const int C = p.C;
+    // One pass with a running maximum: each thread reads, for its 8 outputs,
+    // every chunk's (max, sum) and partial accumulators itself (up to 8
+    // chunks' loads in flight at once) and rescales as the maximum grows, so
+    // the merge costs about one round trip to L2 and no block barrier.
     for (int g = c.tid; g < (p.q_dim >> 3); g += NT) {
         const int hq = (8 * g) / p.hd, d0 = (8 * g) % p.hd;
-        const float* wh = wgt + hq * C;
+        const float* ml = p.part_ml + (size_t)hq * C * 2;
         const float* base = p.part_acc + (size_t)hq * C * p.hd + d0;
+        float M = -3.0e38f, den = 0.f;
         float o[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        for (int c0 = 0; c0 < C; c0 += 4) {
-            float4 a[4][2];
+        for (int c0 = 0; c0 < C; c0 += 8) {
+            float mm[8], ll[8];
+            float4 a[8][2];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
+            for (int k = 0; k < 8; ++k) {
                 const int ch = min(c0 + k, C - 1);
+                mm[k] = __ldcg(ml + 2 * ch);
+                ll[k] = __ldcg(ml + 2 * ch + 1);
                 a[k][0] = __ldcg((const float4*)(base + (size_t)ch * p.hd));
                 a[k][1] = __ldcg((const float4*)(base + (size_t)ch * p.hd + 4));
             }
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float w = c0 + k < C ? wh[c0 + k] : 0.f;
-                o[0] = fmaf(w, a[k][0].x, o[0]); o[1] = fmaf(w, a[k][0].y, o[1]);
-                o[2] = fmaf(w, a[k][0].z, o[2]); o[3] = fmaf(w, a[k][0].w, o[3]);
-                o[4] = fmaf(w, a[k][1].x, o[4]); o[5] = fmaf(w, a[k][1].y, o[5]);
-                o[6] = fmaf(w, a[k][1].z, o[6]); o[7] = fmaf(w, a[k][1].w, o[7]);
+            for (int k = 0; k < 8; ++k) {
+                if (c0 + k >= C) break;
+                const float Mn = fmaxf(M, mm[k]);
+                const float r = expf(M - Mn), w = expf(mm[k] - Mn);
+                M = Mn;
+                den = fmaf(den, r, w * ll[k]);
+                o[0] = fmaf(o[0], r, w * a[k][0].x); o[1] = fmaf(o[1], r, w * a[k][0].y);
+                o[2] = fmaf(o[2], r, w * a[k][0].z); o[3] = fmaf(o[3], r, w * a[k][0].w);
+                o[4] = fmaf(o[4], r, w * a[k][1].x); o[5] = fmaf(o[5], r, w * a[k][1].y);
+                o[6] = fmaf(o[6], r, w * a[k][1].z); o[7] = fmaf(o[7], r, w * a[k][1].w);
             }
         }
-        *(float4*)(c.xs + xs_pos(2 * g, p.q_dim, lq4)) = make_float4(o[0], o[1], o[2], o[3]);
-        *(float4*)(c.xs + xs_pos(2 * g + 1, p.q_dim, lq4)) = make_float4(o[4], o[5], o[6], o[7]);
+        const float inv = 1.f / den;
+        *(float4*)(c.xs + xs_pos(2 * g, p.q_dim, lq4)) = make_float4(o[0] * inv, o[1] * inv, o[2] * inv, o[3] * inv);
+        *(float4*)(c.xs + xs_pos(2 * g + 1, p.q_dim, lq4)) =
+            make_float4(o[4] * inv, o[5] * inv, o[6] * inv, o[7] * inv);
     }
     c.rstd = 1.f;
     bar_consumers();
