@@ -179,9 +179,9 @@ def test_watchdog_returns_timeout(mk):
 
 
 # ------------------------------------------------------------------ full-size models
-def _full_size(mk, name, n_forced, sms=0, prompt_len=None):
-    w = synthetic.get_workload(name)
-    weights = weights_for(name)
+def _full_size(mk, name, n_forced, sms=0, prompt_len=None, workload=None):
+    w = workload or synthetic.get_workload(name)
+    weights = synthetic.generate_weights(w) if workload else weights_for(name)
     desc = mk.make_desc(w)
     dec = mk.Decoder(desc, mk.pack_model(desc, weights), mk.make_config(sms=sms))
     prompt = synthetic.generate_prompt(w, prompt_len)
@@ -196,5 +196,23 @@ def _full_size(mk, name, n_forced, sms=0, prompt_len=None):
 @pytest.mark.parametrize("name", ["llama-1b", "llama-1b-int8", "llama-1b-int4"])
 def test_1b_teacher_forced(mk, name):
     lg, ref, ids = _full_size(mk, name, 6)
+    check_logits(lg, ref)
+    assert np.array_equal(ids, lg.argmax(axis=1))
+
+
+def test_2b_fp16_teacher_forced(mk):
+    # fp16 weights, head_dim 128, d_model 2560: GEMV rows split over two warps,
+    # the fused FFN with 10 lines per column block; the config's 512-token prompt
+    lg, ref, ids = _full_size(mk, "llama-2b-fp16", 6)
+    check_logits(lg, ref)
+    assert np.array_equal(ids, lg.argmax(axis=1))
+
+
+def test_8b_shape_teacher_forced(mk):
+    # Llama-3-8B widths (d 4096, F 14336, vocab 128256, theta 5e5, head_dim 128)
+    # at two layers so the float64 oracle stays small: 16-line column blocks,
+    # two-warp rows, the 17-bit argmax index
+    w = synthetic.get_workload("llama3-8b-8k").with_(n_layers=2, prompt_len=96, decode_steps=8)
+    lg, ref, ids = _full_size(mk, w.name, 6, workload=w)
     check_logits(lg, ref)
     assert np.array_equal(ids, lg.argmax(axis=1))
