@@ -906,12 +906,21 @@ static __device__ __forceinline__ bool attn_task(Ctx& c, const TaskRec& t, int t
 
     float kf[PPW][DPL];
     uint32_t vraw[PPW][DPL / 2];
-    auto load_tile = [&](int jt, int n) {
+    // K rows of a tile go to kf, V rows to vraw; the two halves are loaded
+    // separately so that the next tile's rows are in flight while this one
+    // is computed (V once staged in shared memory, K once the scores are done).
+    auto load_k = [&](int jt, int n) {
+#pragma unroll
+        for (int k = 0; k < PPW; ++k) {
+            const int jj = c.warp + NW * k, j = jt + jj;
+            if (jj < n && j != pos) load_kv_row<DPL>(kbase + (size_t)j * HD, c.lane, kf[k]);
+        }
+    };
+    auto load_v = [&](int jt, int n) {
 #pragma unroll
         for (int k = 0; k < PPW; ++k) {
             const int jj = c.warp + NW * k, j = jt + jj;
             if (jj < n && j != pos) {
-                load_kv_row<DPL>(kbase + (size_t)j * HD, c.lane, kf[k]);
                 if constexpr (DPL == 2) {
                     vraw[k][0] = __ldcg((const unsigned int*)(vbase + (size_t)j * HD + c.lane * 2));
                 } else {
@@ -947,7 +956,10 @@ static __device__ __forceinline__ bool attn_task(Ctx& c, const TaskRec& t, int t
     // The chunk's first cache rows are requested before the counter wait: rows
     // of earlier positions were written by earlier steps, whose writers the
     // wait of this CTA's previous task already ordered before us.
-    if (j1 > j0) load_tile(j0, min(ATTN_TILE, j1 - j0));
+    if (j1 > j0) {
+        load_k(j0, min(ATTN_TILE, j1 - j0));
+        load_v(j0, min(ATTN_TILE, j1 - j0));
+    }
     if (!wait_counters(c, t, task_id, step)) return false;
 
     for (int i = c.tid; i < (rep + 1) * half; i += NT) {
@@ -985,8 +997,9 @@ static __device__ __forceinline__ bool attn_task(Ctx& c, const TaskRec& t, int t
 
     for (int jt = j0; jt < j1; jt += ATTN_TILE) {
         const int n = min(ATTN_TILE, j1 - jt);
-        if (jt != j0) load_tile(jt, n);
+        const int jn = jt + ATTN_TILE, nn = min(ATTN_TILE, j1 - jn);  // next tile
         stage_v(jt, n);
+        if (nn > 0) load_v(jn, nn);
         // scores for (position k, head h), four heads at a time: PPW*4 partial
         // sums per lane, transposed so that lane pairs hold the totals
         for (int h0 = 0; h0 < rep; h0 += 4) {
@@ -1007,6 +1020,7 @@ static __device__ __forceinline__ bool attn_task(Ctx& c, const TaskRec& t, int t
             const int idx = c.lane >> SH, k = idx >> 2, hh = idx & 3, jj = c.warp + NW * k;
             if ((c.lane & ((1 << SH) - 1)) == 0 && h0 + hh < rep && jj < n) at.sc[(h0 + hh) * ATTN_TILE + jj] = sc;
         }
+        if (nn > 0) load_k(jn, nn);  // the scores no longer need this tile's K rows
         bar_consumers();
         if (c.warp < rep) {  // online softmax statistics: warp h owns query head h
             const int h = c.warp;
