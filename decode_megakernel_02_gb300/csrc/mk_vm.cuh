@@ -341,8 +341,9 @@ static __device__ __forceinline__ void prologue_attention(Ctx& c, int lq4) {
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const int ch = min(c0 + k, C - 1);
-                mm[k] = __ldcg(ml + 2 * ch);
-                ll[k] = __ldcg(ml + 2 * ch + 1);
+                const float2 v = __ldcg((const float2*)(ml + 2 * ch));  // (max, sum) in one load
+                mm[k] = v.x;
+                ll[k] = v.y;
                 a[k][0] = __ldcg((const float4*)(base + (size_t)ch * p.hd));
                 a[k][1] = __ldcg((const float4*)(base + (size_t)ch * p.hd + 4));
             }

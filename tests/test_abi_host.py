@@ -184,3 +184,18 @@ def test_validator_never_accepts_what_the_simulator_rejects(mk, sms, chunks, wd)
         rejected += st != mk.MK_OK
     assert not false_accepts, false_accepts[:3]
     assert rejected > 10  # the corpus does exercise the validator
+
+
+def test_tuner_agreement_rule():
+    from decode_megakernel_02_gb300 import tune
+    rng = np.random.default_rng(3)
+    ref = rng.standard_normal((5, 64))
+    assert tune.agrees(ref.copy(), ref)
+    near = ref + 0.5e-2 * np.abs(ref).max(axis=1, keepdims=True) * rng.uniform(-1, 1, ref.shape)
+    assert tune.agrees(near, ref) == bool(np.mean(near.argmax(1) == ref.argmax(1)) >= 0.99)
+    far = ref.copy()
+    far[2, 7] += 0.02 * np.abs(ref[2]).max()
+    assert not tune.agrees(far, ref)
+    bad = ref.copy()
+    bad[0, 0] = np.nan
+    assert not tune.agrees(bad, ref)

@@ -216,3 +216,14 @@ def test_8b_shape_teacher_forced(mk):
     lg, ref, ids = _full_size(mk, w.name, 6, workload=w)
     check_logits(lg, ref)
     assert np.array_equal(ids, lg.argmax(axis=1))
+
+
+def test_schedule_grid_search_on_tiny(mk, capsys):
+    # the tuner validates, agreement-checks and times each grid point
+    from decode_megakernel_02_gb300 import tune
+    import json
+    tune.main(["--workload", "tiny", "--chunks", "0,2,4", "--sms", "0,7", "--reps", "1"])
+    out = json.loads(capsys.readouterr().out)
+    assert len(out["points"]) == 6
+    assert all(p["status"] == "ok" for p in out["points"]), out["points"]
+    assert all(p["tokens_per_s"] > 0 for p in out["points"])
