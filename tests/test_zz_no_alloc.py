@@ -5,6 +5,8 @@ identical, logits within the parity tolerance, KV caches alike.
 
 The file name sorts last so that the suite also runs it after every other
 GPU test in the same process."""
+import gc
+
 import numpy as np
 import pytest
 
@@ -55,15 +57,16 @@ def _compare(mk, name, steps, cfg):
     # every buffer of the static calls exists before the first one
     lgs = [torch.full((n, w.vocab), float("nan"), dtype=torch.float32, device=dev) for n in steps]
     outs = [np.full(n, -1, np.int32) for n in steps]
+    gc.collect()  # tensors of earlier tests are freed now, not during the calls below
     torch.cuda.synchronize()
     pos, tok = len(prompt) - 1, int(prompt[-1])
     for i, n in enumerate(steps):
         alloc0 = torch.cuda.memory_allocated()
         free0 = torch.cuda.mem_get_info()[0]
         mk.decode_static(desc, dec.weights, kv_static, pos, tok, n, cfg=cfg, logits=lgs[i], out=outs[i])
-        if i > 0:  # after the first call's set-up nothing on the device grows
-            assert torch.cuda.mem_get_info()[0] == free0
-        assert torch.cuda.memory_allocated() == alloc0
+        if i > 0:  # after the first call's set-up the device's free memory does not shrink
+            assert torch.cuda.mem_get_info()[0] >= free0
+        assert torch.cuda.memory_allocated() <= alloc0  # nothing allocated through torch
         pos, tok = pos + n, int(outs[i][-1])
 
     for i in range(len(steps)):
