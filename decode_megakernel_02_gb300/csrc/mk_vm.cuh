@@ -757,6 +757,13 @@ __device__ bool gemv_run(Ctx& c, const TaskRec& t, int task_id, int step, float&
             }
         }
     }
+    // Rows shared by g > 1 warps: each warp leaves its partial sums in a
+    // [row][warp] table (the input-vector region, free once every warp holds
+    // its fragment) and the rows are finished after the loop, so the warps of
+    // a group never wait for each other per batch.
+    const bool defer = g > 1 && nrows * g <= p.xs_floats;
+    float* part = c.xs;
+    if (defer) bar_consumers();
     constexpr int B = RW >= 8 ? 3 : RW >= 4 ? 2 : RW >= 2 ? 1 : 0;  // log2(RW)
     const int my_r = c.lane >> (5 - B);                              // row of the batch this lane finishes
     const bool writer = (c.lane & ((32 >> B) - 1)) == 0;
@@ -767,7 +774,7 @@ __device__ bool gemv_run(Ctx& c, const TaskRec& t, int task_id, int step, float&
         const int row_g = row0 + rb + my_r;
         const bool has_row = rb + my_r < nrows;
         float resid = 0.f;  // residual input of this lane's row
-        if (writer && has_row) {
+        if (writer && has_row && !defer) {
             if (op == OP_DOWN || (op == OP_O && layer > 0)) {
                 resid = __ldcg(xbuf(p, layer) + row_g);
             } else if (op == OP_O) {
@@ -805,7 +812,7 @@ __device__ bool gemv_run(Ctx& c, const TaskRec& t, int task_id, int step, float&
         __syncwarp();  // the slot is reused by a later issue of this warp
         if (++c.rs == NB) c.rs = 0;
         float tot = transpose_reduce<RW>(v, c.lane);
-        if (g > 1) {
+        if (g > 1 && !defer) {
             float* scr = &c.sh->gpart[grp][par][0][0];  // [row][warp]
             if (writer) scr[my_r * NW + wig] = tot;
             bar_group(2 + grp, S);
@@ -820,6 +827,10 @@ __device__ bool gemv_run(Ctx& c, const TaskRec& t, int task_id, int step, float&
 #pragma unroll
             for (int r = 1; r < RW; ++r) scale = my_r == r ? rsv[r] : scale;
             tot *= scale;
+        }
+        if (defer) {
+            if (writer && has_row) part[(rb + my_r) * g + wig] = tot;
+            continue;
         }
         if (op == OP_GU || op == OP_FFN) {  // rows alternate gate, up: the up total sits one row further
             const float up = __shfl_down_sync(0xFFFFFFFFu, tot, 32 >> B);
@@ -840,6 +851,36 @@ __device__ bool gemv_run(Ctx& c, const TaskRec& t, int task_id, int step, float&
                 float* xo = xbuf(p, layer);
                 xo[row_g] = resid + tot;
                 if (op == OP_O && p.fused) xbuf(p, layer + 1)[row_g] = resid + tot;  // the FFN adds into this copy
+            }
+        }
+    }
+    if (defer) {  // finish the shared rows: sum the warps' partials, then the epilogue
+        bar_consumers();
+        for (int rr = c.tid; rr < nrows; rr += NT) {
+            const int row_g = row0 + rr;
+            float tot = 0.f;
+            for (int w = 0; w < g; ++w) tot += part[rr * g + w];
+            if (op == OP_GU || op == OP_FFN) {  // gate rows are even, their up row follows
+                if (!(rr & 1) && rr + 1 < nrows) {
+                    float up = 0.f;
+                    for (int w = 0; w < g; ++w) up += part[(rr + 1) * g + w];
+                    if (op == OP_GU) p.h[row_g >> 1] = silu(tot) * up;
+                    else ffn_h(c)[rr >> 1] = silu(tot) * up;
+                }
+            } else if (op == OP_LM) {
+                if (p.logits) p.logits[(size_t)step * p.V + row_g] = tot;
+                if (tot > best_v) {  // rows ascend per thread: the first maximum is kept
+                    best_v = tot;
+                    best_i = row_g;
+                }
+            } else if (op == OP_QKV) {
+                p.qkv[row_g] = tot;
+            } else {  // O and down: residual add
+                float resid;
+                if (op == OP_DOWN || layer > 0) resid = __ldcg(xbuf(p, layer) + row_g);
+                else resid = base_to_f32<BASE>(__ldg((const uint16_t*)(p.w + p.embed) + (size_t)tok * p.d + row_g));
+                xbuf(p, layer)[row_g] = resid + tot;
+                if (op == OP_O && p.fused) xbuf(p, layer + 1)[row_g] = resid + tot;
             }
         }
     }
