@@ -29,7 +29,11 @@ mk_status resolve_config(const mk_model_desc* d, const mk_schedule_config* cfg, 
                          Config* out);
 
 // IR buffers of the decode path.
-enum Buf : int32_t { B_X = 0, B_QKV, B_PART, B_H, B_LOGITS, B_KEY, B_OUT, B_KV, B_COUNT };
+enum Buf : int32_t { B_X = 0, B_QKV, B_PART, B_H, B_LOGITS, B_KEY, B_OUT, B_KV, B_ATT, B_COUNT };
+
+// Whether the split-KV partials are merged by per-group OP_MERGE tasks (true
+// when every O CTA would otherwise read more than 64 KB of partials).
+bool merge_tasks(const mk_model_desc* d, const Config& c);
 
 // Result of lowering: the IR (owning storage) and the matching device tables.
 struct Lowering {
@@ -55,7 +59,7 @@ mk_status validate_ir(const mk_ir* ir, std::string* why);
 
 // Workspace layout (byte offsets).
 struct WsLayout {
-    int64_t status, counters, key, recs, queue_off, inv_freq, x, qkv, part_ml, part_acc,
+    int64_t status, counters, key, recs, queue_off, inv_freq, x, qkv, part_ml, part_acc, att,
         h, tok, out_ids, total;
 };
 WsLayout ws_layout(const mk_model_desc* d, const Config& c, int64_t n_tasks, int32_t n_counters);

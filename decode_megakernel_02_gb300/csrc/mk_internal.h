@@ -17,8 +17,9 @@ enum Op : int32_t {
     OP_DOWN = 5,  // Wdown GEMV rows + residual add -> x
     OP_LM = 6,    // final RMSNorm + LM-head rows + block argmax -> logits, key
     OP_FIN = 7,   // read the step's argmax key -> out id
-    OP_FFN = 8    // RMSNorm prologue + gate/up rows + SwiGLU (kept on chip) + the down
+    OP_FFN = 8,   // RMSNorm prologue + gate/up rows + SwiGLU (kept on chip) + the down
                   // projection's columns of those units, red.add into the next residual
+    OP_MERGE = 9  // split-KV merge of one KV group's query heads -> att (O then reads att)
 };
 
 constexpr int NT = 256;                 // threads per CTA (eight warps)
@@ -111,6 +112,8 @@ struct VmParams {
     float* x;                  // residual stream [2][d]
     float* qkv;                // [q_dim + 2 kv_dim]
     float* part_ml;            // [Hq][C][2]  (running max, sum)
+    float* att;                // [q_dim] merged attention output (merge tasks; else unused)
+    int32_t merge_tasks;       // 1: OP_MERGE tasks merge the partials and O reads att
     float* part_acc;           // [Hq][C][hd]
     float* h;                  // SwiGLU output [F]
     const int32_t* forced;     // nullable: token fed at step s

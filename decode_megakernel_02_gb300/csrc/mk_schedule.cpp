@@ -140,6 +140,10 @@ mk_ir_access A(int buf, int kind, int64_t lo, int64_t hi, int64_t stride = 0, in
 // step's write lands at P0 + e.
 static constexpr int64_t P0 = 1;
 
+bool merge_tasks(const mk_model_desc* d, const Config& c) {
+    return (int64_t)d->n_q_heads * c.C * (d->head_dim + 2) * 4 > 64 * 1024;
+}
+
 mk_status lower(const mk_model_desc* d, const Config& c, Lowering* lw) {
     *lw = Lowering{};
     Builder B{d, c, lw, std::vector<int64_t>(c.sms, 0), c.sms};
@@ -149,9 +153,13 @@ mk_status lower(const mk_model_desc* d, const Config& c, Lowering* lw) {
     const int64_t qd = (int64_t)Hq * hd, kd = (int64_t)Hkv * hd, dm = d->d_model, F = d->d_ffn,
                   V = d->vocab;
     const BlobLayout bl = blob_layout(d);
-    const int CTR_LM = 5 * L;
-    lw->n_counters = 5 * L + 1;
-    auto ctr = [&](int l, int k) { return 5 * l + k; };
+    // Counters per layer: 0 QKV, 1 attention done, 2 O, 3 FFN / gate-up, 4 down,
+    // 5 + g chunks of KV group g (merge tasks only).
+    const int CS = 5 + Hkv;
+    const int CTR_LM = CS * L;
+    lw->n_counters = CS * L + 1;
+    auto ctr = [&](int l, int k) { return CS * l + k; };
+    const bool mt = merge_tasks(d, c);
     const int64_t ML_BYTES = (int64_t)Hq * C * 2 * 4;
     // Residual buffers: x[2][d].  With the fused FFN the layer-l input lives in
     // x[l & 1]; O(l) writes x_mid into x[l & 1] and x[(l + 1) & 1], and the
@@ -228,7 +236,7 @@ mk_status lower(const mk_model_desc* d, const Config& c, Lowering* lw) {
                 t.row0 = g;
                 t.nrows = ch;
                 t.K = C;
-                t.signal_ctr = ctr(l, 1);
+                t.signal_ctr = mt ? ctr(l, 5 + g) : ctr(l, 1);
                 std::vector<mk_ir_access> acc;
                 acc.push_back(A(B_QKV, MK_ACC_READ, 4 * (int64_t)g * rep * hd, 4 * (int64_t)(g + 1) * rep * hd));
                 acc.push_back(A(B_QKV, MK_ACC_READ, 4 * (qd + (int64_t)g * hd), 4 * (qd + (int64_t)(g + 1) * hd)));
@@ -255,6 +263,29 @@ mk_status lower(const mk_model_desc* d, const Config& c, Lowering* lw) {
             }
         }
         B.set_wait(ids, prev_ctr, (int)prev.size(), 0);
+        if (mt) {
+            // ---- merge of each KV group's chunks, on the CTA of the group's last
+            // chunk right after it: att gets the group's query-head outputs
+            std::vector<int> mids;
+            for (int g = 0; g < Hkv; ++g) {
+                const int last = ids[(size_t)g * C + C - 1];
+                DevTask t{};
+                t.op = OP_MERGE;
+                t.layer = l;
+                t.row0 = g;
+                t.K = C;
+                t.signal_ctr = ctr(l, 1);
+                std::vector<mk_ir_access> acc;
+                const int64_t h0 = (int64_t)g * rep, h1 = h0 + rep;
+                acc.push_back(A(B_PART, MK_ACC_READ, h0 * C * 2 * 4, h1 * C * 2 * 4));
+                acc.push_back(A(B_PART, MK_ACC_READ, ML_BYTES + h0 * C * hd * 4, ML_BYTES + h1 * C * hd * 4));
+                acc.push_back(A(B_ATT, MK_ACC_WRITE, h0 * hd * 4, h1 * hd * 4));
+                const int id = B.add_task(lw->tasks[last].sm, t, acc);
+                B.set_wait({id}, ctr(l, 5 + g), C, 0);
+                mids.push_back(id);
+            }
+            ids = mids;
+        }
         prev = ids;
         prev_ctr = ctr(l, 1);
 
@@ -264,7 +295,8 @@ mk_status lower(const mk_model_desc* d, const Config& c, Lowering* lw) {
             int64_t r0 = p.second.first, r1 = p.second.second;
             DevTask t = gemv_task(OP_O, l, r0, r1 - r0, qd, bl.row_o, lb + bl.l_o, 1, ctr(l, 2));
             std::vector<mk_ir_access> acc;
-            acc.push_back(A(B_PART, MK_ACC_READ, 0, ML_BYTES + (int64_t)Hq * C * hd * 4));
+            if (mt) acc.push_back(A(B_ATT, MK_ACC_READ, 0, 4 * qd));
+            else acc.push_back(A(B_PART, MK_ACC_READ, 0, ML_BYTES + (int64_t)Hq * C * hd * 4));
             if (l == 0) acc.push_back(A(B_KEY, MK_ACC_READ, 0, 8));
             acc.push_back(A(B_X, MK_ACC_WRITE, xb(l) + 4 * r0, xb(l) + 4 * r1));
             if (fused) acc.push_back(A(B_X, MK_ACC_WRITE, xb(l + 1) + 4 * r0, xb(l + 1) + 4 * r1));
@@ -732,6 +764,7 @@ WsLayout ws_layout(const mk_model_desc* d, const Config& c, int64_t n_tasks, int
     w.x = take((int64_t)d->d_model * 2 * 4);
     w.qkv = take((qd + 2 * kd) * 4);
     w.part_ml = take((int64_t)d->n_q_heads * c.C * 2 * 4);
+    w.att = take((int64_t)d->n_q_heads * d->head_dim * 4);
     w.part_acc = take((int64_t)d->n_q_heads * c.C * d->head_dim * 4);
     w.h = take((int64_t)d->d_ffn * 4);
     w.tok = take((int64_t)d->max_seq * 4 + 16);

@@ -369,6 +369,55 @@ static __device__ __forceinline__ void prologue_attention(Ctx& c, int lq4) {
     bar_consumers();
 }
 
+// OP_MERGE: the split-KV merge of KV group g's query heads, written once to
+// att[g * rep * hd ...] for every O task to read.  Each thread produces four
+// outputs from all chunks, with the running maximum of prologue_attention.
+static __device__ __forceinline__ void merge_task(Ctx& c, const TaskRec& t) {
+    const VmParams& p = *c.p;
+    const int C = p.C, rep = p.Hq / p.Hkv, g = t.row0;
+    for (int u = c.tid; u < rep * (p.hd >> 2); u += NT) {
+        const int hq = g * rep + (4 * u) / p.hd, d0 = (4 * u) % p.hd;
+        const float* ml = p.part_ml + (size_t)hq * C * 2;
+        const float* base = p.part_acc + (size_t)hq * C * p.hd + d0;
+        float M = -3.0e38f, den = 0.f;
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c0 = 0; c0 < C; c0 += 8) {
+            float2 mlv[8];
+            float4 a[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int ch = min(c0 + k, C - 1);
+                mlv[k] = __ldcg((const float2*)(ml + 2 * ch));
+                a[k] = __ldcg((const float4*)(base + (size_t)ch * p.hd));
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                if (c0 + k >= C) break;
+                const float Mn = fmaxf(M, mlv[k].x);
+                const float r = expf(M - Mn), w = expf(mlv[k].x - Mn);
+                M = Mn;
+                den = fmaf(den, r, w * mlv[k].y);
+                o.x = fmaf(o.x, r, w * a[k].x);
+                o.y = fmaf(o.y, r, w * a[k].y);
+                o.z = fmaf(o.z, r, w * a[k].z);
+                o.w = fmaf(o.w, r, w * a[k].w);
+            }
+        }
+        const float inv = 1.f / den;
+        *(float4*)(p.att + (size_t)hq * p.hd + d0) = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+    }
+}
+
+// O prologue when merge tasks ran: the merged attention output, copied from
+// att into c.xs (planes).
+static __device__ __forceinline__ void prologue_att_copy(Ctx& c, int lq4) {
+    const VmParams& p = *c.p;
+    for (int u = c.tid; u < (p.q_dim >> 2); u += NT)
+        *(float4*)(c.xs + xs_pos(u, p.q_dim, lq4)) = __ldcg((const float4*)(p.att + 4 * u));
+    c.rstd = 1.f;
+    bar_consumers();
+}
+
 // ------------------------------------------------------------------ GEMV rows
 // Packed fp32 FMA on register pairs (sm_100+): {d.x, d.y} = {a.x*b.x + c.x, a.y*b.y + c.y}.
 __device__ __forceinline__ unsigned long long ffma2(unsigned long long a, unsigned long long b,
@@ -732,7 +781,10 @@ __device__ bool gemv_run(Ctx& c, const TaskRec& t, int task_id, int step, float&
         case OP_LM:
             prologue_rmsnorm<BASE>(c, xbuf(p, p.L), nullptr, (const uint16_t*)(p.w + p.final_norm), p.d, p.eps, LQ4);
             break;
-        case OP_O: prologue_attention(c, LQ4); break;
+        case OP_O:
+            if (p.merge_tasks) prologue_att_copy(c, LQ4);
+            else prologue_attention(c, LQ4);
+            break;
         default:  // down reads h straight from device memory
             xin = p.h;
             from_global = true;
@@ -1131,6 +1183,7 @@ __device__ __forceinline__ void consumer(Ctx& c) {
                 }
             } else {
                 ok = t.op == OP_ATTN ? attn_task<HD>(c, t, tid_, s) : wait_counters(c, t, tid_, s);
+                if (ok && t.op == OP_MERGE) merge_task(c, t);
                 if (ok && t.op == OP_FIN && c.tid == 0 && !p.skip_lm) {
                     const unsigned long long k = __ldcg(p.key);
                     if ((k >> 49) != key_tag((uint32_t)(p.epoch0 + s))) {

@@ -110,6 +110,7 @@ def test_packed_down_column_blocks(mk):
 
 # ------------------------------------------------------------------ validator
 @pytest.mark.parametrize("name,sms,chunks", [("tiny", 152, 0), ("tiny", 7, 3), ("tiny", 1, 1), ("tiny", 2, 4),
+                                             ("tiny", 152, 64),
                                              ("llama-1b", 152, 0), ("llama-1b-int8", 152, 0),
                                              ("llama-1b-int4", 64, 2), ("llama-2b-fp16", 152, 0)])
 def test_validator_accepts_real_lowerings(mk, name, sms, chunks):
@@ -169,7 +170,7 @@ def _mutants(ir, rng, n):
     return out
 
 
-@pytest.mark.parametrize("sms,chunks,wd", [(2, 1, None), (3, 2, None), (2, 1, "int8")])
+@pytest.mark.parametrize("sms,chunks,wd", [(2, 1, None), (3, 2, None), (2, 1, "int8"), (2, 64, None)])
 def test_validator_never_accepts_what_the_simulator_rejects(mk, sms, chunks, wd):
     ir = _small_ir(mk, sms, chunks, wd)
     assert S.verdict(ir)[0], S.verdict(ir)[1]

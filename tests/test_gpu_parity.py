@@ -90,8 +90,9 @@ def test_device_dequant_bit_exact(mk, wd):
 
 
 # ------------------------------------------------------------------ tiny model
-@pytest.mark.parametrize("sms,chunks", [(0, 0), (7, 3), (1, 1), (152, 5)])
+@pytest.mark.parametrize("sms,chunks", [(0, 0), (7, 3), (1, 1), (152, 5), (0, 64)])
 def test_tiny_teacher_forced(mk, sms, chunks):
+    # (0, 64): enough partials that per-group merge tasks run (most chunks empty)
     w = synthetic.get_workload("tiny")
     weights = weights_for("tiny")
     desc = mk.make_desc(w)
