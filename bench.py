@@ -4,8 +4,9 @@ A step is one mk_decode launch of the workload's full decode (the 1B bf16
 workload: 256 greedy tokens after a 128-token prompt), rewound to the end of
 the prompt before every step, with weights (2.2 GB, larger than L2) and KV
 cache resident in HBM.  `value` is decode tokens/s from CUDA events on the
-launching stream; `e2e` is the same metric through the host-buffer C-ABI call
-(mk_decode: launch, device->host copy of the ids, stream sync) on the host
+launching stream; `e2e` is the same metric through the host-buffer C-ABI calls
+(mk_set_state with the step's pending token and position, then mk_decode:
+launch, device->host copy of the ids and status, stream sync) on the host
 clock.  `roofline` reports algorithmic bytes per launch (GEMV weights incl.
 quantisation scales, embedding row, norm gains, KV reads and writes at each
 step's position) over the launch time, against the measured HBM copy
@@ -285,8 +286,8 @@ def main():
     host_ids = np.empty(n_tok, np.int32)
     e2e_t = []
     for i in range(args.warmup + args.steps):
-        dec.set_state(pos0, pending)
         t0 = time.perf_counter()
+        dec.set_state(pos0, pending)  # the step's input: the pending token and its position
         dec.decode(n_tok, out=host_ids)
         if i >= args.warmup:
             e2e_t.append(time.perf_counter() - t0)
@@ -309,7 +310,8 @@ def main():
                          "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
                          "algorithmic_bytes_per_launch": alg_bytes,
                          "frac_of_8tbs": achieved / 8000.0},
-            "e2e": {"value": e2e_rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 4 * n_tok + 16},
+            "e2e": {"value": e2e_rate, "unit": UNIT, "h2d_bytes_per_step": 8, "d2h_bytes_per_step": 4 * n_tok + 16,
+                    "inputs": "pending token and position (2 x int32), passed by value in the launch parameters"},
             "gpu_launches": int(launches), "launch": info, "kernel_source": kernel_source_hash()}
     clocks = clk.summary()
     if clocks:
