@@ -163,7 +163,7 @@ struct Ctx {
     float rstd;         // scale of xs applied when the fragments are loaded (RMSNorm)
     int tid, lane, warp;
     bool abort;
-    bool deferred;      // the last batch of the task issued no copy: issue it after the signal
+    int deferred;       // batches of this task that issued no copy: issued after the signal
 };
 
 __device__ __forceinline__ bool aborted(const VmParams& p) { return ld_volatile(p.status) != 0; }
@@ -639,15 +639,30 @@ __device__ __forceinline__ void stream_issue(Ctx& c) {
     cp_async_commit();
 }
 
+// Wait until at most n (0 <= n <= N) of the warp's copy groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait_upto(int n) {
+    if constexpr (N == 0) {
+        cp_async_wait<0>();
+    } else {
+        if (n >= N) cp_async_wait<N>();
+        else cp_async_wait_upto<N - 1>(n);
+    }
+}
+
 // Wait for the ring slot of the batch about to be computed.  NB - 1 batches
-// run ahead; a task's last batch (last = true) defers its issue until after
-// the task's signal, so the copy's back-pressure stays off the signal's path.
+// run ahead.  A batch may defer its issue until after the task's signal
+// (defer = true), which keeps the copy's back-pressure off the signal's path:
+// a task's last batch always does, and so does every batch of a QKV task
+// whose warp computes at most NB - 1 batches of it (each of them was issued
+// before the task began).  Callers never follow a deferred batch with one that
+// issues, so with k issues pending NB - 1 - k groups follow the current one.
 template <int WT>
-__device__ __forceinline__ void ring_acquire(Ctx& c, bool last) {
+__device__ __forceinline__ void ring_acquire(Ctx& c, bool defer) {
     constexpr int NB = ring_slots<WT>();
-    if (last) {
-        c.deferred = true;
-        cp_async_wait<NB - 2>();
+    if (defer) {
+        ++c.deferred;
+        cp_async_wait_upto<NB - 2>(NB - 1 - c.deferred);
     } else {
         stream_issue<WT>(c);
         cp_async_wait<NB - 1>();
@@ -821,6 +836,9 @@ __device__ bool gemv_run(Ctx& c, const TaskRec& t, int task_id, int step, float&
     const bool writer = (c.lane & ((32 >> B) - 1)) == 0;
     int par = 0;
     const int nbatches = (nrows + RW - 1) / RW;
+    // QKV leads the layer's latency-bound chain: when all of this warp's
+    // batches are already in flight, none of them issues a copy before the signal.
+    const bool defer_all = op == OP_QKV && (nbatches - grp + ngroups - 1) / ngroups <= ring_slots<WT>() - 1;
     for (int q = grp; q < nbatches; q += ngroups) {
         const int rb = q * RW;
         const int row_g = row0 + rb + my_r;
@@ -835,7 +853,7 @@ __device__ bool gemv_run(Ctx& c, const TaskRec& t, int task_id, int step, float&
             }
         }
         // keep NB - 1 batches in flight beyond this one, then wait for this one
-        ring_acquire<WT>(c, q + ngroups >= nbatches && op != OP_FFN);
+        ring_acquire<WT>(c, op != OP_FFN && (q + ngroups >= nbatches || defer_all));
         const uint8_t* slot = c.ring + (size_t)c.rs * ring_slot_bytes<WT>();
         float v[RW], rsv[RW];
 #pragma unroll
@@ -1219,10 +1237,7 @@ __device__ __forceinline__ void consumer(Ctx& c) {
                 atomicMax(p.key, key);
             }
             signal_counter(c, t, sw);
-            if (c.deferred) {  // the copy the task's last batch skipped
-                stream_issue<WT>(c);
-                c.deferred = false;
-            }
+            for (; c.deferred > 0; --c.deferred) stream_issue<WT>(c);  // the copies the task skipped
             if (p.trace && c.tid == 0) {
                 const int k = s * c.nrec + qi;
                 if (k < p.trace_cap) {
@@ -1254,7 +1269,7 @@ __global__ void __launch_bounds__(THREADS, 1) vm_kernel(const VmParams p) {
     c.ring = smem_raw + ring_offset(p.xs_floats, p.tab_cap) + (size_t)c.warp * ring_slots<WT>() * ring_slot_bytes<WT>();
     c.rstd = 1.f;
     c.abort = false;
-    c.deferred = false;
+    c.deferred = 0;
     c.rs = 0;
     c.q0 = p.queue_off[blockIdx.x];
     c.nrec = min(p.queue_off[blockIdx.x + 1] - c.q0, p.tab_cap);  // the host sizes tab_cap to the longest queue
