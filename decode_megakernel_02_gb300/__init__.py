@@ -63,7 +63,7 @@ class mk_ir(ctypes.Structure):
                 ("n_buffers", ctypes.c_int32), ("n_acc", ctypes.c_int32),
                 ("tasks", ctypes.POINTER(mk_ir_task)), ("acc", ctypes.POINTER(mk_ir_access)),
                 ("queue", ctypes.POINTER(ctypes.c_int32)), ("queue_off", ctypes.POINTER(ctypes.c_int32)),
-                ("buf_flags", ctypes.POINTER(ctypes.c_int32))]
+                ("buf_flags", ctypes.POINTER(ctypes.c_int32)), ("ctr_buf", ctypes.POINTER(ctypes.c_int32))]
 
 
 _P = ctypes.c_void_p
@@ -234,8 +234,9 @@ def ir_to_dict(ir):
                       "signal": t.signal_ctr, "acc": acc})
     queues = [[ir.queue[j] for j in range(ir.queue_off[s], ir.queue_off[s + 1])] for s in range(ir.n_sms)]
     outputs = [b for b in range(ir.n_buffers) if ir.buf_flags[b] & MK_BUF_OUTPUT]
+    tagged = {c: ir.ctr_buf[c] for c in range(ir.n_counters) if ir.ctr_buf and ir.ctr_buf[c] >= 0}
     return {"n_sms": ir.n_sms, "n_counters": ir.n_counters, "n_buffers": ir.n_buffers, "outputs": outputs,
-            "tasks": tasks, "queues": queues}
+            "tasks": tasks, "queues": queues, "tagged": tagged}
 
 
 def mk_validate_ir(irdict):
@@ -266,7 +267,10 @@ def mk_validate_ir(irdict):
     queue_off = (_I32 * len(offs))(*offs)
     nb = irdict["n_buffers"]
     flags = (_I32 * max(1, nb))(*[MK_BUF_OUTPUT if b in irdict.get("outputs", []) else 0 for b in range(nb)])
-    ir = mk_ir(irdict["n_sms"], T, irdict["n_counters"], nb, len(accs), tasks, acc, queue, queue_off, flags)
+    nc = irdict["n_counters"]
+    tagged = irdict.get("tagged", {})
+    ctr_buf = (_I32 * max(1, nc))(*[tagged.get(c, -1) for c in range(nc)])
+    ir = mk_ir(irdict["n_sms"], T, nc, nb, len(accs), tasks, acc, queue, queue_off, flags, ctr_buf)
     why = ctypes.create_string_buffer(1024)
     st = load().mk_validate_ir(ctypes.byref(ir), why, 1024)
     return st, why.value.decode()

@@ -42,6 +42,11 @@ struct Lowering {
     std::vector<std::vector<int32_t>> queues;
     std::vector<DevTask> dev;
     int32_t n_counters = 0;
+    // Per counter: -1, or the buffer whose tagged values carry it.  Such a
+    // counter has no memory word: its producers' writes of that buffer carry
+    // the step's tag and its waiters poll the values they read, so the device
+    // records keep neither the signal nor the wait.
+    std::vector<int32_t> ctr_buf;
     int64_t bytes_per_sm_max = 0, bytes_per_sm_min = 0;
 };
 mk_status lower(const mk_model_desc* d, const Config& c, Lowering* out);

@@ -10,7 +10,7 @@ namespace mk {
 // Instructions of the VM (AutoMegaKernel explainer, "Methodology", Layer 1:
 // GEMV, attention, RMSNorm ... micro-kernels behind one task ABI).
 enum Op : int32_t {
-    OP_QKV = 1,   // RMSNorm prologue + [Wq;Wk;Wv] GEMV rows -> qkv (fp32)
+    OP_QKV = 1,   // RMSNorm prologue + [Wq;Wk;Wv] GEMV rows -> qkv (fp32, tagged)
     OP_ATTN = 2,  // RoPE + KV append + split-KV GQA attention chunk -> partials
     OP_O = 3,     // merge partials + Wo GEMV rows + residual add -> x
     OP_GU = 4,    // RMSNorm prologue + interleaved gate/up rows + SwiGLU -> h
@@ -109,8 +109,8 @@ struct VmParams {
     const TaskRec* recs;       // every CTA's queue, concatenated in queue order
     const int32_t* queue_off;  // [n_sms + 1]: CTA b owns recs[queue_off[b] .. queue_off[b+1])
     const float* inv_freq;     // [hd/2]
-    float* x;                  // residual stream [2][d]
-    float* qkv;                // [q_dim + 2 kv_dim]
+    float* x;                  // residual stream [2][d], then x_mid [d]
+    unsigned long long* qkv;   // [q_dim + 2 kv_dim] tagged values: fp32 bits | tag << 32
     float* part_ml;            // [Hq][C][2]  (running max, sum)
     float* att;                // [q_dim] merged attention output (merge tasks; else unused)
     int32_t merge_tasks;       // 1: OP_MERGE tasks merge the partials and O reads att

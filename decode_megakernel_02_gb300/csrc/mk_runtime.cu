@@ -83,6 +83,8 @@ mk_status reset_sync_state(mk_handle* h) {
     CK(h, cudaMemsetAsync(h->wsp + h->ws.status, 0, 16, h->st));
     CK(h, cudaMemsetAsync(h->wsp + h->ws.counters, 0, (size_t)h->n_counters * CTR_STRIDE * 4, h->st));
     CK(h, cudaMemsetAsync(h->wsp + h->ws.key, 0, 8, h->st));
+    // tagged values: tags restart with the epoch, so no stale word may match
+    CK(h, cudaMemsetAsync(h->wsp + h->ws.qkv, 0, (size_t)(h->ws.part_ml - h->ws.qkv), h->st));
     h->epoch = 0;
     h->dirty = false;
     return MK_OK;
@@ -104,7 +106,7 @@ mk_status launch(mk_handle* h, int n_steps, const int32_t* forced, int32_t* out_
     p.queue_off = (const int32_t*)(h->wsp + h->ws.queue_off);
     p.inv_freq = (const float*)(h->wsp + h->ws.inv_freq);
     p.x = (float*)(h->wsp + h->ws.x);
-    p.qkv = (float*)(h->wsp + h->ws.qkv);
+    p.qkv = (unsigned long long*)(h->wsp + h->ws.qkv);
     p.part_ml = (float*)(h->wsp + h->ws.part_ml);
     p.part_acc = (float*)(h->wsp + h->ws.part_acc);
     p.att = (float*)(h->wsp + h->ws.att);

@@ -158,6 +158,7 @@ mk_status lower(const mk_model_desc* d, const Config& c, Lowering* lw) {
     const int CS = 5 + Hkv;
     const int CTR_LM = CS * L;
     lw->n_counters = CS * L + 1;
+    lw->ctr_buf.assign(lw->n_counters, -1);
     auto ctr = [&](int l, int k) { return CS * l + k; };
     const bool mt = merge_tasks(d, c);
     const int64_t ML_BYTES = (int64_t)Hq * C * 2 * 4;
@@ -166,6 +167,7 @@ mk_status lower(const mk_model_desc* d, const Config& c, Lowering* lw) {
     // OP_FFN tasks add their down-projection partials into x[(l + 1) & 1].
     const bool fused = bl.down_cols;
     auto xb = [&](int l) -> int64_t { return fused ? (int64_t)(l & 1) * 4 * dm : 0; };
+    const int64_t xm = 8 * dm;  // x_mid: written by O, read by the FFN side
 
     auto gemv_task = [&](int op, int l, int64_t row0, int64_t nrows, int64_t K, int64_t rb,
                          int64_t region, int unit_rows, int signal) {
@@ -200,7 +202,7 @@ mk_status lower(const mk_model_desc* d, const Config& c, Lowering* lw) {
             DevTask t = gemv_task(OP_QKV, l, r0, r1 - r0, dm, bl.row_qkv, lb + bl.l_qkv, 1, ctr(l, 0));
             std::vector<mk_ir_access> acc;
             acc.push_back(l == 0 ? A(B_KEY, MK_ACC_READ, 0, 8) : A(B_X, MK_ACC_READ, xb(l), xb(l) + 4 * dm));
-            acc.push_back(A(B_QKV, MK_ACC_WRITE, 4 * r0, 4 * r1));
+            acc.push_back(A(B_QKV, MK_ACC_WRITE, 8 * r0, 8 * r1));
             ids.push_back(B.add_task(p.first, t, acc));
         }
         if (l == 0) {
@@ -211,6 +213,9 @@ mk_status lower(const mk_model_desc* d, const Config& c, Lowering* lw) {
         }
         prev = ids;
         prev_ctr = ctr(l, 0);
+        std::vector<char> has_qkv(c.sms, 0);
+        for (int id : ids) has_qkv[lw->tasks[id].sm] = 1;
+        bool tag_ok = true;  // every CTA of this layer's attention, merge and O tasks ran a QKV task
 
         // ---- attention: one task per (kv head, chunk), placed on the least-loaded
         // CTAs, no two on one CTA while free CTAs remain (they run in parallel)
@@ -238,10 +243,10 @@ mk_status lower(const mk_model_desc* d, const Config& c, Lowering* lw) {
                 t.K = C;
                 t.signal_ctr = mt ? ctr(l, 5 + g) : ctr(l, 1);
                 std::vector<mk_ir_access> acc;
-                acc.push_back(A(B_QKV, MK_ACC_READ, 4 * (int64_t)g * rep * hd, 4 * (int64_t)(g + 1) * rep * hd));
-                acc.push_back(A(B_QKV, MK_ACC_READ, 4 * (qd + (int64_t)g * hd), 4 * (qd + (int64_t)(g + 1) * hd)));
-                acc.push_back(A(B_QKV, MK_ACC_READ, 4 * (qd + kd + (int64_t)g * hd),
-                                4 * (qd + kd + (int64_t)(g + 1) * hd)));
+                acc.push_back(A(B_QKV, MK_ACC_READ, 8 * (int64_t)g * rep * hd, 8 * (int64_t)(g + 1) * rep * hd));
+                acc.push_back(A(B_QKV, MK_ACC_READ, 8 * (qd + (int64_t)g * hd), 8 * (qd + (int64_t)(g + 1) * hd)));
+                acc.push_back(A(B_QKV, MK_ACC_READ, 8 * (qd + kd + (int64_t)g * hd),
+                                8 * (qd + kd + (int64_t)(g + 1) * hd)));
                 // The cache rows of earlier positions are read from before the
                 // task's own wait (their writers precede this CTA's previous
                 // task), so the read belongs to that previous task.
@@ -260,6 +265,7 @@ mk_status lower(const mk_model_desc* d, const Config& c, Lowering* lw) {
                     acc.push_back(A(B_PART, MK_ACC_WRITE, ac, ac + hd * 4));
                 }
                 ids.push_back(B.add_task(sm, t, acc));
+                tag_ok = tag_ok && has_qkv[sm];
             }
         }
         B.set_wait(ids, prev_ctr, (int)prev.size(), 0);
@@ -281,6 +287,7 @@ mk_status lower(const mk_model_desc* d, const Config& c, Lowering* lw) {
                 acc.push_back(A(B_PART, MK_ACC_READ, ML_BYTES + h0 * C * hd * 4, ML_BYTES + h1 * C * hd * 4));
                 acc.push_back(A(B_ATT, MK_ACC_WRITE, h0 * hd * 4, h1 * hd * 4));
                 const int id = B.add_task(lw->tasks[last].sm, t, acc);
+                tag_ok = tag_ok && has_qkv[lw->tasks[last].sm];
                 B.set_wait({id}, ctr(l, 5 + g), C, 0);
                 mids.push_back(id);
             }
@@ -298,11 +305,18 @@ mk_status lower(const mk_model_desc* d, const Config& c, Lowering* lw) {
             if (mt) acc.push_back(A(B_ATT, MK_ACC_READ, 0, 4 * qd));
             else acc.push_back(A(B_PART, MK_ACC_READ, 0, ML_BYTES + (int64_t)Hq * C * hd * 4));
             if (l == 0) acc.push_back(A(B_KEY, MK_ACC_READ, 0, 8));
-            acc.push_back(A(B_X, MK_ACC_WRITE, xb(l) + 4 * r0, xb(l) + 4 * r1));
+            else acc.push_back(A(B_X, MK_ACC_READ, xb(l) + 4 * r0, xb(l) + 4 * r1));  // residual
+            acc.push_back(A(B_X, MK_ACC_WRITE, xm + 4 * r0, xm + 4 * r1));
             if (fused) acc.push_back(A(B_X, MK_ACC_WRITE, xb(l + 1) + 4 * r0, xb(l + 1) + 4 * r1));
             ids.push_back(B.add_task(p.first, t, acc));
+            tag_ok = tag_ok && has_qkv[p.first];
         }
         B.set_wait(ids, prev_ctr, (int)prev.size(), 0);
+        // The attention tasks read q/k/v as tagged values and need no counter
+        // when every later task of the layer sits on a CTA whose QKV task
+        // already acquired the previous layer's results: then the tags order
+        // nothing that the counter chain must carry.
+        if (tag_ok) lw->ctr_buf[ctr(l, 0)] = B_QKV;
         prev = ids;
         prev_ctr = ctr(l, 2);
 
@@ -319,7 +333,7 @@ mk_status lower(const mk_model_desc* d, const Config& c, Lowering* lw) {
                     const int64_t u0 = b0 * FFN_BLOCK, u1 = b1 * FFN_BLOCK;
                     DevTask t = gemv_task(OP_FFN, l, 2 * u0, 2 * (u1 - u0), dm, bl.row_gu, lb + bl.l_gu, 2, ctr(l, 3));
                     std::vector<mk_ir_access> acc;
-                    acc.push_back(A(B_X, MK_ACC_READ, xb(l), xb(l) + 4 * dm));
+                    acc.push_back(A(B_X, MK_ACC_READ, xm, xm + 4 * dm));
                     acc.push_back(A(B_X, MK_ACC_ATOMIC, xb(l + 1), xb(l + 1) + 4 * dm));
                     ids.push_back(B.add_task(p.first, t, acc));
                 }
@@ -336,7 +350,7 @@ mk_status lower(const mk_model_desc* d, const Config& c, Lowering* lw) {
             int64_t u0 = p.second.first, u1 = p.second.second;
             DevTask t = gemv_task(OP_GU, l, 2 * u0, 2 * (u1 - u0), dm, bl.row_gu, lb + bl.l_gu, 2, ctr(l, 3));
             std::vector<mk_ir_access> acc;
-            acc.push_back(A(B_X, MK_ACC_READ, 0, 4 * dm));
+            acc.push_back(A(B_X, MK_ACC_READ, xm, xm + 4 * dm));
             acc.push_back(A(B_H, MK_ACC_WRITE, 4 * u0, 4 * u1));
             ids.push_back(B.add_task(p.first, t, acc));
         }
@@ -351,6 +365,7 @@ mk_status lower(const mk_model_desc* d, const Config& c, Lowering* lw) {
             DevTask t = gemv_task(OP_DOWN, l, r0, r1 - r0, F, bl.row_down, lb + bl.l_down, 1, ctr(l, 4));
             std::vector<mk_ir_access> acc;
             acc.push_back(A(B_H, MK_ACC_READ, 0, 4 * F));
+            acc.push_back(A(B_X, MK_ACC_READ, xm + 4 * r0, xm + 4 * r1));  // residual: x_mid
             acc.push_back(A(B_X, MK_ACC_WRITE, 4 * r0, 4 * r1));
             ids.push_back(B.add_task(p.first, t, acc));
         }
@@ -412,7 +427,22 @@ mk_status device_tables(const Lowering& lw, int n_sms, std::vector<TaskRec>* rec
     }
     (*queue_off)[n_sms] = (int32_t)queue->size();
     for (int id : *queue) {
-        const DevTask& t = lw.dev[id];
+        DevTask t = lw.dev[id];
+        // counters carried by tagged values exist only in the IR
+        auto tagged = [&](int ctr) { return ctr >= 0 && ctr < (int)lw.ctr_buf.size() && lw.ctr_buf[ctr] >= 0; };
+        if (tagged(t.signal_ctr)) t.signal_ctr = -1;
+        for (int w = 0; w < t.n_waits;) {
+            if (tagged(t.wait_ctr[w])) {
+                for (int v = w; v + 1 < t.n_waits; ++v) {
+                    t.wait_ctr[v] = t.wait_ctr[v + 1];
+                    t.wait_cnt[v] = t.wait_cnt[v + 1];
+                    t.wait_off[v] = t.wait_off[v + 1];
+                }
+                --t.n_waits;
+            } else {
+                ++w;
+            }
+        }
         TaskRec r{};
         bool fits = t.op >= 0 && t.op < 256 && t.layer >= 0 && t.layer < 65536 && t.n_waits >= 0 && t.n_waits <= 2 &&
                     t.w_off >= 0 && (t.w_off & 15) == 0 && (t.w_off >> 4) <= 0xFFFFFFFFll && t.row_bytes >= 0 &&
@@ -468,6 +498,8 @@ mk_ir* to_ir(const Lowering& lw, int n_sms) {
     ir->buf_flags = new int32_t[B_COUNT]();
     ir->buf_flags[B_LOGITS] = MK_BUF_OUTPUT;
     ir->buf_flags[B_OUT] = MK_BUF_OUTPUT;
+    ir->ctr_buf = new int32_t[std::max(1, lw.n_counters)];
+    for (int k = 0; k < lw.n_counters; ++k) ir->ctr_buf[k] = k < (int)lw.ctr_buf.size() ? lw.ctr_buf[k] : -1;
     return ir;
 }
 
@@ -511,6 +543,15 @@ mk_status validate_ir(const mk_ir* ir, std::string* why) {
     }
     for (int t = 0; t < T; ++t)
         if (qcount[t] != 1) return fail("task " + std::to_string(t) + " queued " + std::to_string(qcount[t]) + " times");
+    // tagged counters (ctr_buf may be NULL: none)
+    std::vector<int> tbuf(NC, -1), tset(NB, -1);  // counter -> buffer; buffer -> clock set
+    int n_sets = 1;                                // set 0: happens-before without tagged waits
+    for (int c = 0; c < NC && ir->ctr_buf; ++c) {
+        const int b = ir->ctr_buf[c];
+        if (b < -1 || b >= NB) return fail("counter " + std::to_string(c) + " names missing buffer " + std::to_string(b));
+        tbuf[c] = b;
+        if (b >= 0 && tset[b] < 0) tset[b] = n_sets++;
+    }
     std::vector<int> nprod(NC, 0);
     for (int t = 0; t < T; ++t) {
         const mk_ir_task& k = ir->tasks[t];
@@ -560,9 +601,12 @@ mk_status validate_ir(const mk_ir* ir, std::string* why) {
         if (ir->tasks[t].signal_ctr >= 0) prodlist[ir->tasks[t].signal_ctr].push_back(t);
     std::vector<int> indeg(N, 0);
     std::vector<std::vector<int>> out(N);
-    auto edge = [&](int a, int b) {
+    // in-edges with the clock sets they count in: -1 all, -2 none, k >= 1 set k only
+    std::vector<std::vector<std::pair<int, int>>> in(N);
+    auto edge = [&](int a, int b, int set = -1) {
         out[a].push_back(b);
         indeg[b]++;
+        in[b].push_back({a, set});
     };
     for (int s = 0; s < S; ++s) {
         int prevn = -1;
@@ -579,7 +623,7 @@ mk_status validate_ir(const mk_ir* ir, std::string* why) {
             if (k.signal_ctr >= 0) edge(tn(t, e), cn(k.signal_ctr, e));
             for (int w = 0; w < k.n_waits; ++w) {
                 int ee = e + k.wait_epoch_off[w];
-                if (ee >= 0) edge(cn(k.wait_ctr[w], ee), tn(t, e));
+                if (ee >= 0) edge(cn(k.wait_ctr[w], ee), tn(t, e), tbuf[k.wait_ctr[w]] >= 0 ? -2 : -1);
             }
         }
     // Kahn order; a leftover node means a cycle: some wait can never be met.
@@ -607,25 +651,84 @@ mk_status validate_ir(const mk_ir* ir, std::string* why) {
             return fail("deadlock: cycle among counters");
         }
     }
-    // Vector clocks: vc[n][s] = last queue index on SM s that happens before n.
-    std::vector<int32_t> vc((size_t)N * S, -1);
-    std::vector<std::vector<int>> in(N);
-    for (int n = 0; n < N; ++n)
-        for (int m : out[n]) in[m].push_back(n);
-    auto seq = [&](int t, int e) { return e * qlen[ir->tasks[t].sm] + seqpos[t]; };
-    for (int n : order) {
-        int32_t* v = &vc[(size_t)n * S];
-        for (int p : in[n]) {
-            const int32_t* pv = &vc[(size_t)p * S];
-            for (int s = 0; s < S; ++s) v[s] = std::max(v[s], pv[s]);
-        }
-        if (n < NT_) {
-            int t = n % T, e = n / T;
-            v[ir->tasks[t].sm] = std::max(v[ir->tasks[t].sm], seq(t, e));
+    // A wait on a tagged counter orders the waiting task only after the
+    // producers' writes of the tagged buffer that it reads: every byte of the
+    // buffer it reads must be written by those producers in the waited step,
+    // and it gets a happens-before edge from exactly the producers whose
+    // writes overlap its reads (counted only for accesses to that buffer).
+    auto range_at = [](const mk_ir_access& x, int e) {
+        return std::make_pair(x.lo + e * x.stride, x.hi + e * x.stride + e * x.grow);
+    };
+    for (int t = 0; t < T; ++t) {
+        const mk_ir_task& k = ir->tasks[t];
+        for (int w = 0; w < k.n_waits; ++w) {
+            const int c = k.wait_ctr[w], b = tbuf[c], off = k.wait_epoch_off[w];
+            if (b < 0) continue;
+            if (off != 0)  // the poll looks for the running step's tag
+                return fail("tagged wait: task " + std::to_string(t) + " waits on counter " + std::to_string(c) +
+                            " of an earlier step; tagged values carry only the running step");
+            for (int e = 0; e < EPOCHS; ++e) {
+                const int ee = e + off;
+                if (ee < 0) continue;
+                std::vector<std::pair<int64_t, int64_t>> wr;  // producers' writes of b at step ee
+                for (int p : prodlist[c]) {
+                    const mk_ir_task& pk = ir->tasks[p];
+                    bool linked = false;
+                    for (int a = pk.acc_begin; a < pk.acc_begin + pk.n_acc; ++a) {
+                        const mk_ir_access& y = ir->acc[a];
+                        if (y.buf != b || y.kind == MK_ACC_READ) continue;
+                        const auto ry = range_at(y, ee);
+                        if (ry.second <= ry.first) continue;
+                        wr.push_back(ry);
+                        for (int a2 = k.acc_begin; a2 < k.acc_begin + k.n_acc && !linked; ++a2) {
+                            const mk_ir_access& x = ir->acc[a2];
+                            const auto rx = range_at(x, e);
+                            if (x.buf == b && rx.first < ry.second && ry.first < rx.second) linked = true;
+                        }
+                    }
+                    if (linked) in[tn(t, e)].push_back({tn(p, ee), tset[b]});
+                }
+                std::sort(wr.begin(), wr.end());
+                for (int a = k.acc_begin; a < k.acc_begin + k.n_acc; ++a) {
+                    const mk_ir_access& x = ir->acc[a];
+                    if (x.buf != b) continue;
+                    const auto rx = range_at(x, e);
+                    int64_t at = rx.first;  // first byte not yet covered
+                    for (const auto& y : wr)
+                        if (y.first <= at) at = std::max(at, y.second);
+                    if (at < rx.second)
+                        return fail("tagged wait: task " + std::to_string(t) + " reads bytes [" + std::to_string(at) +
+                                    ", " + std::to_string(rx.second) + ") of buffer " + std::to_string(b) +
+                                    " that no producer of counter " + std::to_string(c) + " writes in that step");
+                }
+            }
         }
     }
-    auto hb = [&](int ta, int ea, int tb, int eb) {  // (ta,ea) happens before (tb,eb)
-        return vc[(size_t)tn(tb, eb) * S + ir->tasks[ta].sm] >= seq(ta, ea);
+    // Vector clocks: vcs[k][n][s] = last queue index on SM s that happens
+    // before n in clock set k.  Set 0 leaves out tagged waits; set tset[b]
+    // adds the producer edges of the tagged waits on buffer b.  Those edges
+    // run parallel to producer -> counter -> waiter paths of the graph, so
+    // Kahn's order is still a topological order.
+    auto seq = [&](int t, int e) { return e * qlen[ir->tasks[t].sm] + seqpos[t]; };
+    std::vector<std::vector<int32_t>> vcs(n_sets, std::vector<int32_t>((size_t)N * S, -1));
+    for (int set = 0; set < n_sets; ++set) {
+        std::vector<int32_t>& vc = vcs[set];
+        for (int n : order) {
+            int32_t* v = &vc[(size_t)n * S];
+            for (const auto& pe : in[n]) {
+                if (pe.second == -2 || (pe.second >= 0 && pe.second != set)) continue;
+                const int32_t* pv = &vc[(size_t)pe.first * S];
+                for (int s = 0; s < S; ++s) v[s] = std::max(v[s], pv[s]);
+            }
+            if (n < NT_) {
+                int t = n % T, e = n / T;
+                v[ir->tasks[t].sm] = std::max(v[ir->tasks[t].sm], seq(t, e));
+            }
+        }
+    }
+    const std::vector<int32_t>& vc0 = vcs[0];
+    auto hb = [&](int ta, int ea, int tb, int eb) {  // (ta,ea) happens before (tb,eb) without tagged waits
+        return vc0[(size_t)tn(tb, eb) * S + ir->tasks[ta].sm] >= seq(ta, ea);
     };
 
     // ---- counter reuse across steps: a wait at step e must not be satisfiable
@@ -635,6 +738,7 @@ mk_status validate_ir(const mk_ir* ir, std::string* why) {
         const mk_ir_task& k = ir->tasks[t];
         for (int w = 0; w < k.n_waits; ++w) {
             int c = k.wait_ctr[w], off = k.wait_epoch_off[w];
+            if (tbuf[c] >= 0) continue;  // no counter word: reusing a tag is a race on the buffer, checked below
             for (int p : prodlist[c])
                 if (!hb(t, 1, p, 2 + off))
                     return fail("race: counter " + std::to_string(c) + " is reused by step e+1 of producer task " +
@@ -664,7 +768,8 @@ mk_status validate_ir(const mk_ir* ir, std::string* why) {
     for (int b = 0; b < NB; ++b)
         for (int s = 0; s < S; ++s)
             std::stable_sort(on[b][s].begin(), on[b][s].end(), [](const Inst& x, const Inst& y) { return x.seq < y.seq; });
-    for (int b = 0; b < NB; ++b)
+    for (int b = 0; b < NB; ++b) {
+        const std::vector<int32_t>& vc = vcs[tset[b] > 0 ? tset[b] : 0];
         for (int sx = 0; sx < S; ++sx)
             for (const Inst& x : on[b][sx]) {
                 if (x.kind == MK_ACC_READ) continue;  // every conflicting pair has a write or atomic side
@@ -686,6 +791,7 @@ mk_status validate_ir(const mk_ir* ir, std::string* why) {
                     }
                 }
             }
+    }
 
     // ---- correctness: every task's writes reach an output (two steps).
     //      Fixpoint over "useful" instances; each round merges the byte ranges
@@ -761,8 +867,8 @@ WsLayout ws_layout(const mk_model_desc* d, const Config& c, int64_t n_tasks, int
     w.recs = take(n_tasks * (int64_t)sizeof(TaskRec));
     w.queue_off = take((int64_t)(c.sms + 1) * 4);
     w.inv_freq = take((int64_t)d->head_dim / 2 * 4);
-    w.x = take((int64_t)d->d_model * 2 * 4);
-    w.qkv = take((qd + 2 * kd) * 4);
+    w.x = take((int64_t)d->d_model * 3 * 4);  // x[2][d], x_mid[d]
+    w.qkv = take((qd + 2 * kd) * 8);  // tagged values
     w.part_ml = take((int64_t)d->n_q_heads * c.C * 2 * 4);
     w.att = take((int64_t)d->n_q_heads * d->head_dim * 4);
     w.part_acc = take((int64_t)d->n_q_heads * c.C * d->head_dim * 4);
@@ -802,6 +908,7 @@ void mk_free_ir(mk_ir* ir) {
     delete[] ir->queue;
     delete[] ir->queue_off;
     delete[] ir->buf_flags;
+    delete[] ir->ctr_buf;
     delete ir;
 }
 

@@ -210,6 +210,57 @@ static __device__ __forceinline__ bool wait_counters(Ctx& c, const TaskRec& t, i
     return c.sh->flag != 0;
 }
 
+// Tagged values carry their own completion.  The QKV rows are stored as one
+// 64-bit word each: the fp32 result in the low half and a tag naming the
+// (step, layer) that wrote it in the high half, with gpu-scope relaxed
+// accesses, which are single-copy atomic for aligned 64-bit words.  A reader
+// that sees the tag it expects therefore sees that step's value, with no
+// counter, barrier or fence on the producer's side; it orders nothing else,
+// so only data whose readers poll the tags travels this way.  Tags start at
+// 1 after every reset of the synchronisation state (which zeroes the words).
+__device__ __forceinline__ uint32_t qkv_tag(const VmParams& p, int step, int layer) {
+    return 1u + (uint32_t)(p.epoch0 + step) * (uint32_t)p.L + (uint32_t)layer;
+}
+__device__ __forceinline__ void st_tagged(unsigned long long* a, float v, uint32_t tag) {
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(a),
+                 "l"(((unsigned long long)tag << 32) | (unsigned long long)__float_as_uint(v))
+                 : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_tagged(const unsigned long long* a) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(a) : "memory");
+    return v;
+}
+// Re-read the word at a until it carries `tag` (v holds a first read).
+// False after an abort or when the watchdog expires (the error is raised).
+__device__ __forceinline__ bool poll_tagged(const VmParams& p, const unsigned long long* a, uint32_t tag,
+                                            unsigned long long& v, int task_id, int step) {
+    if ((uint32_t)(v >> 32) == tag) return true;
+    const uint64_t t0 = gtimer();
+    for (uint32_t it = 1;; ++it) {
+        v = ld_tagged(a);
+        if ((uint32_t)(v >> 32) == tag) return true;
+        if ((it & 63u) == 0u) {
+            if (aborted(p)) return false;
+            if (gtimer() - t0 > (uint64_t)p.watchdog_ns) {
+                raise_error(p, DEV_TIMEOUT, (uint32_t)task_id, (uint32_t)step);
+                return false;
+            }
+        }
+    }
+}
+// Consumer barrier that also ANDs a predicate over the consumer threads.
+__device__ __forceinline__ bool bar_consumers_and(bool ok) {
+    int r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\tsetp.ne.s32 pi, %1, 0;\n\tbar.red.and.pred po, 1, %2, pi;\n\t"
+        "selp.s32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"((int)ok), "n"(NT)
+        : "memory");
+    return r != 0;
+}
+
 // The consumer barrier orders every consumer thread's writes of the task
 // before the release-add by lane 0 of warp sw; a gpu-scope release is
 // cumulative over writes that happen before it, so the waiting CTA's acquire
@@ -676,6 +727,10 @@ __device__ __forceinline__ void ring_acquire(Ctx& c, bool defer) {
 __device__ __forceinline__ float* xbuf(const VmParams& p, int layer) {
     return p.x + (p.fused ? (size_t)(layer & 1) * p.d : 0);
 }
+// x_mid = x + attention output of the running layer, written by O and read by
+// the FFN side.  It has a buffer of its own so that O never overwrites the
+// layer input that QKV tasks elsewhere may still be reading.
+__device__ __forceinline__ float* xmid(const VmParams& p) { return p.x + 2 * (size_t)p.d; }
 // SwiGLU outputs of the running OP_FFN task (the merge scratch is idle then).
 static_assert(sizeof(MergeScratch) >= FFN_MAX_UNITS * sizeof(float), "OP_FFN SwiGLU outputs");
 __device__ __forceinline__ float* ffn_h(Ctx& c) { return reinterpret_cast<float*>(&c.sh->mg); }
@@ -790,7 +845,7 @@ __device__ bool gemv_run(Ctx& c, const TaskRec& t, int task_id, int step, float&
         }
         case OP_GU:
         case OP_FFN:
-            prologue_rmsnorm<BASE>(c, xbuf(p, layer), nullptr,
+            prologue_rmsnorm<BASE>(c, xmid(p), nullptr,
                                    (const uint16_t*)(p.w + p.layer_bytes * layer + p.l_ffn_norm), p.d, p.eps, LQ4);
             break;
         case OP_LM:
@@ -845,7 +900,9 @@ __device__ bool gemv_run(Ctx& c, const TaskRec& t, int task_id, int step, float&
         const bool has_row = rb + my_r < nrows;
         float resid = 0.f;  // residual input of this lane's row
         if (writer && has_row && !defer) {
-            if (op == OP_DOWN || (op == OP_O && layer > 0)) {
+            if (op == OP_DOWN) {
+                resid = __ldcg(xmid(p) + row_g);
+            } else if (op == OP_O && layer > 0) {
                 resid = __ldcg(xbuf(p, layer) + row_g);
             } else if (op == OP_O) {
                 const uint16_t* e = (const uint16_t*)(p.w + p.embed) + (size_t)tok * p.d;
@@ -916,11 +973,12 @@ __device__ bool gemv_run(Ctx& c, const TaskRec& t, int task_id, int step, float&
                     best_i = row_g;
                 }
             } else if (op == OP_QKV) {
-                p.qkv[row_g] = tot;
-            } else {  // O and down: residual add
-                float* xo = xbuf(p, layer);
-                xo[row_g] = resid + tot;
-                if (op == OP_O && p.fused) xbuf(p, layer + 1)[row_g] = resid + tot;  // the FFN adds into this copy
+                st_tagged(p.qkv + row_g, tot, qkv_tag(p, step, layer));
+            } else if (op == OP_O) {  // residual add: x_mid, and with the fused FFN the copy it adds into
+                xmid(p)[row_g] = resid + tot;
+                if (p.fused) xbuf(p, layer + 1)[row_g] = resid + tot;
+            } else {  // down: residual add
+                xbuf(p, layer)[row_g] = resid + tot;
             }
         }
     }
@@ -944,13 +1002,18 @@ __device__ bool gemv_run(Ctx& c, const TaskRec& t, int task_id, int step, float&
                     best_i = row_g;
                 }
             } else if (op == OP_QKV) {
-                p.qkv[row_g] = tot;
+                st_tagged(p.qkv + row_g, tot, qkv_tag(p, step, layer));
             } else {  // O and down: residual add
                 float resid;
-                if (op == OP_DOWN || layer > 0) resid = __ldcg(xbuf(p, layer) + row_g);
+                if (op == OP_DOWN) resid = __ldcg(xmid(p) + row_g);
+                else if (layer > 0) resid = __ldcg(xbuf(p, layer) + row_g);
                 else resid = base_to_f32<BASE>(__ldg((const uint16_t*)(p.w + p.embed) + (size_t)tok * p.d + row_g));
-                xbuf(p, layer)[row_g] = resid + tot;
-                if (op == OP_O && p.fused) xbuf(p, layer + 1)[row_g] = resid + tot;
+                if (op == OP_O) {
+                    xmid(p)[row_g] = resid + tot;
+                    if (p.fused) xbuf(p, layer + 1)[row_g] = resid + tot;
+                } else {
+                    xbuf(p, layer)[row_g] = resid + tot;
+                }
             }
         }
     }
@@ -1065,19 +1128,27 @@ static __device__ __forceinline__ bool attn_task(Ctx& c, const TaskRec& t, int t
             }
         }
     };
-    // The chunk's first cache rows are requested before the counter wait: rows
-    // of earlier positions were written by earlier steps, whose writers the
-    // wait of this CTA's previous task already ordered before us.
+    // The chunk's first cache rows are requested before this step's q/k/v
+    // arrive: rows of earlier positions were written by earlier steps, whose
+    // writers the wait of this CTA's previous task already ordered before us.
     if (j1 > j0) {
         load_k(j0, min(ATTN_TILE, j1 - j0));
         load_v(j0, min(ATTN_TILE, j1 - j0));
     }
-    if (!wait_counters(c, t, task_id, step)) return false;
+    if (!wait_counters(c, t, task_id, step)) return false;  // counter waits, if any, and aborts
 
-    for (int i = c.tid; i < (rep + 1) * half; i += NT) {
+    // The group's query, key and value rows are read as tagged values: each
+    // thread polls its words until they carry this step's tag.
+    const uint32_t tag = qkv_tag(p, step, l);
+    bool ok = true;
+    const unsigned long long* vsrc = p.qkv + p.q_dim + p.kv_dim + (size_t)g * HD + c.tid;  // HD <= NT
+    unsigned long long wv = c.tid < HD ? ld_tagged(vsrc) : 0ull;
+    for (int i = c.tid; i < (rep + 1) * half && ok; i += NT) {
         const int hh = i / half, dd = i % half;
-        const float* src = hh < rep ? p.qkv + (size_t)(g * rep + hh) * HD : p.qkv + p.q_dim + (size_t)g * HD;
-        const float x1 = __ldcg(src + dd), x2 = __ldcg(src + dd + half);
+        const unsigned long long* src = hh < rep ? p.qkv + (size_t)(g * rep + hh) * HD : p.qkv + p.q_dim + (size_t)g * HD;
+        unsigned long long w1 = ld_tagged(src + dd), w2 = ld_tagged(src + dd + half);
+        ok = poll_tagged(p, src + dd, tag, w1, task_id, step) && poll_tagged(p, src + dd + half, tag, w2, task_id, step);
+        const float x1 = __uint_as_float((uint32_t)w1), x2 = __uint_as_float((uint32_t)w2);
         const float ang = __fmul_rn((float)pos, __ldg(p.inv_freq + dd));
         float sn, cs;
         sincosf(ang, &sn, &cs);
@@ -1090,13 +1161,15 @@ static __device__ __forceinline__ bool attn_task(Ctx& c, const TaskRec& t, int t
             at.kcur[dd + half] = round_bf16(o2);
         }
     }
-    for (int i = c.tid; i < HD; i += NT)
-        at.vcur[i] = round_bf16(__ldcg(p.qkv + p.q_dim + p.kv_dim + (size_t)g * HD + i));
+    if (c.tid < HD && ok) {
+        ok = poll_tagged(p, vsrc, tag, wv, task_id, step);
+        at.vcur[c.tid] = round_bf16(__uint_as_float((uint32_t)wv));
+    }
     if (c.tid < rep) {
         sh.m[c.tid] = -1.0e30f;
         sh.l[c.tid] = 0.f;
     }
-    bar_consumers();
+    if (!bar_consumers_and(ok)) return false;
     if (ch == C - 1) {
         for (int i = c.tid; i < HD; i += NT) {
             kbase[(size_t)pos * HD + i] = __bfloat16_as_ushort(__float2bfloat16_rn(at.kcur[i]));
@@ -1237,7 +1310,12 @@ __device__ __forceinline__ void consumer(Ctx& c) {
                 atomicMax(p.key, key);
             }
             signal_counter(c, t, sw);
-            for (; c.deferred > 0; --c.deferred) stream_issue<WT>(c);  // the copies the task skipped
+            // The copies the task skipped go out now, unless an attention or
+            // merge task follows: it does not use the ring, and its own loads
+            // are on the layer's critical path, so the copies wait for its end.
+            const int nop = c.tab[qi + 1 < c.nrec ? qi + 1 : 0].op;
+            if (!(nop == OP_ATTN || nop == OP_MERGE))
+                for (; c.deferred > 0; --c.deferred) stream_issue<WT>(c);
             if (p.trace && c.tid == 0) {
                 const int k = s * c.nrec + qi;
                 if (k < p.trace_cap) {

@@ -154,7 +154,14 @@ mk_status mk_workspace_size(const mk_model_desc* desc, const mk_schedule_config*
  * once per decode step e (epoch): it waits until every (counter, count,
  * epoch_off) satisfies counter >= count * (e + 1 + epoch_off), runs, then adds
  * 1 to signal_ctr (-1: none).  Accesses describe the bytes the instruction
- * touches at epoch e: [lo + e*stride, hi + e*stride + e*grow) of buffer buf. */
+ * touches at epoch e: [lo + e*stride, hi + e*stride + e*grow) of buffer buf.
+ *
+ * A counter c with ctr_buf[c] = b >= 0 is carried by tagged values instead of
+ * a memory word (this library's own device protocol; the pages describe only
+ * counters): each value its producers write to b holds the step's tag, and a
+ * waiting task polls the values of b it reads until they carry that tag.
+ * Such a wait therefore orders the waiting task after the producers' writes
+ * of b that it reads, and after nothing else. */
 #define MK_IR_MAX_WAITS 2
 enum { MK_ACC_READ = 1, MK_ACC_WRITE = 2, MK_ACC_ATOMIC = 3 };
 enum { MK_BUF_OUTPUT = 1 };
@@ -181,6 +188,8 @@ typedef struct {
     int32_t* queue;      /* task ids, SM after SM                                  */
     int32_t* queue_off;  /* [n_sms + 1]: SM s runs queue[queue_off[s] .. queue_off[s+1]) */
     int32_t* buf_flags;  /* [n_buffers]: MK_BUF_OUTPUT marks the step's results      */
+    int32_t* ctr_buf;    /* [n_counters]: -1, or the buffer whose tagged values carry
+                          * the counter (below)                                     */
 } mk_ir;
 
 /* Lower desc/cfg for n_sms CTAs (host only).  *out is library-owned: free it
@@ -198,7 +207,11 @@ void mk_free_ir(mk_ir* ir);
  *   race-free    — every multi-producer counter joined (count == #producers),
  *                   counter reuse across steps ordered, and every pair of
  *                   conflicting accesses ordered by happens-before over three
- *                   unrolled steps;
+ *                   unrolled steps (a wait on a tagged counter counts only
+ *                   for accesses to its buffer, and only from the producers
+ *                   whose writes overlap the waiter's reads);
+ *   tag-complete — every byte of a tagged buffer that a waiter reads is
+ *                   written by the counter's producers in the waited step;
  *   correct      — every task's writes reach an output buffer.
  * Returns MK_OK or MK_ERR_SCHEDULE_INVALID with the first reason in `why`
  * (may be NULL).  Host only; no device is touched. */

@@ -27,8 +27,17 @@ Wait semantics at epoch e: (counter c, count t, epoch offset o) passes once
 c >= t * (e + 1 + o); a threshold <= 0 passes at once.  Access ranges at epoch
 e are [lo + e*stride, hi + e*stride + e*grow).
 
+Tagged counters ("tagged": {counter: buffer}) have no memory word: the
+producers' writes of the buffer carry the step's tag and the waiting task
+polls the bytes of that buffer it reads.  Such a wait passes once every
+producer instance (step e + o) whose writes of the buffer overlap the task's
+reads of it has finished, and never if some byte it reads is written by no
+producer in that step (the poll would spin forever).  This model keeps
+memory sequentially consistent, so it cannot see that such a wait orders
+nothing but the tagged buffer; the library's validator checks that part.
+
 IR (plain dicts, the same fields the library exports):
-  {"n_sms", "n_counters", "n_buffers", "outputs": [buf ids],
+  {"n_sms", "n_counters", "n_buffers", "outputs": [buf ids], "tagged" (optional),
    "tasks": [{"sm", "waits": [(c, t, o)], "signal": c or -1,
               "acc": [(buf, kind, lo, hi, stride, grow)]}],
    "queues": [[task ids of SM 0 in order], ...]}
@@ -55,6 +64,9 @@ def malformed(ir):
     for t, k in enumerate(seen):
         if k != 1:
             return f"task {t} queued {k} times"
+    for c, b in ir.get("tagged", {}).items():
+        if not (0 <= c < n_c) or not (0 <= b < n_b):
+            return f"tagged counter {c} -> buffer {b}"
     for i, t in enumerate(ir["tasks"]):
         for (c, cnt, o) in t["waits"]:
             if not (0 <= c < n_c):
@@ -74,11 +86,46 @@ def _instances(ir, epochs):
     return seqs
 
 
-def _ready(ir, ctr, t, e):
+def _tag_sources(ir, t, e, c, o, cache):
+    """Producer instances a tagged wait of task t at epoch e depends on, or
+    None when some byte it reads of the tagged buffer has no producer."""
+    key = (t, e, c, o)
+    if key not in cache:
+        b, ee = ir["tagged"][c], e + o
+        reads = [_ranges(x, e)[2:] for x in ir["tasks"][t]["acc"] if x[0] == b]
+        writes, srcs = [], []
+        for p, task in enumerate(ir["tasks"]):
+            if task["signal"] != c or ee < 0:
+                continue
+            w = [_ranges(y, ee)[2:] for y in task["acc"] if y[0] == b and y[1] != READ]
+            w = [r for r in w if r[1] > r[0]]
+            writes += w
+            if any(lo < hy and ly < hi for (lo, hi) in reads for (ly, hy) in w):
+                srcs.append((p, ee))
+        covered = all(all(any(ly <= k < hy for (ly, hy) in writes) for k in range(lo, hi)) for (lo, hi) in reads)
+        cache[key] = srcs if covered else None
+    return cache[key]
+
+
+def _ready(ir, ctr, t, e, done=None, cache=None):
+    tagged = ir.get("tagged", {})
     for (c, cnt, o) in ir["tasks"][t]["waits"]:
-        if ctr[c] < cnt * (e + 1 + o):
+        if c in tagged:
+            srcs = _tag_sources(ir, t, e, c, o, cache)
+            if srcs is None or not all(done(p, ee) for (p, ee) in srcs):
+                return False
+        elif ctr[c] < cnt * (e + 1 + o):
             return False
     return True
+
+
+def _index(ir):
+    """Task -> (SM, position in its queue, queue length)."""
+    where = {}
+    for s, q in enumerate(ir["queues"]):
+        for i, t in enumerate(q):
+            where[t] = (s, i, len(q))
+    return where
 
 
 def deadlocks(ir, epochs=3):
@@ -86,13 +133,19 @@ def deadlocks(ir, epochs=3):
     seqs = _instances(ir, epochs)
     pos = [0] * len(seqs)
     ctr = [0] * ir["n_counters"]
+    where, cache = _index(ir), {}
+
+    def done(p, ee):
+        s, i, n = where[p]
+        return pos[s] > ee * n + i
+
     progress = True
     while progress:
         progress = False
         for s, seq in enumerate(seqs):
             while pos[s] < len(seq):
                 t, e = seq[pos[s]]
-                if not _ready(ir, ctr, t, e):
+                if not _ready(ir, ctr, t, e, done, cache):
                     break
                 sig = ir["tasks"][t]["signal"]
                 if sig >= 0:
@@ -140,6 +193,7 @@ def races(ir, epochs=2, max_states=2_000_000):
                     ctr[sig_of[t]] += 1
         return ctr
 
+    where, cache = _index(ir), {}
     start = tuple((0, 0) for _ in range(n))
     seen = {start}
     dq = deque([start])
@@ -167,7 +221,12 @@ def races(ir, epochs=2, max_states=2_000_000):
                 if ctr is None:
                     ctr = counters(st)
                 t, e = seqs[s][idx]
-                if not _ready(ir, ctr, t, e):
+
+                def done(p, ee, st=st):
+                    sp, i, m = where[p]
+                    return st[sp][0] > ee * m + i
+
+                if not _ready(ir, ctr, t, e, done, cache):
                     continue
                 nxt = list(st)
                 nxt[s] = (idx, 1)

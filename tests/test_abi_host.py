@@ -200,3 +200,47 @@ def test_tuner_agreement_rule():
     bad = ref.copy()
     bad[0, 0] = np.nan
     assert not tune.agrees(bad, ref)
+
+
+# ------------------------------------------------------------------ tagged counters
+def _tagged_case(mk):
+    """A small real schedule whose q/k/v counter is tagged, one attention task
+    waiting on it, and a QKV producer whose rows that task reads."""
+    ir = _small_ir(mk, 3, 2)
+    assert ir["tagged"], "the lowering tags the q/k/v counter"
+    c, b = next(iter(ir["tagged"].items()))
+    a = next(i for i, t in enumerate(ir["tasks"]) if any(w[0] == c for w in t["waits"]))
+    reads = [x for x in ir["tasks"][a]["acc"] if x[0] == b]
+    q = next(i for i, t in enumerate(ir["tasks"]) if t["signal"] == c and any(
+        y[0] == b and y[1] != S.READ and y[2] < x[3] and x[2] < y[3] for y in t["acc"] for x in reads))
+    return ir, c, b, a, q
+
+
+def test_tagged_wait_orders_only_its_buffer(mk):
+    ir, c, b, a, q = _tagged_case(mk)
+    assert mk.mk_validate_ir(ir)[0] == mk.MK_OK
+    # a side channel: the producer also writes bytes of another buffer that the waiter reads
+    other = 3  # the hidden-state buffer, unused by this fused schedule
+    ir["tasks"][q]["acc"].append((other, S.WRITE, 0, 8, 0, 0))
+    ir["tasks"][a]["acc"].append((other, S.READ, 0, 8, 0, 0))
+    st, why = mk.mk_validate_ir(ir)
+    assert st != mk.MK_OK and "race" in why, why
+    # through a counter word the same access is ordered
+    ir["tagged"] = {}
+    st, why = mk.mk_validate_ir(ir)
+    assert st == mk.MK_OK, why
+
+
+def test_tagged_wait_must_be_covered_and_current(mk):
+    ir, c, b, a, q = _tagged_case(mk)
+    import copy
+    m = copy.deepcopy(ir)
+    m["tasks"][q]["acc"] = [y for y in m["tasks"][q]["acc"] if y[0] != b]  # the producer stops writing its rows
+    st, why = mk.mk_validate_ir(m)
+    assert st != mk.MK_OK and "tagged wait" in why, why
+    assert not S.verdict(m)[0]
+    m = copy.deepcopy(ir)
+    m["tasks"][a]["waits"] = [(w[0], w[1], -1) if w[0] == c else w for w in m["tasks"][a]["waits"]]
+    st, why = mk.mk_validate_ir(m)
+    assert st != mk.MK_OK and "tagged wait" in why, why
+    assert not S.verdict(m)[0]

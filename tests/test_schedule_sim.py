@@ -108,3 +108,37 @@ def test_malformed_references():
     ir = producer_consumer()
     ir["queues"] = [[0, 1], []]
     assert S.verdict(ir)[1].startswith("malformed")
+
+
+# ---- tagged counters: the waiter polls the values it reads of the tagged buffer
+def tagged_pair(waiter_reads=(0, 8)):
+    # P1 writes buf0[0:8), P2 writes buf0[8:16); both "signal" tagged counter c0.
+    # W reads buf0[waiter_reads] after a tagged wait on c0 (count 2) and writes
+    # the output; P2 first waits for W through the ordinary counter c1.
+    lo, hi = waiter_reads
+    tasks = [T(0, signal=0, acc=[(0, W, 0, 8, 0, 0)]),
+             T(1, waits=[(1, 1, 0)], signal=0, acc=[(0, W, 8, 16, 0, 0), (1, W, 4, 8, 0, 0)]),
+             T(2, waits=[(0, 2, 0)], signal=1, acc=[(0, R, lo, hi, 0, 0), (1, W, 0, 4, 0, 0)])]
+    ir = IR(tasks, [[0], [1], [2]], 2)
+    ir["tagged"] = {0: 0}
+    return ir
+
+
+def test_tagged_wait_needs_only_the_overlapping_producers():
+    # As a counter wait this is a cycle W -> P2 -> W; polling buf0[0:8) needs only P1.
+    ir = tagged_pair()
+    assert not S.deadlocks(ir, 1)
+    plain = dict(ir, tagged={})
+    assert S.deadlocks(plain, 1)
+
+
+def test_tagged_wait_on_bytes_nobody_writes_deadlocks():
+    # The poll of buf0[16:24) never sees its tag.
+    ir = tagged_pair(waiter_reads=(16, 24))
+    assert S.deadlocks(ir, 1)
+
+
+def test_tagged_wait_orders_the_overlapping_producer():
+    ir = tagged_pair()
+    # W may not run before P1 has written what W reads: no (P1, W) race in one step
+    assert ((0, 0), (2, 0)) not in S.races(ir, epochs=1)
