@@ -29,6 +29,11 @@ constexpr int MAXG = 8;                 // 8-element k groups per lane
 constexpr int MAX_K = 8 * NT * MAXG;    // 16384: eight warps x 32 lanes x MAXG groups
 constexpr int MAX_REP = 8;              // query heads per KV head
 constexpr int ATTN_TILE = 32;           // positions per online-softmax tile
+// Copies of the split-KV partials (and of the merged attention output) that
+// their producers write: every O task reads all of them, and CTAs that read
+// the same lines at the same moment queue at the L2 slices holding them, so
+// CTA b reads copy b % PART_COPIES.
+constexpr int PART_COPIES = 4;
 constexpr int CTR_STRIDE = 32;          // u32 words between counters (128 B lines)
 constexpr int MAX_HC = 1024;            // query heads x split-KV chunks (merge scratch)
 constexpr int FFN_BLOCK = 8;            // hidden units per 16-byte column block of a fused down projection
@@ -111,10 +116,10 @@ struct VmParams {
     const float* inv_freq;     // [hd/2]
     float* x;                  // residual stream [2][d], then x_mid [d]
     unsigned long long* qkv;   // [q_dim + 2 kv_dim] tagged values: fp32 bits | tag << 32
-    float* part_ml;            // [Hq][C][2]  (running max, sum)
-    float* att;                // [q_dim] merged attention output (merge tasks; else unused)
+    float* part_ml;            // [PART_COPIES][Hq][C][2]  (running max, sum)
+    float* att;                // [PART_COPIES][q_dim] merged attention output (merge tasks; else unused)
     int32_t merge_tasks;       // 1: OP_MERGE tasks merge the partials and O reads att
-    float* part_acc;           // [Hq][C][hd]
+    float* part_acc;           // [PART_COPIES][Hq][C][hd]
     float* h;                  // SwiGLU output [F]
     const int32_t* forced;     // nullable: token fed at step s
     int32_t* out_ids;          // nullable: argmax of step s

@@ -161,7 +161,7 @@ mk_status lower(const mk_model_desc* d, const Config& c, Lowering* lw) {
     lw->ctr_buf.assign(lw->n_counters, -1);
     auto ctr = [&](int l, int k) { return CS * l + k; };
     const bool mt = merge_tasks(d, c);
-    const int64_t ML_BYTES = (int64_t)Hq * C * 2 * 4;
+    const int64_t ML_BYTES = (int64_t)Hq * C * 2 * 4, PART_BYTES = ML_BYTES + (int64_t)Hq * C * hd * 4;
     // Residual buffers: x[2][d].  With the fused FFN the layer-l input lives in
     // x[l & 1]; O(l) writes x_mid into x[l & 1] and x[(l + 1) & 1], and the
     // OP_FFN tasks add their down-projection partials into x[(l + 1) & 1].
@@ -259,11 +259,13 @@ mk_status lower(const mk_model_desc* d, const Config& c, Lowering* lw) {
                     if (ch == C - 1)  // the chunk holding the newest position appends it
                         acc.push_back(A(B_KV, MK_ACC_WRITE, base + P0 * hd * 2, base + (P0 + 1) * hd * 2, hd * 2, 0));
                 }
-                for (int i = g * rep; i < (g + 1) * rep; ++i) {
-                    int64_t ml = ((int64_t)i * C + ch) * 2 * 4, ac = ML_BYTES + ((int64_t)i * C + ch) * hd * 4;
-                    acc.push_back(A(B_PART, MK_ACC_WRITE, ml, ml + 8));
-                    acc.push_back(A(B_PART, MK_ACC_WRITE, ac, ac + hd * 4));
-                }
+                for (int k = 0; k < PART_COPIES; ++k)  // every copy of the partials
+                    for (int i = g * rep; i < (g + 1) * rep; ++i) {
+                        int64_t ml = k * PART_BYTES + ((int64_t)i * C + ch) * 2 * 4,
+                                ac = k * PART_BYTES + ML_BYTES + ((int64_t)i * C + ch) * hd * 4;
+                        acc.push_back(A(B_PART, MK_ACC_WRITE, ml, ml + 8));
+                        acc.push_back(A(B_PART, MK_ACC_WRITE, ac, ac + hd * 4));
+                    }
                 ids.push_back(B.add_task(sm, t, acc));
                 tag_ok = tag_ok && has_qkv[sm];
             }
@@ -283,9 +285,11 @@ mk_status lower(const mk_model_desc* d, const Config& c, Lowering* lw) {
                 t.signal_ctr = ctr(l, 1);
                 std::vector<mk_ir_access> acc;
                 const int64_t h0 = (int64_t)g * rep, h1 = h0 + rep;
-                acc.push_back(A(B_PART, MK_ACC_READ, h0 * C * 2 * 4, h1 * C * 2 * 4));
-                acc.push_back(A(B_PART, MK_ACC_READ, ML_BYTES + h0 * C * hd * 4, ML_BYTES + h1 * C * hd * 4));
-                acc.push_back(A(B_ATT, MK_ACC_WRITE, h0 * hd * 4, h1 * hd * 4));
+                const int64_t cpo = (lw->tasks[last].sm % PART_COPIES) * PART_BYTES;  // the CTA's copy
+                acc.push_back(A(B_PART, MK_ACC_READ, cpo + h0 * C * 2 * 4, cpo + h1 * C * 2 * 4));
+                acc.push_back(A(B_PART, MK_ACC_READ, cpo + ML_BYTES + h0 * C * hd * 4, cpo + ML_BYTES + h1 * C * hd * 4));
+                for (int k = 0; k < PART_COPIES; ++k)
+                    acc.push_back(A(B_ATT, MK_ACC_WRITE, k * 4 * qd + h0 * hd * 4, k * 4 * qd + h1 * hd * 4));
                 const int id = B.add_task(lw->tasks[last].sm, t, acc);
                 tag_ok = tag_ok && has_qkv[lw->tasks[last].sm];
                 B.set_wait({id}, ctr(l, 5 + g), C, 0);
@@ -302,8 +306,9 @@ mk_status lower(const mk_model_desc* d, const Config& c, Lowering* lw) {
             int64_t r0 = p.second.first, r1 = p.second.second;
             DevTask t = gemv_task(OP_O, l, r0, r1 - r0, qd, bl.row_o, lb + bl.l_o, 1, ctr(l, 2));
             std::vector<mk_ir_access> acc;
-            if (mt) acc.push_back(A(B_ATT, MK_ACC_READ, 0, 4 * qd));
-            else acc.push_back(A(B_PART, MK_ACC_READ, 0, ML_BYTES + (int64_t)Hq * C * hd * 4));
+            const int cp = p.first % PART_COPIES;  // the CTA's copy
+            if (mt) acc.push_back(A(B_ATT, MK_ACC_READ, cp * 4 * qd, (cp + 1) * 4 * qd));
+            else acc.push_back(A(B_PART, MK_ACC_READ, cp * PART_BYTES, (cp + 1) * PART_BYTES));
             if (l == 0) acc.push_back(A(B_KEY, MK_ACC_READ, 0, 8));
             else acc.push_back(A(B_X, MK_ACC_READ, xb(l) + 4 * r0, xb(l) + 4 * r1));  // residual
             acc.push_back(A(B_X, MK_ACC_WRITE, xm + 4 * r0, xm + 4 * r1));
@@ -869,9 +874,9 @@ WsLayout ws_layout(const mk_model_desc* d, const Config& c, int64_t n_tasks, int
     w.inv_freq = take((int64_t)d->head_dim / 2 * 4);
     w.x = take((int64_t)d->d_model * 3 * 4);  // x[2][d], x_mid[d]
     w.qkv = take((qd + 2 * kd) * 8);  // tagged values
-    w.part_ml = take((int64_t)d->n_q_heads * c.C * 2 * 4);
-    w.att = take((int64_t)d->n_q_heads * d->head_dim * 4);
-    w.part_acc = take((int64_t)d->n_q_heads * c.C * d->head_dim * 4);
+    w.part_ml = take((int64_t)PART_COPIES * d->n_q_heads * c.C * 2 * 4);
+    w.att = take((int64_t)PART_COPIES * d->n_q_heads * d->head_dim * 4);
+    w.part_acc = take((int64_t)PART_COPIES * d->n_q_heads * c.C * d->head_dim * 4);
     w.h = take((int64_t)d->d_ffn * 4);
     w.tok = take((int64_t)d->max_seq * 4 + 16);
     w.out_ids = take((int64_t)d->max_seq * 4 + 16);

@@ -382,8 +382,9 @@ static __device__ __forceinline__ void prologue_attention(Ctx& c, int lq4) {
     // the merge costs about one round trip to L2 and no block barrier.
     for (int g = c.tid; g < (p.q_dim >> 3); g += NT) {
         const int hq = (8 * g) / p.hd, d0 = (8 * g) % p.hd;
-        const float* ml = p.part_ml + (size_t)hq * C * 2;
-        const float* base = p.part_acc + (size_t)hq * C * p.hd + d0;
+        const int cp = blockIdx.x % PART_COPIES;  // this CTA's copy of the partials
+        const float* ml = p.part_ml + ((size_t)cp * p.Hq + hq) * C * 2;
+        const float* base = p.part_acc + ((size_t)cp * p.Hq + hq) * C * p.hd + d0;
         float M = -3.0e38f, den = 0.f;
         float o[8] = {0, 0, 0, 0, 0, 0, 0, 0};
         for (int c0 = 0; c0 < C; c0 += 8) {
@@ -428,8 +429,9 @@ static __device__ __forceinline__ void merge_task(Ctx& c, const TaskRec& t) {
     const int C = p.C, rep = p.Hq / p.Hkv, g = t.row0;
     for (int u = c.tid; u < rep * (p.hd >> 2); u += NT) {
         const int hq = g * rep + (4 * u) / p.hd, d0 = (4 * u) % p.hd;
-        const float* ml = p.part_ml + (size_t)hq * C * 2;
-        const float* base = p.part_acc + (size_t)hq * C * p.hd + d0;
+        const int cp = blockIdx.x % PART_COPIES;
+        const float* ml = p.part_ml + ((size_t)cp * p.Hq + hq) * C * 2;
+        const float* base = p.part_acc + ((size_t)cp * p.Hq + hq) * C * p.hd + d0;
         float M = -3.0e38f, den = 0.f;
         float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int c0 = 0; c0 < C; c0 += 8) {
@@ -455,7 +457,9 @@ static __device__ __forceinline__ void merge_task(Ctx& c, const TaskRec& t) {
             }
         }
         const float inv = 1.f / den;
-        *(float4*)(p.att + (size_t)hq * p.hd + d0) = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+        const float4 r = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+#pragma unroll
+        for (int k = 0; k < PART_COPIES; ++k) *(float4*)(p.att + (size_t)k * p.q_dim + (size_t)hq * p.hd + d0) = r;
     }
 }
 
@@ -464,7 +468,8 @@ static __device__ __forceinline__ void merge_task(Ctx& c, const TaskRec& t) {
 static __device__ __forceinline__ void prologue_att_copy(Ctx& c, int lq4) {
     const VmParams& p = *c.p;
     for (int u = c.tid; u < (p.q_dim >> 2); u += NT)
-        *(float4*)(c.xs + xs_pos(u, p.q_dim, lq4)) = __ldcg((const float4*)(p.att + 4 * u));
+        *(float4*)(c.xs + xs_pos(u, p.q_dim, lq4)) =
+            __ldcg((const float4*)(p.att + (size_t)(blockIdx.x % PART_COPIES) * p.q_dim + 4 * u));
     c.rstd = 1.f;
     bar_consumers();
 }
@@ -1240,12 +1245,17 @@ static __device__ __forceinline__ bool attn_task(Ctx& c, const TaskRec& t, int t
 #pragma unroll
     for (int e = 0; e < OPT; ++e) {
         const int oe = c.tid + NT * e, h = oe / HD, dd = oe % HD;
-        if (h < rep) p.part_acc[(((size_t)(g * rep + h)) * C + ch) * HD + dd] = acc[e];
+        if (h < rep) {
+#pragma unroll
+            for (int k = 0; k < PART_COPIES; ++k)
+                p.part_acc[(((size_t)k * p.Hq + g * rep + h) * C + ch) * HD + dd] = acc[e];
+        }
     }
     if (c.tid < rep) {
-        float* ml = p.part_ml + ((size_t)(g * rep + c.tid) * C + ch) * 2;
-        ml[0] = sh.m[c.tid];
-        ml[1] = sh.l[c.tid];
+        const float2 mlv = make_float2(sh.m[c.tid], sh.l[c.tid]);
+#pragma unroll
+        for (int k = 0; k < PART_COPIES; ++k)
+            *(float2*)(p.part_ml + (((size_t)k * p.Hq + g * rep + c.tid) * C + ch) * 2) = mlv;
     }
     return true;
 }
