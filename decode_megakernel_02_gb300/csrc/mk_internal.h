@@ -119,7 +119,7 @@ struct VmParams {
     float* part_ml;            // [PART_COPIES][Hq][C][2]  (running max, sum)
     float* att;                // [PART_COPIES][q_dim] merged attention output (merge tasks; else unused)
     int32_t merge_tasks;       // 1: OP_MERGE tasks merge the partials and O reads att
-    float* part_acc;           // [PART_COPIES][Hq][C][hd]
+    uint16_t* part_acc;        // [PART_COPIES][Hq][C][hd] fp16 bit patterns
     float* h;                  // SwiGLU output [F]
     const int32_t* forced;     // nullable: token fed at step s
     int32_t* out_ids;          // nullable: argmax of step s

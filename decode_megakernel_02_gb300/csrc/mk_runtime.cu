@@ -108,7 +108,7 @@ mk_status launch(mk_handle* h, int n_steps, const int32_t* forced, int32_t* out_
     p.x = (float*)(h->wsp + h->ws.x);
     p.qkv = (unsigned long long*)(h->wsp + h->ws.qkv);
     p.part_ml = (float*)(h->wsp + h->ws.part_ml);
-    p.part_acc = (float*)(h->wsp + h->ws.part_acc);
+    p.part_acc = (uint16_t*)(h->wsp + h->ws.part_acc);
     p.att = (float*)(h->wsp + h->ws.att);
     p.merge_tasks = merge_tasks(&h->d, h->c) ? 1 : 0;
     p.h = (float*)(h->wsp + h->ws.h);

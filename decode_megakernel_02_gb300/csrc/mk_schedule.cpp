@@ -161,7 +161,7 @@ mk_status lower(const mk_model_desc* d, const Config& c, Lowering* lw) {
     lw->ctr_buf.assign(lw->n_counters, -1);
     auto ctr = [&](int l, int k) { return CS * l + k; };
     const bool mt = merge_tasks(d, c);
-    const int64_t ML_BYTES = (int64_t)Hq * C * 2 * 4, PART_BYTES = ML_BYTES + (int64_t)Hq * C * hd * 4;
+    const int64_t ML_BYTES = (int64_t)Hq * C * 2 * 4, PART_BYTES = ML_BYTES + (int64_t)Hq * C * hd * 2;
     // Residual buffers: x[2][d].  With the fused FFN the layer-l input lives in
     // x[l & 1]; O(l) writes x_mid into x[l & 1] and x[(l + 1) & 1], and the
     // OP_FFN tasks add their down-projection partials into x[(l + 1) & 1].
@@ -262,9 +262,9 @@ mk_status lower(const mk_model_desc* d, const Config& c, Lowering* lw) {
                 for (int k = 0; k < PART_COPIES; ++k)  // every copy of the partials
                     for (int i = g * rep; i < (g + 1) * rep; ++i) {
                         int64_t ml = k * PART_BYTES + ((int64_t)i * C + ch) * 2 * 4,
-                                ac = k * PART_BYTES + ML_BYTES + ((int64_t)i * C + ch) * hd * 4;
+                                ac = k * PART_BYTES + ML_BYTES + ((int64_t)i * C + ch) * hd * 2;
                         acc.push_back(A(B_PART, MK_ACC_WRITE, ml, ml + 8));
-                        acc.push_back(A(B_PART, MK_ACC_WRITE, ac, ac + hd * 4));
+                        acc.push_back(A(B_PART, MK_ACC_WRITE, ac, ac + hd * 2));
                     }
                 ids.push_back(B.add_task(sm, t, acc));
                 tag_ok = tag_ok && has_qkv[sm];
@@ -287,7 +287,7 @@ mk_status lower(const mk_model_desc* d, const Config& c, Lowering* lw) {
                 const int64_t h0 = (int64_t)g * rep, h1 = h0 + rep;
                 const int64_t cpo = (lw->tasks[last].sm % PART_COPIES) * PART_BYTES;  // the CTA's copy
                 acc.push_back(A(B_PART, MK_ACC_READ, cpo + h0 * C * 2 * 4, cpo + h1 * C * 2 * 4));
-                acc.push_back(A(B_PART, MK_ACC_READ, cpo + ML_BYTES + h0 * C * hd * 4, cpo + ML_BYTES + h1 * C * hd * 4));
+                acc.push_back(A(B_PART, MK_ACC_READ, cpo + ML_BYTES + h0 * C * hd * 2, cpo + ML_BYTES + h1 * C * hd * 2));
                 for (int k = 0; k < PART_COPIES; ++k)
                     acc.push_back(A(B_ATT, MK_ACC_WRITE, k * 4 * qd + h0 * hd * 4, k * 4 * qd + h1 * hd * 4));
                 const int id = B.add_task(lw->tasks[last].sm, t, acc);
@@ -876,7 +876,7 @@ WsLayout ws_layout(const mk_model_desc* d, const Config& c, int64_t n_tasks, int
     w.qkv = take((qd + 2 * kd) * 8);  // tagged values
     w.part_ml = take((int64_t)PART_COPIES * d->n_q_heads * c.C * 2 * 4);
     w.att = take((int64_t)PART_COPIES * d->n_q_heads * d->head_dim * 4);
-    w.part_acc = take((int64_t)PART_COPIES * d->n_q_heads * c.C * d->head_dim * 4);
+    w.part_acc = take((int64_t)PART_COPIES * d->n_q_heads * c.C * d->head_dim * 2);  // fp16
     w.h = take((int64_t)d->d_ffn * 4);
     w.tok = take((int64_t)d->max_seq * 4 + 16);
     w.out_ids = take((int64_t)d->max_seq * 4 + 16);

@@ -384,20 +384,19 @@ static __device__ __forceinline__ void prologue_attention(Ctx& c, int lq4) {
         const int hq = (8 * g) / p.hd, d0 = (8 * g) % p.hd;
         const int cp = blockIdx.x % PART_COPIES;  // this CTA's copy of the partials
         const float* ml = p.part_ml + ((size_t)cp * p.Hq + hq) * C * 2;
-        const float* base = p.part_acc + ((size_t)cp * p.Hq + hq) * C * p.hd + d0;
+        const uint16_t* base = p.part_acc + ((size_t)cp * p.Hq + hq) * C * p.hd + d0;
         float M = -3.0e38f, den = 0.f;
         float o[8] = {0, 0, 0, 0, 0, 0, 0, 0};
         for (int c0 = 0; c0 < C; c0 += 8) {
             float mm[8], ll[8];
-            float4 a[8][2];
+            uint4 a[8];  // eight fp16 accumulators
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const int ch = min(c0 + k, C - 1);
                 const float2 v = __ldcg((const float2*)(ml + 2 * ch));  // (max, sum) in one load
                 mm[k] = v.x;
                 ll[k] = v.y;
-                a[k][0] = __ldcg((const float4*)(base + (size_t)ch * p.hd));
-                a[k][1] = __ldcg((const float4*)(base + (size_t)ch * p.hd + 4));
+                a[k] = __ldcg((const uint4*)(base + (size_t)ch * p.hd));
             }
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
@@ -406,10 +405,12 @@ static __device__ __forceinline__ void prologue_attention(Ctx& c, int lq4) {
                 const float r = expf(M - Mn), w = expf(mm[k] - Mn);
                 M = Mn;
                 den = fmaf(den, r, w * ll[k]);
-                o[0] = fmaf(o[0], r, w * a[k][0].x); o[1] = fmaf(o[1], r, w * a[k][0].y);
-                o[2] = fmaf(o[2], r, w * a[k][0].z); o[3] = fmaf(o[3], r, w * a[k][0].w);
-                o[4] = fmaf(o[4], r, w * a[k][1].x); o[5] = fmaf(o[5], r, w * a[k][1].y);
-                o[6] = fmaf(o[6], r, w * a[k][1].z); o[7] = fmaf(o[7], r, w * a[k][1].w);
+                const uint32_t h4[4] = {a[k].x, a[k].y, a[k].z, a[k].w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    o[2 * i] = fmaf(o[2 * i], r, w * half_bits_to_f32(h4[i] & 0xFFFFu));
+                    o[2 * i + 1] = fmaf(o[2 * i + 1], r, w * half_bits_to_f32(h4[i] >> 16));
+                }
             }
         }
         const float inv = 1.f / den;
@@ -431,17 +432,17 @@ static __device__ __forceinline__ void merge_task(Ctx& c, const TaskRec& t) {
         const int hq = g * rep + (4 * u) / p.hd, d0 = (4 * u) % p.hd;
         const int cp = blockIdx.x % PART_COPIES;
         const float* ml = p.part_ml + ((size_t)cp * p.Hq + hq) * C * 2;
-        const float* base = p.part_acc + ((size_t)cp * p.Hq + hq) * C * p.hd + d0;
+        const uint16_t* base = p.part_acc + ((size_t)cp * p.Hq + hq) * C * p.hd + d0;
         float M = -3.0e38f, den = 0.f;
         float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int c0 = 0; c0 < C; c0 += 8) {
             float2 mlv[8];
-            float4 a[8];
+            uint2 a[8];  // four fp16 accumulators
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const int ch = min(c0 + k, C - 1);
                 mlv[k] = __ldcg((const float2*)(ml + 2 * ch));
-                a[k] = __ldcg((const float4*)(base + (size_t)ch * p.hd));
+                a[k] = __ldcg((const uint2*)(base + (size_t)ch * p.hd));
             }
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
@@ -450,10 +451,10 @@ static __device__ __forceinline__ void merge_task(Ctx& c, const TaskRec& t) {
                 const float r = expf(M - Mn), w = expf(mlv[k].x - Mn);
                 M = Mn;
                 den = fmaf(den, r, w * mlv[k].y);
-                o.x = fmaf(o.x, r, w * a[k].x);
-                o.y = fmaf(o.y, r, w * a[k].y);
-                o.z = fmaf(o.z, r, w * a[k].z);
-                o.w = fmaf(o.w, r, w * a[k].w);
+                o.x = fmaf(o.x, r, w * half_bits_to_f32(a[k].x & 0xFFFFu));
+                o.y = fmaf(o.y, r, w * half_bits_to_f32(a[k].x >> 16));
+                o.z = fmaf(o.z, r, w * half_bits_to_f32(a[k].y & 0xFFFFu));
+                o.w = fmaf(o.w, r, w * half_bits_to_f32(a[k].y >> 16));
             }
         }
         const float inv = 1.f / den;
@@ -1248,7 +1249,8 @@ static __device__ __forceinline__ bool attn_task(Ctx& c, const TaskRec& t, int t
         if (h < rep) {
 #pragma unroll
             for (int k = 0; k < PART_COPIES; ++k)
-                p.part_acc[(((size_t)k * p.Hq + g * rep + h) * C + ch) * HD + dd] = acc[e];
+                p.part_acc[(((size_t)k * p.Hq + g * rep + h) * C + ch) * HD + dd] =
+                    __half_as_ushort(__float2half_rn(acc[e]));
         }
     }
     if (c.tid < rep) {
