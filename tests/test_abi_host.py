@@ -244,3 +244,16 @@ def test_tagged_wait_must_be_covered_and_current(mk):
     st, why = mk.mk_validate_ir(m)
     assert st != mk.MK_OK and "tagged wait" in why, why
     assert not S.verdict(m)[0]
+
+
+@pytest.mark.parametrize("name", ["llama-1b", "llama-2b-fp16", "llama3-8b-8k"])
+def test_lowering_tags_every_layer(mk, name):
+    """The QKV -> attention hop of every layer travels as tagged values at the
+    bench's launch shape, and the validator accepts the result."""
+    w = synthetic.get_workload(name)
+    ir = mk.mk_build_ir(mk.make_desc(w), mk.make_config(), 152)
+    assert len(ir["tagged"]) == w.n_layers
+    assert set(ir["tagged"].values()) == {1}  # the q/k/v buffer
+    waiters = [t for t in ir["tasks"] if any(c in ir["tagged"] for c, _, _ in t["waits"])]
+    assert waiters and {mk.OPS[t["op"]] for t in waiters} == {"attn"}
+    assert mk.mk_validate_ir(ir)[0] == mk.MK_OK
