@@ -289,7 +289,7 @@ void mk_destroy(mk_handle* h);
 
 /* ------------------------------------------------------------------ allocation-free decode */
 /* Largest scratch mk_decode_static accepts (8 MiB; a Llama-3-8B layout with an
- * 8k context needs about 2.5 MiB). */
+ * 8k context needs about 1.6 MiB on 152 SMs). */
 #define MK_STATIC_SCRATCH_BYTES (8u << 20)
 
 /* Greedy decode of n_steps tokens from position pos feeding `token`, without a
@@ -312,8 +312,8 @@ void mk_destroy(mk_handle* h);
  * device) and, like every call whose desc or resolved config differs from the
  * previous call's on that device, lowers, validates and uploads the schedule;
  * make that first call before any stream capture.  Every call zeroes the
- * status words, sync counters and argmax key before its launch; all other
- * scratch is written before it is read.
+ * status words, sync counters, argmax key and tagged q/k/v words before its
+ * launch; all other scratch is written before it is read.
  * Calls share the one array per device: calls that overlap (other host
  * threads, other streams) race on it.  Calls of this library are serialised
  * by a host lock, and each returns only after its launch has finished.
