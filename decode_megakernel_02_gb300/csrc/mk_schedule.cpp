@@ -773,29 +773,75 @@ mk_status validate_ir(const mk_ir* ir, std::string* why) {
     for (int b = 0; b < NB; ++b)
         for (int s = 0; s < S; ++s)
             std::stable_sort(on[b][s].begin(), on[b][s].end(), [](const Inst& x, const Inst& y) { return x.seq < y.seq; });
+    // Per instance X with a write or atomic access: its non-read ranges, sorted
+    // by start with a running maximum of their ends, answer "does range y
+    // conflict with X" by binary search.  Atomic ranges are kept apart, since
+    // an atomic y conflicts only with X's plain writes.
+    struct Rng {
+        int64_t lo, hi;
+    };
+    auto prep = [](std::vector<Rng>& v, std::vector<int64_t>& pm) {
+        std::sort(v.begin(), v.end(), [](const Rng& x, const Rng& y) { return x.lo < y.lo; });
+        pm.resize(v.size());
+        int64_t m = INT64_MIN;
+        for (size_t k = 0; k < v.size(); ++k) pm[k] = m = std::max(m, v[k].hi);
+    };
+    auto hits = [](const std::vector<Rng>& v, const std::vector<int64_t>& pm, int64_t lo, int64_t hi) -> int {
+        // index of a range of v overlapping [lo, hi), or -1
+        size_t n = std::lower_bound(v.begin(), v.end(), hi, [](const Rng& x, int64_t h) { return x.lo < h; }) - v.begin();
+        if (n == 0 || pm[n - 1] <= lo) return -1;
+        for (size_t k = n; k-- > 0;)
+            if (v[k].hi > lo) return (int)k;
+        return -1;
+    };
+    std::vector<Rng> xw, xa;  // X's plain-write and atomic ranges
+    std::vector<int64_t> pw, pa;
     for (int b = 0; b < NB; ++b) {
         const std::vector<int32_t>& vc = vcs[tset[b] > 0 ? tset[b] : 0];
-        for (int sx = 0; sx < S; ++sx)
-            for (const Inst& x : on[b][sx]) {
-                if (x.kind == MK_ACC_READ) continue;  // every conflicting pair has a write or atomic side
+        for (int sx = 0; sx < S; ++sx) {
+            const auto& lx = on[b][sx];
+            for (size_t i = 0; i < lx.size();) {
+                size_t j = i;
+                xw.clear();
+                xa.clear();
+                for (; j < lx.size() && lx[j].seq == lx[i].seq; ++j) {  // one instance: [i, j)
+                    if (lx[j].kind == MK_ACC_WRITE) xw.push_back({lx[j].lo, lx[j].hi});
+                    if (lx[j].kind == MK_ACC_ATOMIC) xa.push_back({lx[j].lo, lx[j].hi});
+                }
+                const Inst& x = lx[i];
+                i = j;
+                if (xw.empty() && xa.empty()) continue;  // every conflicting pair has a write or atomic side
+                prep(xw, pw);
+                prep(xa, pa);
                 const int32_t* vx = &vc[(size_t)tn(x.t, x.e) * S];
                 for (int s = 0; s < S; ++s) {
                     const auto& list = on[b][s];
                     auto it = std::upper_bound(list.begin(), list.end(), vx[s],
                                                [](int32_t v, const Inst& y) { return v < y.seq; });
+                    int32_t yseq = -1;
                     for (; it != list.end(); ++it) {
                         const Inst& y = *it;
-                        if (vc[(size_t)tn(y.t, y.e) * S + sx] >= x.seq) break;  // y comes after x
+                        if (y.seq != yseq) {  // the ordering test holds for every access of an instance
+                            yseq = y.seq;
+                            if (vc[(size_t)tn(y.t, y.e) * S + sx] >= x.seq) break;  // y comes after x
+                        }
                         if (y.t == x.t && y.e == x.e) continue;
-                        if (y.lo >= x.hi || x.lo >= y.hi) continue;
-                        if (x.kind == MK_ACC_ATOMIC && y.kind == MK_ACC_ATOMIC) continue;
+                        int k = hits(xw, pw, y.lo, y.hi);
+                        const Rng* r = k >= 0 ? &xw[k] : nullptr;
+                        if (!r && y.kind != MK_ACC_ATOMIC) {
+                            k = hits(xa, pa, y.lo, y.hi);
+                            r = k >= 0 ? &xa[k] : nullptr;
+                        }
+                        if (!r) continue;
                         return fail("race: task " + std::to_string(x.t) + " (step " + std::to_string(x.e) +
                                     ") and task " + std::to_string(y.t) + " (step " + std::to_string(y.e) +
-                                    ") touch buffer " + std::to_string(b) + " bytes [" + std::to_string(std::max(x.lo, y.lo)) +
-                                    ", " + std::to_string(std::min(x.hi, y.hi)) + ") without happens-before");
+                                    ") touch buffer " + std::to_string(b) + " bytes [" +
+                                    std::to_string(std::max(r->lo, y.lo)) + ", " + std::to_string(std::min(r->hi, y.hi)) +
+                                    ") without happens-before");
                     }
                 }
             }
+        }
     }
 
     // ---- correctness: every task's writes reach an output (two steps).
