@@ -18,7 +18,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 CU_SRCS = ["mk_vm_bf16.cu", "mk_vm_fp16.cu", "mk_vm_int8.cu", "mk_vm_int4.cu", "mk_vm_common.cu", "mk_runtime.cu",
            "mk_static.cu"]
-CPP_SRCS = ["mk_host.cpp", "mk_schedule.cpp"]
+CPP_SRCS = ["mk_host.cpp", "mk_schedule.cpp", "mk_validate.cpp"]
 
 
 def _sources():
