@@ -25,7 +25,7 @@ MK_ACC_READ, MK_ACC_WRITE, MK_ACC_ATOMIC = 1, 2, 3
 MK_BUF_OUTPUT = 1
 MK_IR_MAX_WAITS = 2
 MK_STATIC_SCRATCH_BYTES = 8 << 20
-OPS = {1: "qkv", 2: "attn", 3: "o", 4: "gu", 5: "down", 6: "lm", 7: "fin"}
+OPS = {1: "qkv", 2: "attn", 3: "o", 4: "gu", 5: "down", 6: "lm", 7: "fin", 8: "ffn", 9: "merge"}
 WDTYPES = {"bf16": MK_W_BF16, "fp16": MK_W_FP16, "int8": MK_W_INT8_ROW, "int4": MK_W_INT4_G128}
 STATUS_NAMES = {0: "MK_OK", 1: "MK_ERR_INVALID_ARG", 2: "MK_ERR_UNSUPPORTED", 3: "MK_ERR_SCHEDULE_INVALID",
                 4: "MK_ERR_CAPACITY", 5: "MK_ERR_CUDA", 6: "MK_ERR_TIMEOUT", 7: "MK_ERR_DEVICE"}
