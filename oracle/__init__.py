@@ -19,4 +19,4 @@ heads; incremental KV-cache decode equal to full causal recompute; brute force
 on tiny quantiser rows; the schedule simulator against hand-built schedules
 whose safety is known by inspection.
 """
-from . import llama, quant, schedule_sim  # noqa: F401
+from . import llama, quant, sampling, schedule_sim  # noqa: F401
