@@ -210,11 +210,12 @@ def teacher_forced(m: Model, prompt, forced, max_seq=None):
     return np.stack(out)
 
 
-def forward_full(m: Model, tokens):
+def forward_full(m: Model, tokens, last=None):
     """All positions at once with a causal mask (matrix form).
 
     K and V are rounded to bf16 exactly as the cache stores them.  Returns the
-    logits for every position [T, V]."""
+    logits for every position [T, V], or for the last ``last`` positions only
+    (the final norm and LM head are then applied to those rows alone)."""
     s = m.s
     T = len(tokens)
     x = m.W("embed")[np.asarray(tokens)].copy()
@@ -236,4 +237,6 @@ def forward_full(m: Model, tokens):
         x = x + o.reshape(T, -1) @ m.W(f"l{l}.wo").T
         h = rmsnorm(x, m.W(f"l{l}.ffn_norm"), s.rms_eps)
         x = x + swiglu(h @ m.W(f"l{l}.wgate").T, h @ m.W(f"l{l}.wup").T) @ m.W(f"l{l}.wdown").T
+    if last is not None:
+        x = x[T - last:]
     return rmsnorm(x, m.W("final_norm"), s.rms_eps) @ m.W("lm_head").T
