@@ -24,7 +24,14 @@ import sys
 import threading
 import time
 
-import numpy as np
+# The CPU oracle's BLAS threads are set before NumPy loads its BLAS: all host
+# cores unless the caller fixed a count.
+ORACLE_THREADS = int(os.environ.get("OPENBLAS_NUM_THREADS") or os.environ.get("OMP_NUM_THREADS")
+                     or os.cpu_count() or 1)
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, str(ORACLE_THREADS))
+
+import numpy as np  # noqa: E402
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
@@ -154,6 +161,26 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def blas_info():
+    """BLAS library NumPy uses and its thread count, as far as this NumPy reports them."""
+    vendor, threads = "unknown", ORACLE_THREADS
+    try:
+        cfg = np.show_config(mode="dicts")
+        b = cfg.get("Build Dependencies", {}).get("blas", {})
+        vendor = f"{b.get('name', 'unknown')} {b.get('version', '')}".strip()
+    except Exception:
+        pass
+    try:
+        from threadpoolctl import threadpool_info
+        pools = [p for p in threadpool_info() if p.get("user_api") == "blas"]
+        if pools:
+            threads = int(pools[0]["num_threads"])
+            vendor = f"{pools[0].get('internal_api', vendor)} {pools[0].get('version', '')}".strip()
+    except Exception:
+        pass
+    return vendor, threads
+
+
 def oracle_rate(w, weights, budget_s=12.0, min_steps=2, max_steps=64):
     """Tokens/s of the float64 oracle decoding from the end of the prompt."""
     from oracle import llama as L
@@ -192,6 +219,7 @@ def main():
     ap.add_argument("--rows-in-flight", type=int, default=0)
     ap.add_argument("--chunks", type=int, default=0)
     ap.add_argument("--tokens", type=int, default=0, help="decode tokens per step (default: the workload's)")
+    ap.add_argument("--l2-prefetch-kb", type=int, default=0, help="0: default, -1: off")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -213,12 +241,13 @@ def main():
             if s >= args.warmup:
                 rates.append(r)
         v = float(np.mean(rates))
-        cores = os.cpu_count()
+        vendor, cores = blas_info()
         line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * 4 / v,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic", "config": config,
-                "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "blas": vendor,
+                                 "host_cpus": os.cpu_count(),
                                  "sample": f"up to 4 greedy decode steps from position {pos0} per step"},
                 "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
@@ -238,7 +267,8 @@ def main():
     weights = synthetic.generate_weights(w)
     desc = mk.make_desc(w)
     blob = mk.pack_model(desc, weights)
-    cfg = mk.make_config(sms=args.sms, rows_in_flight=args.rows_in_flight, attn_chunks=args.chunks)
+    cfg = mk.make_config(sms=args.sms, rows_in_flight=args.rows_in_flight, attn_chunks=args.chunks,
+                         l2_prefetch_kb=args.l2_prefetch_kb)
     dec = mk.Decoder(desc, blob, cfg)
     del blob
     prompt = synthetic.generate_prompt(w)
@@ -318,9 +348,11 @@ def main():
         line["clocks"] = clocks
     if rank == 0 and not args.no_cpu_baseline:
         r, n, dt = oracle_rate(w, weights)
-        line["cpu_baseline"] = {"value": r, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+        vendor, threads = blas_info()
+        line["cpu_baseline"] = {"value": r, "unit": UNIT, "cores": threads, "kind": "oracle", "blas": vendor,
+                                "host_cpus": os.cpu_count(),
                                 "sample": f"{n} greedy decode steps from position {pos0} ({dt:.1f} s; prompt cache "
-                                          f"zero-filled, untimed), float64 NumPy, BLAS threads = all cores"}
+                                          f"zero-filled, untimed), float64 NumPy, {threads} BLAS threads"}
     if rank == 0:
         print(json.dumps(line))
     dec.close()

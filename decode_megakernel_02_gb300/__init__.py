@@ -25,7 +25,8 @@ MK_ACC_READ, MK_ACC_WRITE, MK_ACC_ATOMIC = 1, 2, 3
 MK_BUF_OUTPUT = 1
 MK_IR_MAX_WAITS = 2
 MK_STATIC_SCRATCH_BYTES = 8 << 20
-OPS = {1: "qkv", 2: "attn", 3: "o", 4: "gu", 5: "down", 6: "lm", 7: "fin", 8: "ffn", 9: "merge"}
+OPS = {1: "qkv", 2: "attn", 3: "o", 4: "gu", 5: "down", 6: "lm", 7: "fin", 8: "ffn", 9: "merge", 10: "select"}
+MK_MAX_TOP_K = 64
 WDTYPES = {"bf16": MK_W_BF16, "fp16": MK_W_FP16, "int8": MK_W_INT8_ROW, "int4": MK_W_INT4_G128}
 STATUS_NAMES = {0: "MK_OK", 1: "MK_ERR_INVALID_ARG", 2: "MK_ERR_UNSUPPORTED", 3: "MK_ERR_SCHEDULE_INVALID",
                 4: "MK_ERR_CAPACITY", 5: "MK_ERR_CUDA", 6: "MK_ERR_TIMEOUT", 7: "MK_ERR_DEVICE"}
@@ -42,7 +43,13 @@ class mk_model_desc(ctypes.Structure):
 
 class mk_schedule_config(ctypes.Structure):
     _fields_ = [("sms", ctypes.c_int32), ("rows_in_flight", ctypes.c_int32), ("attn_chunks", ctypes.c_int32),
-                ("watchdog_ms", ctypes.c_int32)]
+                ("watchdog_ms", ctypes.c_int32), ("l2_prefetch_kb", ctypes.c_int32),
+                ("token_select", ctypes.c_int32)]
+
+
+class mk_sampling(ctypes.Structure):
+    _fields_ = [("temperature", ctypes.c_float), ("top_k", ctypes.c_int32), ("seed", ctypes.c_uint64),
+                ("eos_id", ctypes.c_int32)]
 
 
 class mk_ir_task(ctypes.Structure):
@@ -97,6 +104,8 @@ SIGNATURES = {
     "mk_get_launch_info": (_I32, [_P, ctypes.POINTER(_I32), ctypes.POINTER(_I32), ctypes.POINTER(_I32),
                                   ctypes.POINTER(_I32), ctypes.POINTER(_I32)]),
     "mk_launch_count": (_I64, [_P]),
+    "mk_set_sampling": (_I32, [_P, ctypes.POINTER(mk_sampling)]),
+    "mk_last_steps": (_I32, [_P]),
     "mk_last_error": (ctypes.c_char_p, [_P]),
     "mk_destroy": (None, [_P]),
     "mk_decode_static": (_I32, [_DESC, _CFG, _P, _SZ, _P, _SZ, _I32, _I32, _I32, _P, _P, _P]),
@@ -147,8 +156,8 @@ def make_desc(workload, max_seq=None, wdtype=None, flags=0):
                          workload.rope_theta, max_seq or workload.max_seq, wd, base, flags)
 
 
-def make_config(sms=0, rows_in_flight=0, attn_chunks=0, watchdog_ms=0):
-    return mk_schedule_config(sms, rows_in_flight, attn_chunks, watchdog_ms)
+def make_config(sms=0, rows_in_flight=0, attn_chunks=0, watchdog_ms=0, l2_prefetch_kb=0, token_select=0):
+    return mk_schedule_config(sms, rows_in_flight, attn_chunks, watchdog_ms, l2_prefetch_kb, token_select)
 
 
 # ------------------------------------------------------------------ host calls
@@ -337,12 +346,23 @@ class Decoder:
 
     def decode(self, n_steps, out=None):
         """Greedy decode (synchronous); returns int32 ids (numpy)."""
-        out = np.empty(n_steps, np.int32) if out is None else out
+        if out is None:
+            out = np.empty(n_steps, np.int32)
+        elif not (isinstance(out, np.ndarray) and out.dtype == np.int32 and out.flags.c_contiguous
+                  and out.size >= n_steps):
+            raise ValueError("out must be a C-contiguous int32 numpy array of at least n_steps elements")
         _check(load().mk_decode(self.h, n_steps, out.ctypes.data), self.h)
         return out
 
     def decode_async(self, n_steps, forced=None, out_ids=None, logits=None):
         """Enqueue one launch; tensors are device tensors (or None)."""
+        torch = self.torch
+        for t, dt, n, name in ((forced, torch.int32, n_steps, "forced"), (out_ids, torch.int32, n_steps, "out_ids"),
+                               (logits, torch.float32, n_steps * self.desc.vocab, "logits")):
+            if t is not None and not (t.device == self.weights.device and t.dtype == dt and t.is_contiguous()
+                                      and t.numel() >= n):
+                raise ValueError(f"{name} must be a contiguous {dt} tensor on {self.weights.device} "
+                                 f"with at least {n} elements")
         ptr = (lambda t: t.data_ptr() if t is not None else None)
         _check(load().mk_decode_async(self.h, n_steps, ptr(forced), ptr(out_ids), ptr(logits)), self.h)
 
@@ -371,6 +391,17 @@ class Decoder:
     def launch_count(self):
         return load().mk_launch_count(self.h)
 
+    def set_sampling(self, temperature=0.0, top_k=0, seed=0, eos_id=-1):
+        """Token selection of later launches (mk_set_sampling): greedy at
+        temperature 0, else Gumbel-max sampling over all tokens or the top_k
+        logits; decoding stops after emitting eos_id (-1: never)."""
+        s = mk_sampling(float(temperature), int(top_k), int(seed) & 0xFFFFFFFFFFFFFFFF, int(eos_id))
+        _check(load().mk_set_sampling(self.h, ctypes.byref(s)), self.h)
+
+    def last_steps(self):
+        """Steps the last launch ran (fewer than asked after an EOS stop)."""
+        return load().mk_last_steps(self.h)
+
     def teacher_forced(self, forced_tokens):
         """Feed forced_tokens[s] at step s; returns (logits [n, V] float32, argmax ids [n])."""
         torch = self.torch
@@ -389,7 +420,16 @@ def decode_static(desc, weights, kv, pos, token, n_steps, cfg=None, logits=None,
     device).  weights/kv/logits are caller-owned device tensors; returns the
     int32 ids (numpy, host)."""
     import torch
-    out = np.empty(n_steps, np.int32) if out is None else out
+    if out is None:
+        out = np.empty(n_steps, np.int32)
+    elif not (isinstance(out, np.ndarray) and out.dtype == np.int32 and out.flags.c_contiguous
+              and out.size >= n_steps):
+        raise ValueError("out must be a C-contiguous int32 numpy array of at least n_steps elements")
+    if logits is not None and not (logits.is_cuda and logits.dtype == torch.float32 and logits.is_contiguous()
+                                   and logits.device == weights.device
+                                   and logits.numel() >= n_steps * desc.vocab):
+        raise ValueError("logits must be a contiguous float32 tensor on the weights' device with at least "
+                         "n_steps * vocab elements")
     st = stream or torch.cuda.current_stream()
     _check(load().mk_decode_static(ctypes.byref(desc), ctypes.byref(cfg) if cfg else None, weights.data_ptr(),
                                    weights.numel() * weights.element_size(), kv.data_ptr(),

@@ -24,12 +24,14 @@ BlobLayout blob_layout(const mk_model_desc* d);
 struct Config {
     int sms, rw, C;
     int64_t watchdog_ns;
+    int pf_bytes;             // L2 prefetch of each GEMV task's weights per CTA (0: off)
+    bool token_select;        // an OP_SELECT task after the LM head selects each step's token
 };
 mk_status resolve_config(const mk_model_desc* d, const mk_schedule_config* cfg, int n_sms,
                          Config* out);
 
 // IR buffers of the decode path.
-enum Buf : int32_t { B_X = 0, B_QKV, B_PART, B_H, B_LOGITS, B_KEY, B_OUT, B_KV, B_ATT, B_COUNT };
+enum Buf : int32_t { B_X = 0, B_QKV, B_PART, B_H, B_LOGITS, B_KEY, B_OUT, B_KV, B_ATT, B_CAND, B_TOKW, B_COUNT };
 
 // Whether the split-KV partials are merged by per-group OP_MERGE tasks (true
 // when every O CTA would otherwise read more than 64 KB of partials).
@@ -48,6 +50,8 @@ struct Lowering {
     // records keep neither the signal nor the wait.
     std::vector<int32_t> ctr_buf;
     int64_t bytes_per_sm_max = 0, bytes_per_sm_min = 0;
+    int32_t ctr_tok = 0, n_tok = 0;   // the counter after which a step's token is final, its producers
+    int32_t lm_rows_max = 0;          // most LM-head rows of one CTA
 };
 mk_status lower(const mk_model_desc* d, const Config& c, Lowering* out);
 
@@ -64,7 +68,7 @@ mk_status validate_ir(const mk_ir* ir, std::string* why);
 
 // Workspace layout (byte offsets).
 struct WsLayout {
-    int64_t status, counters, key, recs, queue_off, inv_freq, x, qkv, part_ml, part_acc, att,
+    int64_t status, counters, key, tokw, cand, recs, queue_off, inv_freq, x, qkv, part_ml, part_acc, att,
         h, tok, out_ids, total;
 };
 WsLayout ws_layout(const mk_model_desc* d, const Config& c, int64_t n_tasks, int32_t n_counters);

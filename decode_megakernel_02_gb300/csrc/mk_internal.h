@@ -19,7 +19,8 @@ enum Op : int32_t {
     OP_FIN = 7,   // read the step's argmax key -> out id
     OP_FFN = 8,   // RMSNorm prologue + gate/up rows + SwiGLU (kept on chip) + the down
                   // projection's columns of those units, red.add into the next residual
-    OP_MERGE = 9  // split-KV merge of one KV group's query heads -> att (O then reads att)
+    OP_MERGE = 9, // split-KV merge of one KV group's query heads -> att (O then reads att)
+    OP_SELECT = 10  // token-select: the step's top-k sample from every CTA's candidates
 };
 
 constexpr int NT = 256;                 // threads per CTA (eight warps)
@@ -38,6 +39,8 @@ constexpr int CTR_STRIDE = 32;          // u32 words between counters (128 B lin
 constexpr int MAX_HC = 1024;            // query heads x split-KV chunks (merge scratch)
 constexpr int FFN_BLOCK = 8;            // hidden units per 16-byte column block of a fused down projection
 constexpr int FFN_MAX_UNITS = 2 * MAX_HC;  // hidden units of one OP_FFN task (its SwiGLU outputs reuse the merge scratch)
+constexpr int MAX_TOP_K = MK_MAX_TOP_K;     // top-k candidates per CTA
+constexpr int LM_MAX_ROWS = 2 * MAX_HC;     // LM-head rows of one CTA under top-k sampling (kept in the merge scratch)
 
 // The FFN runs fused (OP_FFN) for 16-bit weights when every warp's share of
 // the d_model output rows is a whole number of 32-row lines (d_model % 256
@@ -108,7 +111,7 @@ struct BlobLayout {
 struct VmParams {
     const uint8_t* w;          // packed blob
     uint16_t* kv;              // bf16 KV cache [L][2][Hkv][max_seq][hd]
-    uint32_t* status;          // [0] status, [1] queue index, [2] detail, [3] last token
+    uint32_t* status;          // [0] status, [1] queue index, [2] detail, [3] last token, [4] steps run
     uint32_t* counters;        // n_counters lines of CTR_STRIDE words
     unsigned long long* key;   // the step's packed argmax key
     const TaskRec* recs;       // every CTA's queue, concatenated in queue order
@@ -135,6 +138,15 @@ struct VmParams {
     int32_t xs_floats;         // shared-memory input vector capacity: max(d, q_dim)
     int32_t tab_cap;           // task records a CTA's shared-memory table holds (longest queue)
     int64_t watchdog_ns;
+    int32_t pf_bytes;          // L2 prefetch of a GEMV task's weights past the rings' lookahead, per CTA (0: off)
+    // token selection
+    float inv_temp;            // 1 / temperature (0: greedy argmax)
+    int32_t top_k;             // > 0: candidates are the top_k logits (token-select task)
+    uint32_t seed_lo, seed_hi; // Philox4x32-10 key
+    int32_t eos;               // -1: none; else a launch stops after the step that selects it
+    int32_t ctr_tok, n_tok;    // the counter after which the step's token is final, and its producers
+    unsigned long long* cand;  // token-select: MAX_TOP_K candidate keys per CTA
+    unsigned long long* tokw;  // token-select: the selected token | (epoch + 1) << 32 (nullptr: read the key)
     unsigned long long* trace; // nullable: per-task timestamps [ctas][trace_cap][4]
     int32_t trace_cap;
 };

@@ -53,6 +53,16 @@ struct mk_handle {
     std::vector<int32_t> queue_store;    // owns `queue` for handles made by mk_create
     unsigned long long* trace = nullptr;
     int32_t trace_cap = 0;
+    // token selection (mk_set_sampling)
+    float temperature = 0.f;
+    int32_t top_k = 0;
+    uint64_t seed = 0;
+    int32_t eos = -1;
+    int32_t ctr_tok = 0, n_tok = 0;      // the counter after which a step's token is final, its producers
+    int32_t lm_rows_max = 0;
+    int32_t launched = 0;                // steps of the last launch
+    int32_t last_steps = 0;              // steps it ran (fewer after an EOS stop)
+    bool unsettled = false;              // an async launch with EOS whose step count is not read yet
     std::string err;
 };
 
@@ -80,9 +90,11 @@ mk_status cuda_fail(mk_handle* h, cudaError_t e, const char* what) {
     } while (0)
 
 mk_status reset_sync_state(mk_handle* h) {
-    CK(h, cudaMemsetAsync(h->wsp + h->ws.status, 0, 16, h->st));
+    CK(h, cudaMemsetAsync(h->wsp + h->ws.status, 0, 32, h->st));
     CK(h, cudaMemsetAsync(h->wsp + h->ws.counters, 0, (size_t)h->n_counters * CTR_STRIDE * 4, h->st));
     CK(h, cudaMemsetAsync(h->wsp + h->ws.key, 0, 8, h->st));
+    CK(h, cudaMemsetAsync(h->wsp + h->ws.tokw, 0, 8, h->st));
+    CK(h, cudaMemsetAsync(h->wsp + h->ws.cand, 0, (size_t)h->c.sms * MAX_TOP_K * 8, h->st));
     // tagged values: tags restart with the epoch, so no stale word may match
     CK(h, cudaMemsetAsync(h->wsp + h->ws.qkv, 0, (size_t)(h->ws.part_ml - h->ws.qkv), h->st));
     h->epoch = 0;
@@ -90,8 +102,21 @@ mk_status reset_sync_state(mk_handle* h) {
     return MK_OK;
 }
 
+// Let the kernel take up to the device's opt-in shared memory per block
+// (minus its static shared memory).  The attribute is per kernel function, so
+// every handle and static call sets the same value.
+cudaError_t raise_smem_limit(const void* kfn, int smem_optin) {
+    cudaFuncAttributes fa{};
+    cudaError_t e = cudaFuncGetAttributes(&fa, kfn);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                smem_optin - (int)fa.sharedSizeBytes);
+}
+
 mk_status launch(mk_handle* h, int n_steps, const int32_t* forced, int32_t* out_ids, float* logits,
                  int skip_lm) {
+    if (h->unsettled)
+        return herr(h, MK_ERR_INVALID_ARG, "an earlier launch with an EOS id is not finished: call mk_finish first");
     if (h->dirty || h->epoch + (uint32_t)n_steps >= (uint32_t)KEY_TAG_MAX - 1u) {
         mk_status st = reset_sync_state(h);
         if (st) return st;
@@ -145,21 +170,48 @@ mk_status launch(mk_handle* h, int n_steps, const int32_t* forced, int32_t* out_
     p.xs_floats = h->xs_floats;
     p.tab_cap = h->tab_cap;
     p.watchdog_ns = h->c.watchdog_ns;
+    p.pf_bytes = h->c.pf_bytes;
+    const bool sampling = h->temperature > 0.f && !skip_lm;
+    p.inv_temp = sampling ? 1.f / h->temperature : 0.f;
+    p.top_k = sampling ? h->top_k : 0;
+    p.seed_lo = (uint32_t)h->seed;
+    p.seed_hi = (uint32_t)(h->seed >> 32);
+    p.eos = skip_lm ? -1 : h->eos;
+    p.ctr_tok = h->ctr_tok;
+    p.n_tok = h->n_tok;
+    p.cand = (unsigned long long*)(h->wsp + h->ws.cand);
+    p.tokw = h->c.token_select ? (unsigned long long*)(h->wsp + h->ws.tokw) : nullptr;
     p.trace = h->trace;
     p.trace_cap = h->trace_cap;
     void* args[] = {&p};
     CK(h, cudaLaunchCooperativeKernel(h->kfn, dim3(h->c.sms), dim3(THREADS), args, h->smem, h->st));
     h->epoch += (uint32_t)n_steps;
     h->launches++;
+    h->launched = n_steps;
+    h->last_steps = n_steps;
     return MK_OK;
 }
 
-mk_status read_status(mk_handle* h) {
-    uint32_t s[4] = {0, 0, 0, 0};
+// Steps the last decode launch ran, from the status word the FIN / select task
+// writes (s[4]); with an EOS id it may be fewer than launched, and the
+// synchronisation epoch advances only by the steps that ran.
+int32_t steps_run(mk_handle* h, const uint32_t* s) {
+    if (h->eos < 0) return h->launched;
+    const int32_t ran = (int32_t)s[4];
+    const int32_t steps = ran >= 1 && ran <= h->launched ? ran : h->launched;
+    h->epoch -= (uint32_t)(h->launched - steps);
+    h->last_steps = steps;
+    return steps;
+}
+
+mk_status read_status(mk_handle* h, uint32_t* out5 = nullptr) {
+    uint32_t s[5] = {0, 0, 0, 0, 0};
     CK(h, cudaMemcpyAsync(s, h->wsp + h->ws.status, sizeof s, cudaMemcpyDeviceToHost, h->st));
     CK(h, cudaStreamSynchronize(h->st));
+    if (out5) std::memcpy(out5, s, sizeof s);
     if (s[0] == DEV_OK) return MK_OK;
     h->dirty = true;
+    h->unsettled = false;
     const int task = h->queue && s[1] < (uint32_t)h->n_tasks ? h->queue[s[1]] : -1;
     if (s[0] == DEV_TIMEOUT)
         return herr(h, MK_ERR_TIMEOUT, "device wait gave up (task %d, step %u); counters are reset on the next launch",
@@ -274,6 +326,9 @@ mk_status mk_create(const mk_model_desc* desc, const mk_schedule_config* cfg, co
     h->tab_cap = tab_cap;
     h->queue_store = queue;
     h->queue = h->queue_store.data();
+    h->ctr_tok = lw.ctr_tok;
+    h->n_tok = lw.n_tok;
+    h->lm_rows_max = lw.lm_rows_max;
     if (!h->kfn) {
         delete h;
         set_error("no kernel for wdtype %d / base %d", desc->wdtype, desc->base_dtype);
@@ -284,7 +339,11 @@ mk_status mk_create(const mk_model_desc* desc, const mk_schedule_config* cfg, co
         delete h;
         return s;
     };
-    e = cudaFuncSetAttribute(h->kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->smem);
+    // The attribute belongs to the kernel function, not to this handle: other
+    // handles launch the same instantiation with their own (possibly larger)
+    // shared memory, so it is raised to the device's opt-in limit instead of
+    // this handle's need, and no handle can lower it under another.
+    e = raise_smem_limit(h->kfn, smem_optin);
     if (e != cudaSuccess) return fail(cuda_fail(h, e, "cudaFuncSetAttribute"));
     int per_sm = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, h->kfn, THREADS, h->smem);
@@ -350,9 +409,12 @@ mk_status mk_decode(mk_handle* h, int32_t n_steps, int32_t* out_ids_host) {
     int32_t* ids_dev = (int32_t*)(h->wsp + h->ws.out_ids);
     if ((st = launch(h, n_steps, nullptr, ids_dev, nullptr, 0))) return st;
     CK(h, cudaMemcpyAsync(out_ids_host, ids_dev, (size_t)n_steps * 4, cudaMemcpyDeviceToHost, h->st));
-    if ((st = read_status(h))) return st;
-    h->pos += n_steps;
-    h->pending = out_ids_host[n_steps - 1];
+    uint32_t s[5];
+    if ((st = read_status(h, s))) return st;
+    const int32_t steps = steps_run(h, s);
+    for (int32_t i = steps; i < n_steps; ++i) out_ids_host[i] = -1;  // after an EOS stop
+    h->pos += steps;
+    h->pending = out_ids_host[steps - 1];
     return MK_OK;
 }
 
@@ -363,6 +425,7 @@ mk_status mk_decode_async(mk_handle* h, int32_t n_steps, const int32_t* forced_d
     if ((st = launch(h, n_steps, forced_dev, out_ids_dev, logits_dev, 0))) return st;
     h->pos += n_steps;
     h->pending = -1;  // the last argmax stays on the device
+    h->unsettled = h->eos >= 0;  // pos is provisional until mk_finish reads the steps that ran
     return MK_OK;
 }
 
@@ -371,8 +434,45 @@ mk_status mk_finish(mk_handle* h) {
         set_error("NULL handle");
         return MK_ERR_INVALID_ARG;
     }
-    return read_status(h);
+    uint32_t s[5];
+    const bool unsettled = h->unsettled;
+    mk_status st = read_status(h, s);
+    if (st) return st;
+    if (unsettled) {
+        const int32_t launched = h->launched;
+        h->pos -= launched - steps_run(h, s);
+        h->unsettled = false;
+    }
+    return MK_OK;
 }
+
+mk_status mk_set_sampling(mk_handle* h, const mk_sampling* smp) {
+    if (!h || !smp) {
+        set_error("NULL argument");
+        return MK_ERR_INVALID_ARG;
+    }
+    if (!(smp->temperature >= 0.f) || !std::isfinite(smp->temperature))
+        return herr(h, MK_ERR_INVALID_ARG, "temperature %g: need a finite value >= 0", (double)smp->temperature);
+    if (smp->top_k < 0 || smp->top_k > MAX_TOP_K || smp->top_k > h->d.vocab)
+        return herr(h, MK_ERR_INVALID_ARG, "top_k %d: need 0 .. %d (and <= vocab)", smp->top_k, MAX_TOP_K);
+    if (smp->eos_id < -1 || smp->eos_id >= h->d.vocab)
+        return herr(h, MK_ERR_INVALID_ARG, "eos_id %d out of range", smp->eos_id);
+    if (smp->top_k > 0 && smp->temperature > 0.f) {
+        if (!h->c.token_select)
+            return herr(h, MK_ERR_UNSUPPORTED, "top-k sampling needs a handle created with token_select = 1");
+        if (h->lm_rows_max > LM_MAX_ROWS)
+            return herr(h, MK_ERR_UNSUPPORTED, "top-k sampling: %d LM-head rows on one CTA > %d", h->lm_rows_max,
+                        LM_MAX_ROWS);
+    }
+    if (h->unsettled) return herr(h, MK_ERR_INVALID_ARG, "call mk_finish first");
+    h->temperature = smp->temperature;
+    h->top_k = smp->top_k;
+    h->seed = smp->seed;
+    h->eos = smp->eos_id;
+    return MK_OK;
+}
+
+int32_t mk_last_steps(const mk_handle* h) { return h ? h->last_steps : 0; }
 
 mk_status mk_get_state(const mk_handle* h, int32_t* pos, int32_t* pending) {
     if (!h) {
@@ -423,7 +523,8 @@ namespace {
 // Per-device state of mk_decode_static: the scratch array's address and the
 // schedule currently uploaded into it.
 struct StaticSlot {
-    uint8_t* base = nullptr;  // set once per device
+    uint8_t* base = nullptr;  // set once per device context
+    unsigned long long ctx_id = 0;  // the context `base` belongs to
     bool ready = false;       // tables below match the uploaded schedule
     mk_model_desc d{};
     Config c{};
@@ -432,14 +533,44 @@ struct StaticSlot {
     const void* kfn = nullptr;
     size_t smem = 0;
     int32_t xs_floats = 0, tab_cap = 0;
+    int32_t ctr_tok = 0, n_tok = 0;
     std::vector<int32_t> queue;
 };
 constexpr int MAX_STATIC_DEVICES = 64;
 std::mutex g_static_mu;
 StaticSlot g_static[MAX_STATIC_DEVICES];
 
+// Unique id of the device's current context, through the driver entry points
+// that the runtime hands out (no link against the driver library).  The
+// device is made current first, which also creates its primary context.
+mk_status context_id(int dev, unsigned long long* id) {
+    using GetCurrent = int (*)(void**);
+    using GetId = int (*)(void*, unsigned long long*);
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    cudaError_t e = cudaSetDevice(dev);
+    cudaDriverEntryPointQueryResult q1 = cudaDriverEntryPointSymbolNotFound, q2 = q1;
+    if (e == cudaSuccess && !get_current)
+        e = cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", (void**)&get_current, 12000, cudaEnableDefault, &q1);
+    if (e == cudaSuccess && !get_id)
+        e = cudaGetDriverEntryPointByVersion("cuCtxGetId", (void**)&get_id, 12000, cudaEnableDefault, &q2);
+    if (e != cudaSuccess || !get_current || !get_id) {
+        get_current = nullptr;
+        get_id = nullptr;
+        set_error("context query: %s", e != cudaSuccess ? cudaGetErrorString(e) : "driver entry point not found");
+        return MK_ERR_CUDA;
+    }
+    void* ctx = nullptr;
+    if (get_current(&ctx) != 0 || !ctx || get_id(ctx, id) != 0) {
+        set_error("no current CUDA context on device %d", dev);
+        return MK_ERR_CUDA;
+    }
+    return MK_OK;
+}
+
 bool same_config(const Config& a, const Config& b) {
-    return a.sms == b.sms && a.rw == b.rw && a.C == b.C && a.watchdog_ns == b.watchdog_ns;
+    return a.sms == b.sms && a.rw == b.rw && a.C == b.C && a.watchdog_ns == b.watchdog_ns &&
+           a.pf_bytes == b.pf_bytes && a.token_select == b.token_select;
 }
 
 // Lower, validate and upload the schedule for (desc, c) into the slot's scratch.
@@ -480,7 +611,8 @@ mk_status static_setup(StaticSlot& s, const mk_model_desc* desc, const Config& c
         set_error("shared memory need %zu > %d", smem, smem_optin);
         return MK_ERR_UNSUPPORTED;
     }
-    cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    // the kernel-wide limit, as in mk_create (shared with every handle)
+    cudaError_t e = raise_smem_limit(kfn, smem_optin);
     int per_sm = 0;
     if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kfn, THREADS, smem);
     if (e != cudaSuccess) {
@@ -512,6 +644,8 @@ mk_status static_setup(StaticSlot& s, const mk_model_desc* desc, const Config& c
     s.xs_floats = xs_floats;
     s.tab_cap = tab_cap;
     s.queue = std::move(queue);
+    s.ctr_tok = lw.ctr_tok;
+    s.n_tok = lw.n_tok;
     s.ready = true;
     return MK_OK;
 }
@@ -556,7 +690,12 @@ mk_status mk_decode_static(const mk_model_desc* desc, const mk_schedule_config* 
         return MK_ERR_UNSUPPORTED;
     }
     StaticSlot& s = g_static[dev];
-    if (!s.base) {
+    // A reset of the device's primary context (cudaDeviceReset) re-creates the
+    // array, zeroed, at a possibly new address: a context with a new id gets
+    // the symbol lookup and the schedule upload again.
+    unsigned long long ctx = 0;
+    if ((st = context_id(dev, &ctx))) return st;
+    if (!s.base || s.ctx_id != ctx) {
         void* p = nullptr;
         e = static_scratch_address(&p);
         if (e != cudaSuccess || !p) {
@@ -564,6 +703,8 @@ mk_status mk_decode_static(const mk_model_desc* desc, const mk_schedule_config* 
             return MK_ERR_CUDA;
         }
         s.base = (uint8_t*)p;
+        s.ctx_id = ctx;
+        s.ready = false;
     }
     Config c;
     if ((st = resolve_config(desc, cfg, n_sms, &c))) return st;
@@ -600,6 +741,8 @@ mk_status mk_decode_static(const mk_model_desc* desc, const mk_schedule_config* 
     h.xs_floats = s.xs_floats;
     h.tab_cap = s.tab_cap;
     h.queue = s.queue.data();
+    h.ctr_tok = s.ctr_tok;
+    h.n_tok = s.n_tok;
     h.pos = pos;
     h.pending = token;
     h.has_seq = true;

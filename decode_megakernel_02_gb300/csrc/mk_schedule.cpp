@@ -51,6 +51,16 @@ mk_status resolve_config(const mk_model_desc* d, const mk_schedule_config* cfg, 
         return MK_ERR_INVALID_ARG;
     }
     c.watchdog_ns = (int64_t)(cfg->watchdog_ms ? cfg->watchdog_ms : 1000) * 1000000;
+    if (cfg->l2_prefetch_kb > (1 << 20)) {
+        set_error("l2_prefetch_kb %d above 1 GiB", cfg->l2_prefetch_kb);
+        return MK_ERR_INVALID_ARG;
+    }
+    c.pf_bytes = cfg->l2_prefetch_kb < 0 ? 0 : (cfg->l2_prefetch_kb ? cfg->l2_prefetch_kb : 1024) * 1024;
+    if (cfg->token_select != 0 && cfg->token_select != 1) {
+        set_error("token_select %d: 0 or 1", cfg->token_select);
+        return MK_ERR_INVALID_ARG;
+    }
+    c.token_select = cfg->token_select == 1;
     *out = c;
     return MK_OK;
 }
@@ -153,7 +163,10 @@ mk_status lower(const mk_model_desc* d, const Config& c, Lowering* lw) {
     // 5 + g chunks of KV group g (merge tasks only).
     const int CS = 5 + Hkv;
     const int CTR_LM = CS * L;
-    lw->n_counters = CS * L + 1;
+    const int CTR_TOK = CS * L + 1;  // token-select schedules: the step's token is final
+    const bool ts = c.token_select;
+    const int64_t CAND_BYTES = (int64_t)MAX_TOP_K * 8;  // one CTA's candidate keys
+    lw->n_counters = CS * L + (ts ? 2 : 1);
     lw->ctr_buf.assign(lw->n_counters, -1);
     auto ctr = [&](int l, int k) { return CS * l + k; };
     const bool mt = merge_tasks(d, c);
@@ -197,7 +210,7 @@ mk_status lower(const mk_model_desc* d, const Config& c, Lowering* lw) {
             int64_t r0 = p.second.first, r1 = p.second.second;
             DevTask t = gemv_task(OP_QKV, l, r0, r1 - r0, dm, bl.row_qkv, lb + bl.l_qkv, 1, ctr(l, 0));
             std::vector<mk_ir_access> acc;
-            acc.push_back(l == 0 ? A(B_KEY, MK_ACC_READ, 0, 8) : A(B_X, MK_ACC_READ, xb(l), xb(l) + 4 * dm));
+            acc.push_back(l == 0 ? A(ts ? B_TOKW : B_KEY, MK_ACC_READ, 0, 8) : A(B_X, MK_ACC_READ, xb(l), xb(l) + 4 * dm));
             acc.push_back(A(B_QKV, MK_ACC_WRITE, 8 * r0, 8 * r1));
             ids.push_back(B.add_task(p.first, t, acc));
         }
@@ -305,7 +318,7 @@ mk_status lower(const mk_model_desc* d, const Config& c, Lowering* lw) {
             const int cp = p.first % PART_COPIES;  // the CTA's copy
             if (mt) acc.push_back(A(B_ATT, MK_ACC_READ, cp * 4 * qd, (cp + 1) * 4 * qd));
             else acc.push_back(A(B_PART, MK_ACC_READ, cp * PART_BYTES, (cp + 1) * PART_BYTES));
-            if (l == 0) acc.push_back(A(B_KEY, MK_ACC_READ, 0, 8));
+            if (l == 0) acc.push_back(A(ts ? B_TOKW : B_KEY, MK_ACC_READ, 0, 8));
             else acc.push_back(A(B_X, MK_ACC_READ, xb(l) + 4 * r0, xb(l) + 4 * r1));  // residual
             acc.push_back(A(B_X, MK_ACC_WRITE, xm + 4 * r0, xm + 4 * r1));
             if (fused) acc.push_back(A(B_X, MK_ACC_WRITE, xb(l + 1) + 4 * r0, xb(l + 1) + 4 * r1));
@@ -383,24 +396,36 @@ mk_status lower(const mk_model_desc* d, const Config& c, Lowering* lw) {
         acc.push_back(A(B_X, MK_ACC_READ, xb(L), xb(L) + 4 * dm));
         acc.push_back(A(B_LOGITS, MK_ACC_WRITE, 4 * r0, 4 * r1, 4 * V, 0));
         acc.push_back(A(B_KEY, MK_ACC_ATOMIC, 0, 8));
+        if (ts) acc.push_back(A(B_CAND, MK_ACC_WRITE, p.first * CAND_BYTES, (p.first + 1) * CAND_BYTES));
         lm_ids.push_back(B.add_task(p.first, t, acc));
+        lw->lm_rows_max = std::max<int32_t>(lw->lm_rows_max, (int32_t)(r1 - r0));
     }
     B.set_wait(lm_ids, prev_ctr, (int)prev.size(), 0);
 
-    // ---- read the key -> out id; on the CTA that starts the next step first
+    // ---- read the key -> out id; on the CTA that starts the next step first.
+    // Token-select schedules: OP_SELECT picks the token from every CTA's
+    // candidates, publishes it and signals CTR_TOK.
     {
         DevTask t{};
-        t.op = OP_FIN;
+        t.op = ts ? OP_SELECT : OP_FIN;
         t.layer = L;
-        t.signal_ctr = -1;
+        t.signal_ctr = ts ? CTR_TOK : -1;
         std::vector<mk_ir_access> acc;
         acc.push_back(A(B_KEY, MK_ACC_READ, 0, 8));
         acc.push_back(A(B_OUT, MK_ACC_WRITE, 0, 4, 4, 0));
+        if (ts) {
+            acc.push_back(A(B_CAND, MK_ACC_READ, 0, c.sms * CAND_BYTES));
+            acc.push_back(A(B_TOKW, MK_ACC_WRITE, 0, 8));
+        }
         int id = B.add_task(fin_sm, t, acc);
         B.set_wait({id}, CTR_LM, (int)lm_ids.size(), 0);
     }
-    // The first layer of step e waits for the LM head of step e-1 (the token).
-    B.set_wait(first_qkv, CTR_LM, (int)lm_ids.size(), -1);
+    // The first layer of step e waits for the token of step e-1: the LM head's
+    // argmax key, or the token-select task's word.
+    if (ts) B.set_wait(first_qkv, CTR_TOK, 1, -1);
+    else B.set_wait(first_qkv, CTR_LM, (int)lm_ids.size(), -1);
+    lw->ctr_tok = ts ? CTR_TOK : CTR_LM;
+    lw->n_tok = ts ? 1 : (int)lm_ids.size();
 
     for (size_t i = 0; i < lw->tasks.size(); ++i) {
         lw->tasks[i].acc_begin = (int32_t)lw->acc.size();
@@ -515,7 +540,9 @@ WsLayout ws_layout(const mk_model_desc* d, const Config& c, int64_t n_tasks, int
     const int64_t qd = (int64_t)d->n_q_heads * d->head_dim, kd = (int64_t)d->n_kv_heads * d->head_dim;
     w.status = take(256);
     w.counters = take((int64_t)n_counters * CTR_STRIDE * 4);
-    w.key = take(128);
+    w.key = take(64);
+    w.tokw = take(64);
+    w.cand = take((int64_t)c.sms * MAX_TOP_K * 8);
     w.recs = take(n_tasks * (int64_t)sizeof(TaskRec));
     w.queue_off = take((int64_t)(c.sms + 1) * 4);
     w.inv_freq = take((int64_t)d->head_dim / 2 * 4);

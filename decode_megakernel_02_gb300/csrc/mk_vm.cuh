@@ -108,6 +108,7 @@ struct Shared {
     int32_t abort;                  // set when this CTA must stop
     int32_t tok;                    // broadcast of the step's input token
     unsigned long long t_waited;    // trace: when the current task's wait completed
+    unsigned long long t_ph[2];     // trace: input ready (prologue done / q,k,v arrived), compute done
 };
 
 // Weights per 16-byte chunk of a packed row's codes.
@@ -164,6 +165,7 @@ struct Ctx {
     int tid, lane, warp;
     bool abort;
     int deferred;       // batches of this task that issued no copy: issued after the signal
+    int cur;            // queue slot of the running task
 };
 
 __device__ __forceinline__ bool aborted(const VmParams& p) { return ld_volatile(p.status) != 0; }
@@ -173,6 +175,37 @@ static __device__ void raise_error(const VmParams& p, uint32_t code, uint32_t ta
         p.status[1] = task;
         p.status[2] = detail;
     }
+}
+
+// ------------------------------------------------------------------ L2 prefetch
+// The warps' rings keep NB - 1 batches of a few KB each in flight, which is
+// short of what HBM needs in flight to stream at full rate, and a task's first
+// ring copies go out only when the previous task frees its slots.  So just
+// before a GEMV task waits for its inputs, thread 0 asks L2 to prefetch the
+// task's weight bytes past the rings' lookahead (up to pf_bytes, in 32 KB bulk
+// requests); weight bytes never depend on activations.  The ring copies then
+// find them in L2.
+constexpr uint32_t PF_PIECE = 32768;
+
+__device__ __forceinline__ void prefetch_l2(const void* gptr, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gptr), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ uint32_t prefetch_range(const uint8_t* a, uint32_t n, uint32_t budget) {
+    n = min(n, budget);
+    for (uint32_t o = 0; o < n; o += PF_PIECE) prefetch_l2(a + o, min(PF_PIECE, n - o));
+    return n;
+}
+
+// Thread 0, before the task's wait.
+template <int WT>
+__device__ __forceinline__ void prefetch_task(const VmParams& p, const TaskRec& t) {
+    const uint32_t rb = (uint32_t)t.row_bytes16 * 16u;
+    const int skip = min(t.nrows, (ring_slots<WT>() - 1) * (NW / t.wpr) * RW);  // the rings' lookahead
+    uint32_t budget = (uint32_t)p.pf_bytes;
+    budget -= prefetch_range(p.w + (size_t)t.w_off16 * 16 + (size_t)skip * rb, (uint32_t)(t.nrows - skip) * rb, budget);
+    if (t.op == OP_FFN && budget)
+        prefetch_range(p.w + p.layer_bytes * t.layer + p.l_down + (size_t)(t.row0 / (2 * FFN_BLOCK)) * p.d * 16,
+                       (uint32_t)(t.nrows / (2 * FFN_BLOCK)) * (uint32_t)p.d * 16u, budget);
 }
 
 // Consumer wait on a counter: thread 0 spins, the rest learn the outcome at
@@ -287,9 +320,82 @@ __device__ __forceinline__ int signal_warp(const TaskRec& t, bool gemv) {
 __device__ __forceinline__ unsigned long long key_tag(uint32_t epoch) {
     return (unsigned long long)(epoch + 1u);
 }
+// Order-preserving map of an fp32 value to u32.  -0 is first made +0, so the
+// two zeros are equal keys and a tie between them goes to the lower index,
+// as with a plain comparison of the values.
 __device__ __forceinline__ uint32_t float_order(float f) {
     uint32_t u = __float_as_uint(f);
+    if (u == 0x80000000u) u = 0u;
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// ------------------------------------------------------------------ sampling
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy
+// as 1, 2, 3", SC 2011): ten rounds, each of two 32 x 32 -> 64-bit products
+// whose halves are mixed with the other two words and the key; the key is
+// bumped by two Weyl constants between rounds.  Counter (c0, c1, 0, 0); the
+// first output word is returned.
+__device__ __forceinline__ uint32_t philox_x0(uint32_t c0, uint32_t c1, uint32_t k0, uint32_t k1) {
+    uint32_t c2 = 0u, c3 = 0u;
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        if (r) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        const uint32_t hi0 = __umulhi(0xD2511F53u, c0), lo0 = 0xD2511F53u * c0;
+        const uint32_t hi1 = __umulhi(0xCD9E8D57u, c2), lo1 = 0xCD9E8D57u * c2;
+        const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+        c0 = n0;
+        c1 = lo1;
+        c2 = n2;
+        c3 = lo0;
+    }
+    return c0;
+}
+// Gumbel-max score of token i fed at position pos: logit / T - log(-log(u)),
+// u = (2 (x >> 9) + 1) 2^-24 of the draw x for counter (i, pos); u is exact in
+// fp32 and lies in (0, 1).  Out of line: it sits in the LM-head epilogue of
+// the GEMV loop, which must keep its registers.
+static __device__ __noinline__ float sample_score(float logit, uint32_t i, uint32_t pos, float inv_temp,
+                                                  uint32_t k0, uint32_t k1) {
+    const uint32_t x = philox_x0(i, pos, k0, k1);
+    const float u = __uint2float_rn(2u * (x >> 9) + 1u) * 5.9604644775390625e-8f;
+    return fmaf(logit, inv_temp, -logf(-logf(u)));
+}
+// 56-bit selection key of (value, index): the larger value wins, then the
+// lower index.  Zero is below every key of a finite value.
+__device__ __forceinline__ unsigned long long sel_key(float v, uint32_t idx) {
+    return ((unsigned long long)float_order(v) << 24) | (unsigned long long)(0xFFFFFFu - idx);
+}
+__device__ __forceinline__ float sel_value(unsigned long long k) {
+    const uint32_t u = (uint32_t)(k >> 24);
+    return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
+}
+__device__ __forceinline__ uint32_t sel_index(unsigned long long k) { return 0xFFFFFFu - (uint32_t)(k & 0xFFFFFFu); }
+
+// The LM-head tasks' argmax of step s (once all of them have signalled).
+static __device__ __forceinline__ int key_token(const VmParams& p, int step) {
+    const unsigned long long k = __ldcg(p.key);
+    if ((k >> 49) != key_tag((uint32_t)(p.epoch0 + step))) {
+        raise_error(p, DEV_BAD_KEY, 0xFFFFFFFEu, (uint32_t)step);
+        return -1;
+    }
+    return (int)((1u << KEY_IDX_BITS) - 1u - (uint32_t)(k & ((1ull << KEY_IDX_BITS) - 1ull)));
+}
+
+// Token selected at step s - 1 (s >= 1), once that step's token is final:
+// written by its token-select task, else the LM-head tasks' argmax key.
+static __device__ __forceinline__ int selected_token(const VmParams& p, int step) {
+    if (p.tokw) {
+        const unsigned long long k = __ldcg(p.tokw);
+        if ((uint32_t)(k >> 32) != (uint32_t)(p.epoch0 + step)) {
+            raise_error(p, DEV_BAD_KEY, 0xFFFFFFFEu, (uint32_t)step);
+            return -1;
+        }
+        return (int)(uint32_t)k;
+    }
+    return key_token(p, step - 1);
 }
 
 // Token fed at step s.  Called by thread 0; broadcast through shared memory.
@@ -300,12 +406,8 @@ static __device__ __forceinline__ int step_token(const VmParams& p, int step) {
     } else if (step == 0) {
         tok = p.pending >= 0 ? p.pending : (int)__ldcg((const unsigned int*)p.status + 3);
     } else {
-        unsigned long long k = __ldcg(p.key);
-        if ((k >> 49) != key_tag((uint32_t)(p.epoch0 + step - 1))) {
-            raise_error(p, DEV_BAD_KEY, 0xFFFFFFFEu, (uint32_t)step);
-            return -1;
-        }
-        tok = (int)((1u << KEY_IDX_BITS) - 1u - (uint32_t)(k & ((1ull << KEY_IDX_BITS) - 1ull)));
+        tok = selected_token(p, step);
+        if (tok < 0) return -1;
     }
     if (tok < 0 || tok >= p.V) {
         raise_error(p, DEV_BAD_TOKEN, 0xFFFFFFFDu, (uint32_t)step);
@@ -372,7 +474,8 @@ static __device__ __forceinline__ void prologue_rmsnorm(Ctx& c, const float* x, 
 }
 
 // Merge the split-KV partials of every query head into the attention output:
-// o = sum_c e^(m_c - M) acc_c / sum_c e^(m_c - M) l_c, M = max_c m_c.
+// o = sum_c e^(m_c - M) l_c a_c / sum_c e^(m_c - M) l_c, M = max_c m_c, where
+// a_c is chunk c's output normalised by its own sum l_c.
 static __device__ __forceinline__ void prologue_attention(Ctx& c, int lq4) {
     const VmParams& p = *c.p;
     const int C = p.C;
@@ -404,12 +507,13 @@ static __device__ __forceinline__ void prologue_attention(Ctx& c, int lq4) {
                 const float Mn = fmaxf(M, mm[k]);
                 const float r = expf(M - Mn), w = expf(mm[k] - Mn);
                 M = Mn;
-                den = fmaf(den, r, w * ll[k]);
+                const float wl = w * ll[k];  // the chunk's weight: its partials are acc / l
+                den = fmaf(den, r, wl);
                 const uint32_t h4[4] = {a[k].x, a[k].y, a[k].z, a[k].w};
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    o[2 * i] = fmaf(o[2 * i], r, w * half_bits_to_f32(h4[i] & 0xFFFFu));
-                    o[2 * i + 1] = fmaf(o[2 * i + 1], r, w * half_bits_to_f32(h4[i] >> 16));
+                    o[2 * i] = fmaf(o[2 * i], r, wl * half_bits_to_f32(h4[i] & 0xFFFFu));
+                    o[2 * i + 1] = fmaf(o[2 * i + 1], r, wl * half_bits_to_f32(h4[i] >> 16));
                 }
             }
         }
@@ -450,11 +554,12 @@ static __device__ __forceinline__ void merge_task(Ctx& c, const TaskRec& t) {
                 const float Mn = fmaxf(M, mlv[k].x);
                 const float r = expf(M - Mn), w = expf(mlv[k].x - Mn);
                 M = Mn;
-                den = fmaf(den, r, w * mlv[k].y);
-                o.x = fmaf(o.x, r, w * half_bits_to_f32(a[k].x & 0xFFFFu));
-                o.y = fmaf(o.y, r, w * half_bits_to_f32(a[k].x >> 16));
-                o.z = fmaf(o.z, r, w * half_bits_to_f32(a[k].y & 0xFFFFu));
-                o.w = fmaf(o.w, r, w * half_bits_to_f32(a[k].y >> 16));
+                const float wl = w * mlv[k].y;  // the chunk's weight: its partials are acc / l
+                den = fmaf(den, r, wl);
+                o.x = fmaf(o.x, r, wl * half_bits_to_f32(a[k].x & 0xFFFFu));
+                o.y = fmaf(o.y, r, wl * half_bits_to_f32(a[k].x >> 16));
+                o.z = fmaf(o.z, r, wl * half_bits_to_f32(a[k].y & 0xFFFFu));
+                o.w = fmaf(o.w, r, wl * half_bits_to_f32(a[k].y >> 16));
             }
         }
         const float inv = 1.f / den;
@@ -866,6 +971,7 @@ __device__ bool gemv_run(Ctx& c, const TaskRec& t, int task_id, int step, float&
             from_global = true;
             break;
     }
+    if (p.trace && c.tid == 0) c.sh->t_ph[0] = gtimer();
     // the lane's fragment of the input vector: k of chunk L + S*j
     unsigned long long xr[NG * HP];
     {
@@ -974,8 +1080,12 @@ __device__ bool gemv_run(Ctx& c, const TaskRec& t, int task_id, int step, float&
         } else if (wig == 0 && writer && has_row) {
             if (op == OP_LM) {
                 if (p.logits) p.logits[(size_t)step * p.V + row_g] = tot;
-                if (tot > best_v) {  // rows ascend per lane: the first maximum is kept
-                    best_v = tot;
+                float v = tot;
+                if (p.top_k > 0) ffn_h(c)[rb + my_r] = tot;  // the CTA's top-k is taken after the loop
+                else if (p.inv_temp > 0.f)
+                    v = sample_score(tot, (uint32_t)row_g, (uint32_t)(p.pos0 + step), p.inv_temp, p.seed_lo, p.seed_hi);
+                if (v > best_v) {  // rows ascend per lane: the first maximum is kept
+                    best_v = v;
                     best_i = row_g;
                 }
             } else if (op == OP_QKV) {
@@ -988,6 +1098,7 @@ __device__ bool gemv_run(Ctx& c, const TaskRec& t, int task_id, int step, float&
             }
         }
     }
+    if (p.trace && c.tid == 0) c.sh->t_ph[1] = gtimer();
     if (defer) {  // finish the shared rows: sum the warps' partials, then the epilogue
         bar_consumers();
         for (int rr = c.tid; rr < nrows; rr += NT) {
@@ -1003,8 +1114,12 @@ __device__ bool gemv_run(Ctx& c, const TaskRec& t, int task_id, int step, float&
                 }
             } else if (op == OP_LM) {
                 if (p.logits) p.logits[(size_t)step * p.V + row_g] = tot;
-                if (tot > best_v) {  // rows ascend per thread: the first maximum is kept
-                    best_v = tot;
+                float v = tot;
+                if (p.top_k > 0) ffn_h(c)[rr] = tot;
+                else if (p.inv_temp > 0.f)
+                    v = sample_score(tot, (uint32_t)row_g, (uint32_t)(p.pos0 + step), p.inv_temp, p.seed_lo, p.seed_hi);
+                if (v > best_v) {  // rows ascend per thread: the first maximum is kept
+                    best_v = v;
                     best_i = row_g;
                 }
             } else if (op == OP_QKV) {
@@ -1066,8 +1181,10 @@ __device__ __forceinline__ void load_kv_row(const uint16_t* rowp, int lane, floa
 // w, w+8, ... of a tile for the scores (its K rows in registers) and stages
 // their V rows in shared memory; for P.V each thread owns fixed output
 // elements (head, dim).  The first tile's rows are requested before the
-// queries are rotated, so cache reads overlap the qkv reads.  Writes
-// (max, sum, unnormalised output) per query head.
+// queries are rotated, so cache reads overlap the qkv reads.  Writes, per
+// query head, the chunk's running max m, its sum l = sum e^(s - m), and its
+// output normalised by l (bounded by max|v|, so fp16 holds it at any chunk
+// length); a merge weights each chunk by e^(m - M) * l.
 template <int HD>
 static __device__ __forceinline__ bool attn_task(Ctx& c, const TaskRec& t, int task_id, int step) {
     const VmParams& p = *c.p;
@@ -1176,6 +1293,7 @@ static __device__ __forceinline__ bool attn_task(Ctx& c, const TaskRec& t, int t
         sh.l[c.tid] = 0.f;
     }
     if (!bar_consumers_and(ok)) return false;
+    if (p.trace && c.tid == 0) c.sh->t_ph[0] = gtimer();
     if (ch == C - 1) {
         for (int i = c.tid; i < HD; i += NT) {
             kbase[(size_t)pos * HD + i] = __bfloat16_as_ushort(__float2bfloat16_rn(at.kcur[i]));
@@ -1243,14 +1361,15 @@ static __device__ __forceinline__ bool attn_task(Ctx& c, const TaskRec& t, int t
         }
         bar_consumers();  // the next tile overwrites scores and V rows
     }
+    if (p.trace && c.tid == 0) c.sh->t_ph[1] = gtimer();
 #pragma unroll
     for (int e = 0; e < OPT; ++e) {
         const int oe = c.tid + NT * e, h = oe / HD, dd = oe % HD;
-        if (h < rep) {
+        if (h < rep) {  // stored normalised (acc / l), so its range is that of v
+            const float lh = sh.l[h];
+            const uint16_t v = __half_as_ushort(__float2half_rn(lh > 0.f ? acc[e] / lh : 0.f));
 #pragma unroll
-            for (int k = 0; k < PART_COPIES; ++k)
-                p.part_acc[(((size_t)k * p.Hq + g * rep + h) * C + ch) * HD + dd] =
-                    __half_as_ushort(__float2half_rn(acc[e]));
+            for (int k = 0; k < PART_COPIES; ++k) p.part_acc[(((size_t)k * p.Hq + g * rep + h) * C + ch) * HD + dd] = v;
         }
     }
     if (c.tid < rep) {
@@ -1262,22 +1381,209 @@ static __device__ __forceinline__ bool attn_task(Ctx& c, const TaskRec& t, int t
     return true;
 }
 
+// ------------------------------------------------------------------ top-k selection
+// The selection code runs once per step at most, so it is kept out of line
+// (the hot GEMV and attention code keeps the instruction cache); it gets the
+// block's handles by value instead of the context, which would then have to
+// live in local memory.
+struct Blk {
+    const VmParams* p;
+    Shared* sh;
+    float* xs;
+    int tid, lane, warp;
+};
+__device__ __forceinline__ Blk blk(const Ctx& c) { return Blk{c.p, c.sh, c.xs, c.tid, c.lane, c.warp}; }
+
+// Scratch of a block selection, in the input-vector region: the LM-head task
+// holds its input fragments in registers by then (its rows are in the merge
+// scratch), and the select task has no input vector.
+struct SelScratch {
+    uint32_t hist[256];
+    unsigned long long prefix;
+    uint32_t need;       // rank still to find inside the current prefix
+    uint32_t count;      // compaction cursor
+    unsigned long long best;
+};
+static_assert(sizeof(SelScratch) <= sizeof(AttnScratch), "selection scratch");
+static_assert(LM_MAX_ROWS * sizeof(float) <= sizeof(MergeScratch), "LM rows of a CTA");
+
+// The k-th largest of the n distinct 56-bit keys key(0..n-1) (1 <= k <= n),
+// by seven 8-bit radix passes from the top: each pass histograms the digit of
+// the keys that share the prefix found so far, and the bin holding rank k
+// extends the prefix.  Every consumer thread calls it; all get the result.
+template <typename KeyFn>
+__device__ __forceinline__ unsigned long long block_kth_largest(const Blk& b, int n, uint32_t k, KeyFn key) {
+    SelScratch& ss = *reinterpret_cast<SelScratch*>(b.xs);
+    if (b.tid == 0) {
+        ss.prefix = 0ull;
+        ss.need = k;
+    }
+    for (int shift = 48; shift >= 0; shift -= 8) {
+        for (int i = b.tid; i < 256; i += NT) ss.hist[i] = 0u;
+        bar_consumers();
+        const unsigned long long pre = ss.prefix;
+        for (int i = b.tid; i < n; i += NT) {
+            const unsigned long long kk = key(i);
+            if ((kk >> (shift + 8)) == (pre >> (shift + 8))) atomicAdd(&ss.hist[(kk >> shift) & 255u], 1u);
+        }
+        bar_consumers();
+        if (b.warp == 0) {  // lane l scans bins 255 - 8l .. 248 - 8l (descending order)
+            uint32_t cnt[8], tot = 0u;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                cnt[j] = ss.hist[255 - 8 * b.lane - j];
+                tot += cnt[j];
+            }
+            uint32_t before = tot;  // inclusive scan over lanes, then made exclusive
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, before, o);
+                if (b.lane >= o) before += v;
+            }
+            before -= tot;
+            const uint32_t need = ss.need;
+            if (before < need && need <= before + tot) {  // exactly one lane
+                uint32_t acc = before;
+                for (int j = 0; j < 8; ++j) {
+                    if (need <= acc + cnt[j]) {
+                        ss.prefix = pre | ((unsigned long long)(255 - 8 * b.lane - j) << shift);
+                        ss.need = need - acc;
+                        break;
+                    }
+                    acc += cnt[j];
+                }
+            }
+        }
+        bar_consumers();
+    }
+    return ss.prefix;
+}
+
+// After an LM-head task under top-k sampling: the CTA's k largest logits
+// (ties: lower index) become its candidates, as selection keys in
+// cand[blockIdx.x][0 .. MAX_TOP_K) (unused slots zero).
+static __device__ __noinline__ void lm_candidates(Blk b, int row0, int n) {
+    const VmParams& p = *b.p;
+    const float* v = reinterpret_cast<const float*>(&b.sh->mg);
+    auto key = [&](int i) { return sel_key(v[i], (uint32_t)(row0 + i)); };
+    const uint32_t k = (uint32_t)min(p.top_k, n);
+    const unsigned long long kth = block_kth_largest(b, n, k, key);
+    SelScratch& ss = *reinterpret_cast<SelScratch*>(b.xs);
+    unsigned long long* out = p.cand + (size_t)blockIdx.x * MAX_TOP_K;
+    if (b.tid == 0) ss.count = 0u;
+    for (int j = b.tid + (int)k; j < MAX_TOP_K; j += NT) out[j] = 0ull;
+    bar_consumers();
+    for (int i = b.tid; i < n; i += NT) {
+        const unsigned long long kk = key(i);
+        if (kk >= kth) out[atomicAdd(&ss.count, 1u)] = kk;
+    }
+}
+
+// OP_SELECT (token-select schedules): the step's token from every CTA's
+// candidates.  Greedy (T = 0) and full-vocabulary sampling take the LM-head
+// tasks' key; top-k sampling takes the global top k of the candidates (the
+// top k of the vocabulary, since each CTA sent its own top k) and samples it
+// by the largest Gumbel-max score.
+static __device__ __noinline__ void select_task(Blk b, int step) {
+    const VmParams& p = *b.p;
+    if (p.top_k == 0) {
+        if (b.tid == 0) {
+            const int id = key_token(p, step);
+            if (id >= 0) {
+                if (p.out_ids) p.out_ids[step] = id;
+                p.status[3] = (uint32_t)id;
+                p.status[4] = (uint32_t)(step + 1);
+                *p.tokw = (unsigned long long)(uint32_t)id | ((unsigned long long)(uint32_t)(p.epoch0 + step + 1) << 32);
+            }
+        }
+        return;
+    }
+    const int n = (int)gridDim.x * MAX_TOP_K;
+    const unsigned long long* cand = p.cand;
+    auto key = [&](int i) { return __ldcg(cand + i); };
+    const unsigned long long kth = block_kth_largest(b, n, (uint32_t)p.top_k, key);
+    SelScratch& ss = *reinterpret_cast<SelScratch*>(b.xs);
+    unsigned long long best = 0ull;
+    for (int i = b.tid; i < n; i += NT) {
+        const unsigned long long kk = __ldcg(cand + i);
+        if (kk == 0ull || kk < kth) continue;
+        const uint32_t idx = sel_index(kk);
+        const float z = sample_score(sel_value(kk), idx, (uint32_t)(p.pos0 + step), p.inv_temp, p.seed_lo, p.seed_hi);
+        const unsigned long long zk = sel_key(z, idx);
+        best = zk > best ? zk : best;
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+        best = other > best ? other : best;
+    }
+    if (b.tid == 0) ss.best = 0ull;
+    bar_consumers();
+    if (b.lane == 0) atomicMax(&ss.best, best);
+    bar_consumers();
+    if (b.tid == 0) {
+        const uint32_t id = sel_index(ss.best);
+        if (p.out_ids) p.out_ids[step] = (int32_t)id;
+        p.status[3] = id;
+        p.status[4] = (uint32_t)(step + 1);
+        *p.tokw = (unsigned long long)id | ((unsigned long long)(uint32_t)(p.epoch0 + step + 1) << 32);
+    }
+}
+
+// EOS: at the start of step s >= 1 every CTA waits until the previous step's
+// token is final (its counter), reads it, and stops when it is eos.  Every
+// CTA sees the same token at the same step boundary, so all stop together
+// and no task of the stopped step runs.  False also after an abort.
+static __device__ __noinline__ bool eos_continue(Blk b, int step) {
+    const VmParams& p = *b.p;
+    if (b.tid == 0) {
+        int go = b.sh->abort ? 0 : 1;
+        const uint32_t* ctr = p.counters + (size_t)p.ctr_tok * CTR_STRIDE;
+        const uint32_t target = (uint32_t)p.n_tok * (uint32_t)(p.epoch0 + step);
+        const uint64_t t0 = gtimer();
+        for (uint32_t it = 1; go && (int32_t)(ld_acquire(ctr) - target) < 0; ++it) {
+            if ((it & 63u) == 0u) {
+                if (aborted(p)) go = 0;
+                else if (gtimer() - t0 > (uint64_t)p.watchdog_ns) {
+                    raise_error(p, DEV_TIMEOUT, 0xFFFFFFFCu, (uint32_t)step);
+                    go = 0;
+                }
+            }
+        }
+        if (go) {
+            const int tok = selected_token(p, step);  // the previous step's choice (forced or not)
+            go = tok >= 0 && tok != p.eos;
+        }
+        b.sh->flag = go;
+    }
+    bar_consumers();
+    return b.sh->flag != 0;
+}
+
 // ------------------------------------------------------------------ consumer
 template <int WT, int BASE, int HD>
 __device__ __forceinline__ void consumer(Ctx& c) {
     const VmParams& p = *c.p;
     for (int s = 0; s < p.n_steps && !c.abort; ++s) {
+        if (p.eos >= 0 && s > 0 && !p.skip_lm && !eos_continue(blk(c), s)) break;
         for (int qi = 0; qi < c.nrec && !c.abort; ++qi) {
             const TaskRec& t = c.tab[qi];
             const int tid_ = c.q0 + qi;  // queue index: identifies the task in errors and traces
+            c.cur = qi;
             const uint64_t t_start = p.trace ? gtimer() : 0;
+            if (p.trace && c.tid == 0) c.sh->t_ph[0] = c.sh->t_ph[1] = 0ull;
             float best_v = -3.0e38f;
             int best_i = 0;
             const bool gemv = t.op == OP_QKV || t.op == OP_O || t.op == OP_GU || t.op == OP_DOWN || t.op == OP_FFN ||
                               (t.op == OP_LM && !p.skip_lm);
             bool ok;
             if (gemv) {
+                if (p.pf_bytes && c.tid == 0) prefetch_task<WT>(p, t);
                 ok = gemv_task<WT, BASE>(c, t, tid_, s, best_v, best_i);
+                if (ok && t.op == OP_LM && p.top_k > 0) {
+                    bar_consumers();  // every row of the task is in shared memory
+                    lm_candidates(blk(c), t.row0, t.nrows);
+                }
                 if constexpr (WT == MK_W_BF16 || WT == MK_W_FP16) {
                     if (ok && t.op == OP_FFN) {
                         bar_consumers();  // every SwiGLU output of the task is in shared memory
@@ -1287,6 +1593,7 @@ __device__ __forceinline__ void consumer(Ctx& c) {
             } else {
                 ok = t.op == OP_ATTN ? attn_task<HD>(c, t, tid_, s) : wait_counters(c, t, tid_, s);
                 if (ok && t.op == OP_MERGE) merge_task(c, t);
+                if (ok && t.op == OP_SELECT && !p.skip_lm) select_task(blk(c), s);
                 if (ok && t.op == OP_FIN && c.tid == 0 && !p.skip_lm) {
                     const unsigned long long k = __ldcg(p.key);
                     if ((k >> 49) != key_tag((uint32_t)(p.epoch0 + s))) {
@@ -1295,6 +1602,7 @@ __device__ __forceinline__ void consumer(Ctx& c) {
                         const int id = (int)((1u << KEY_IDX_BITS) - 1u - (uint32_t)(k & ((1ull << KEY_IDX_BITS) - 1ull)));
                         if (p.out_ids) p.out_ids[s] = id;
                         p.status[3] = (uint32_t)id;
+                        p.status[4] = (uint32_t)(s + 1);
                     }
                 }
             }
@@ -1336,7 +1644,9 @@ __device__ __forceinline__ void consumer(Ctx& c) {
                     r[1] = t_start;
                     r[2] = c.sh->t_waited;
                     r[3] = gtimer();
-                    r[4] = r[5] = r[6] = r[7] = 0;
+                    r[4] = c.sh->t_ph[0];
+                    r[5] = c.sh->t_ph[1];
+                    r[6] = r[7] = 0;
                 }
             }
         }
@@ -1361,6 +1671,7 @@ __global__ void __launch_bounds__(THREADS, 1) vm_kernel(const VmParams p) {
     c.abort = false;
     c.deferred = 0;
     c.rs = 0;
+    c.cur = 0;
     c.q0 = p.queue_off[blockIdx.x];
     c.nrec = min(p.queue_off[blockIdx.x + 1] - c.q0, p.tab_cap);  // the host sizes tab_cap to the longest queue
     for (int i = threadIdx.x; i < c.nrec * (int)(sizeof(TaskRec) / 16); i += NT)

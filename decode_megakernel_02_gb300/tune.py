@@ -7,14 +7,19 @@ keep the fastest.  This is the deterministic core of that loop, with no agent:
 1. Every grid point goes through the static validator (`mk_validate_schedule`).
    A rejected schedule is recorded with its reason and never launched.
 2. Each accepted point decodes the same teacher-forced token stream. Its logits
-   must match those of the default configuration (the one the parity suite
-   checks against the CPU oracle): max|dlogit| <= 1e-2 * max|logit| per step,
-   with the same argmax on >= 99% of the steps.
+   must match the reference: max|dlogit| <= 1e-2 * max|logit| per step, with
+   the same argmax on >= 99% of the steps.  The reference is a file of
+   teacher-forced logits given with --reference (float32 [forced, vocab], the
+   logits of the last prompt token and of forced tokens 1.. of the stream
+   `forced_stream` builds; the parity tests write it from the CPU oracle), or,
+   without one, the default configuration's own logits.
 3. The points that pass are timed with CUDA events over full decode launches.
    The result is printed as JSON, fastest first.
 
-    python -m decode_megakernel_02_gb300.tune --workload llama-1b --chunks 2,3,4,6,8 --sms 0,144
+    python -m decode_megakernel_02_gb300.tune --workload llama-1b --chunks 2,3,4,6,8 --sms 0,144 \
+        --prefetch-kb=-1,256,1024
 """
+import itertools
 import argparse
 import json
 import os
@@ -67,6 +72,12 @@ def run_point(desc, blob, cfg, prompt, forced, n_time, reps):
         dec.close()
 
 
+def forced_stream(w, n):
+    """Teacher-forced inputs: the last prompt token, then n - 1 seeded random tokens."""
+    prompt = synthetic.generate_prompt(w)
+    return prompt, np.concatenate([prompt[-1:], synthetic.gen.random_tokens(w, n - 1, 7)]).astype(np.int32)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--workload", default="llama-1b")
@@ -75,6 +86,8 @@ def main(argv=None):
     ap.add_argument("--forced", type=int, default=8, help="teacher-forced steps of the agreement check")
     ap.add_argument("--tokens", type=int, default=0, help="tokens per timed launch (default: the workload's)")
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--prefetch-kb", default="0", help="L2 prefetch KB per CTA per task (0: default, -1: off)")
+    ap.add_argument("--reference", default=None, help=".npy teacher-forced reference logits [forced, vocab]")
     args = ap.parse_args(argv)
 
     from decode_megakernel_02_gb300 import build
@@ -84,32 +97,37 @@ def main(argv=None):
     desc = mk.make_desc(w)
     blob = mk.pack_model(desc, weights)
     del weights
-    prompt = synthetic.generate_prompt(w)
-    forced = np.concatenate([prompt[-1:], synthetic.gen.random_tokens(w, args.forced - 1, 7)]).astype(np.int32)
+    prompt, forced = forced_stream(w, args.forced)
     n_time = args.tokens or w.decode_steps
 
-    ref, _, _ = run_point(desc, blob, mk.make_config(), prompt, forced, 1, 1)
+    if args.reference:
+        ref, ref_kind = np.load(args.reference), "reference file"
+        if ref.shape != (args.forced, w.vocab):
+            raise SystemExit(f"--reference holds {ref.shape}, expected {(args.forced, w.vocab)}")
+    else:
+        ref, ref_kind = run_point(desc, blob, mk.make_config(), prompt, forced, 1, 1)[0], "default configuration"
+    ints = (lambda v: [int(x) for x in v.split(",")])
     rows = []
-    for sms in [int(x) for x in args.sms.split(",")]:
-        for ch in [int(x) for x in args.chunks.split(",")]:
-            cfg = mk.make_config(sms=sms, attn_chunks=ch)
-            point = {"sms": sms, "attn_chunks": ch}
-            st, why = mk.mk_validate_schedule(desc, cfg, sms or 152)
-            if st != mk.MK_OK:
-                rows.append(dict(point, status="rejected by the validator", why=why))
-                continue
-            try:
-                lg, ms, info = run_point(desc, blob, cfg, prompt, forced, n_time, args.reps)
-            except mk.MKError as e:
-                rows.append(dict(point, status="error", why=str(e)))
-                continue
-            if not agrees(lg, ref):
-                rows.append(dict(point, status="rejected: logits differ from the default configuration"))
-                continue
-            rows.append(dict(point, status="ok", tokens_per_s=n_time / (ms / 1000.0), ms_per_launch=ms,
-                             ctas=info["ctas"], n_tasks=info["n_tasks"]))
+    for sms, ch, kb in itertools.product(ints(args.sms), ints(args.chunks), ints(args.prefetch_kb)):
+        cfg = mk.make_config(sms=sms, attn_chunks=ch, l2_prefetch_kb=kb)
+        point = {"sms": sms, "attn_chunks": ch, "l2_prefetch_kb": kb}
+        st, why = mk.mk_validate_schedule(desc, cfg, sms or 152)
+        if st != mk.MK_OK:
+            rows.append(dict(point, status="rejected by the validator", why=why))
+            continue
+        try:
+            lg, ms, info = run_point(desc, blob, cfg, prompt, forced, n_time, args.reps)
+        except mk.MKError as e:
+            rows.append(dict(point, status="error", why=str(e)))
+            continue
+        if not agrees(lg, ref):
+            rows.append(dict(point, status=f"rejected: logits differ from the {ref_kind}"))
+            continue
+        rows.append(dict(point, status="ok", tokens_per_s=n_time / (ms / 1000.0), ms_per_launch=ms,
+                         ctas=info["ctas"], n_tasks=info["n_tasks"]))
     rows.sort(key=lambda r: -r.get("tokens_per_s", 0.0))
-    print(json.dumps({"workload": w.name, "tokens_per_launch": n_time, "points": rows}, indent=1))
+    print(json.dumps({"workload": w.name, "tokens_per_launch": n_time, "agreement_reference": ref_kind,
+                      "points": rows}, indent=1))
 
 
 if __name__ == "__main__":

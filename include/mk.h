@@ -92,6 +92,12 @@ typedef struct {
                                value built)                                               */
     int32_t attn_chunks;    /* split-KV chunks per KV head; default from max_seq and sms     */
     int32_t watchdog_ms;    /* a device wait gives up after this long; default 1000          */
+    int32_t l2_prefetch_kb; /* KB of a GEMV task's weights (past what the warps' rings load
+                               first) each CTA asks L2 to prefetch just before the task's
+                               wait; 0 default (1024), < 0 off                              */
+    int32_t token_select;   /* 1: one more task per step selects the token after the LM
+                               head (needed for top-k sampling); 0 (default): the LM-head
+                               tasks' block argmax is the selection                       */
 } mk_schedule_config;
 
 /* ------------------------------------------------------------------ packing
@@ -281,6 +287,43 @@ mk_status mk_set_state(mk_handle* h, int32_t pos, int32_t pending);
 mk_status mk_get_launch_info(const mk_handle* h, int32_t* ctas, int32_t* threads,
                              int32_t* smem_bytes, int32_t* rows_in_flight, int32_t* n_tasks);
 
+/* Token selection of later mk_decode / mk_decode_async launches (Kog monokernel
+ * tutorial, "How the monokernel removes launch overhead": sampling and the
+ * end-of-sequence check stay inside the one resident kernel).
+ *   temperature: 0 selects greedy argmax (lowest index on ties, the default).
+ *     T > 0 draws token i with probability proportional to exp(logit_i / T)
+ *     over the candidate set, by the Gumbel-max rule: the candidate with the
+ *     largest logit_i / T - log(-log(u_i)) (lowest index on ties), computed in
+ *     fp32 inside the LM-head task.
+ *   top_k: 0 = every token is a candidate; 1..MK_MAX_TOP_K = the k largest
+ *     logits (lower index first among equal logits); needs a handle created
+ *     with mk_schedule_config.token_select = 1, else MK_ERR_UNSUPPORTED.
+ *   seed: u_i comes from Philox4x32-10 (Salmon et al., SC 2011) with key
+ *     (seed low 32 bits, seed high 32 bits) and counter (i, pos, 0, 0), pos
+ *     the absolute position of the token being fed; first output word x,
+ *     u = (2 * (x >> 9) + 1) * 2^-24.  Draws depend only on (seed, pos, i), so
+ *     a decode split over several calls draws as one call does.
+ *   eos_id: -1 = none.  Otherwise a launch stops after the step that selects
+ *     eos_id: that id is emitted, later steps do not run (no KV writes), and
+ *     pos advances by the steps run.  mk_decode fills the rest of
+ *     out_ids_host with -1.  After mk_decode_async, call mk_finish before the
+ *     next launch (it reads how many steps ran; a launch before it returns
+ *     MK_ERR_INVALID_ARG).
+ * Errors: INVALID_ARG (NULL, T < 0 or not finite, top_k out of range, eos_id
+ * out of range), UNSUPPORTED (top_k on a handle without token_select). */
+#define MK_MAX_TOP_K 64
+typedef struct {
+    float temperature;
+    int32_t top_k;
+    uint64_t seed;
+    int32_t eos_id;
+} mk_sampling;
+mk_status mk_set_sampling(mk_handle* h, const mk_sampling* s);
+
+/* Steps the last launch ran (n_steps, or fewer after an EOS stop); valid after
+ * mk_decode or mk_finish. */
+int32_t mk_last_steps(const mk_handle* h);
+
 /* Kernel launches issued by this handle so far (one per prefill/decode call). */
 int64_t mk_launch_count(const mk_handle* h);
 
@@ -334,7 +377,9 @@ mk_status mk_debug_dequant(const mk_model_desc* desc, const void* weights_dev, i
 
 /* Record %globaltimer stamps of every task of later launches into trace_dev,
  * uint64 [ctas][records_per_cta][8] = {queue index | step << 32, task start,
- * wait done, after signal, 0, 0, 0, 0}.  The queue index is the task's
+ * wait done, after signal, input ready, compute done, 0, 0}: "input ready" is
+ * the end of a GEMV task's prologue or the arrival of an attention task's
+ * q/k/v, "compute done" the end of its row batches or tiles (0 for others).  The queue index is the task's
  * position in the concatenated per-CTA queues (mk_ir.queue holds the task id
  * at each index).  Record k of a CTA is step * queue_len + queue slot, and
  * records past the capacity are dropped.  NULL disables tracing.  The buffer

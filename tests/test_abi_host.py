@@ -30,7 +30,7 @@ def mk():
 def declared_functions():
     text = open(os.path.join(ROOT, "include", "mk.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:mk_status|int64_t|const char\s*\*|void)\s*\*?\s*(mk_\w+)\s*\(",
+    return sorted(set(re.findall(r"^\s*(?:mk_status|int64_t|int32_t|const char\s*\*|void)\s*\*?\s*(mk_\w+)\s*\(",
                                  text, flags=re.M)))
 
 
@@ -119,6 +119,25 @@ def test_validator_accepts_real_lowerings(mk, name, sms, chunks):
     assert st == mk.MK_OK, why
 
 
+@pytest.mark.parametrize("name,sms", [("tiny", 152), ("tiny", 3), ("llama-1b", 152), ("llama3-8b-8k", 152)])
+def test_validator_accepts_token_select_lowerings(mk, name, sms):
+    """The token-select schedule (an OP_SELECT task after the LM head, the next
+    step's first layer waiting on its counter) passes the validator."""
+    w = synthetic.get_workload(name)
+    cfg = mk.make_config(sms=sms, token_select=1)
+    st, why = mk.mk_validate_schedule(mk.make_desc(w), cfg, sms)
+    assert st == mk.MK_OK, why
+    ir = mk.mk_build_ir(mk.make_desc(w), cfg, sms)
+    assert [mk.OPS[t["op"]] for t in ir["tasks"]].count("select") == 1
+
+
+def test_header_constants_match_the_binding(mk):
+    text = open(os.path.join(ROOT, "include", "mk.h")).read()
+    m = re.search(r"#define MK_STATIC_SCRATCH_BYTES \((\d+)u << (\d+)\)", text)
+    assert m and int(m.group(1)) << int(m.group(2)) == mk.MK_STATIC_SCRATCH_BYTES
+    assert int(re.search(r"#define MK_MAX_TOP_K (\d+)", text).group(1)) == mk.MK_MAX_TOP_K
+
+
 def _small_ir(mk, sms, chunks, wdtype=None):
     w = synthetic.get_workload("tiny").with_(n_layers=1)
     if wdtype:
@@ -170,21 +189,111 @@ def _mutants(ir, rng, n):
     return out
 
 
-@pytest.mark.parametrize("sms,chunks,wd", [(2, 1, None), (3, 2, None), (2, 1, "int8"), (2, 64, None)])
-def test_validator_never_accepts_what_the_simulator_rejects(mk, sms, chunks, wd):
+def _delete_task(m, j):
+    """Remove task j from the schedule and renumber the later ones."""
+    m["tasks"].pop(j)
+    m["queues"] = [[i - (i > j) for i in q if i != j] for q in m["queues"]]
+
+
+def _more_mutants(ir, rng, n):
+    """The kinds of _mutants plus edits of what tasks touch: a dropped access, a
+    shrunken or shifted byte range, a deleted task, an access moved to another
+    buffer, and a hole in the coverage of a tagged buffer."""
+    import copy
+    out = []
+    base = _mutants(ir, rng, n // 2)
+    out.extend(base)
+    T = len(ir["tasks"])
+    tagged_bufs = set(ir.get("tagged", {}).values())
+    for _ in range(n - len(base)):
+        m = copy.deepcopy(ir)
+        kind = rng.randrange(5)
+        j = rng.randrange(T)
+        t = m["tasks"][j]
+        if kind == 0 and t["acc"]:
+            t["acc"].pop(rng.randrange(len(t["acc"])))
+        elif kind == 1 and t["acc"]:
+            i = rng.randrange(len(t["acc"]))
+            b, k, lo, hi, st, gr = t["acc"][i]
+            d = rng.choice([4, 8, 16, 64, max(4, (hi - lo) // 2)])
+            how = rng.randrange(3)
+            if how == 0:
+                lo = min(hi, lo + d)          # shrink from below
+            elif how == 1:
+                hi = max(lo, hi - d)          # shrink from above
+            else:
+                lo, hi = lo + d, hi + d       # shift
+            t["acc"][i] = (b, k, lo, hi, st, gr)
+        elif kind == 2:
+            _delete_task(m, j)
+        elif kind == 3 and t["acc"]:
+            i = rng.randrange(len(t["acc"]))
+            b, k, lo, hi, st, gr = t["acc"][i]
+            t["acc"][i] = (rng.choice([x for x in range(m["n_buffers"]) if x != b]), k, lo, hi, st, gr)
+        elif kind == 4 and tagged_bufs:
+            writers = [(jj, i) for jj, tt in enumerate(m["tasks"]) for i, x in enumerate(tt["acc"])
+                       if x[0] in tagged_bufs and x[1] != S.READ]
+            jj, i = rng.choice(writers)
+            b, k, lo, hi, st, gr = m["tasks"][jj]["acc"][i]
+            d = rng.choice([8, 16, max(8, (hi - lo) // 2)])
+            m["tasks"][jj]["acc"][i] = (b, k, lo, max(lo, hi - d), st, gr) if rng.randrange(2) else \
+                (b, k, min(hi, lo + d), hi, st, gr)
+        out.append(m)
+    return out
+
+
+# (sms, chunks, weight type, layers, mutants): 1- and 2-layer tiny schedules,
+# all with tagged q/k/v counters; about 5,400 mutants in all
+CORPUS = [(2, 1, None, 1, 1500), (3, 2, None, 1, 1500), (2, 1, "int8", 1, 800), (3, 2, None, 2, 1000),
+          (2, 2, "int4", 2, 600)]
+
+
+def test_validator_mutation_corpus(mk):
+    """AutoMegaKernel explainer ("Main contributions"): the validator rejects
+    every unsafe schedule of an adversarial corpus (no false accept) and
+    accepts every real lowering.  Ground truth is the brute-force simulator."""
+    totals = dict(mutants=0, unsafe=0, rejected=0, false_accepts=0, safe_rejected=0)
+    examples = []
+    for sms, chunks, wd, layers, n in CORPUS:
+        w = synthetic.get_workload("tiny").with_(n_layers=layers)
+        if wd:
+            w = w.with_(wdtype=wd)
+        ir = mk.mk_build_ir(mk.make_desc(w, max_seq=16), mk.make_config(sms=sms, attn_chunks=chunks), sms)
+        assert ir["tagged"], "the corpus starts from schedules with tagged counters"
+        assert S.verdict(ir)[0] and mk.mk_validate_ir(ir)[0] == mk.MK_OK
+        rng = random.Random(7919 * sms + 31 * chunks + layers)
+        for m in _more_mutants(ir, rng, n):
+            safe, why = S.verdict(m)
+            st, vwhy = mk.mk_validate_ir(m)
+            totals["mutants"] += 1
+            totals["unsafe"] += not safe
+            totals["rejected"] += st != mk.MK_OK
+            if st == mk.MK_OK and not safe:
+                totals["false_accepts"] += 1
+                examples.append(why)
+            totals["safe_rejected"] += safe and st != mk.MK_OK
+    print("validator corpus:", totals)
+    assert totals["mutants"] >= 5000
+    assert totals["false_accepts"] == 0, examples[:3]
+    assert totals["unsafe"] >= 1000  # the corpus is adversarial
+
+
+@pytest.mark.parametrize("sms,chunks,wd,n", [(2, 1, None, 60), (3, 2, None, 60), (2, 1, "int8", 60),
+                                             (2, 64, None, 12)])
+def test_validator_never_accepts_what_the_simulator_rejects(mk, sms, chunks, wd, n):
     ir = _small_ir(mk, sms, chunks, wd)
     assert S.verdict(ir)[0], S.verdict(ir)[1]
     assert mk.mk_validate_ir(ir)[0] == mk.MK_OK
     rng = random.Random(1000 * sms + chunks)
     false_accepts, rejected = [], 0
-    for m in _mutants(ir, rng, 60):
+    for m in _mutants(ir, rng, n):
         safe, why = S.verdict(m)
         st, vwhy = mk.mk_validate_ir(m)
         if st == mk.MK_OK and not safe:
             false_accepts.append(why)
         rejected += st != mk.MK_OK
     assert not false_accepts, false_accepts[:3]
-    assert rejected > 10  # the corpus does exercise the validator
+    assert rejected > n // 6  # the corpus does exercise the validator
 
 
 def test_tuner_agreement_rule():
