@@ -219,7 +219,6 @@ def main():
     ap.add_argument("--rows-in-flight", type=int, default=0)
     ap.add_argument("--chunks", type=int, default=0)
     ap.add_argument("--tokens", type=int, default=0, help="decode tokens per step (default: the workload's)")
-    ap.add_argument("--l2-prefetch-kb", type=int, default=0, help="0: default, -1: off")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -267,8 +266,7 @@ def main():
     weights = synthetic.generate_weights(w)
     desc = mk.make_desc(w)
     blob = mk.pack_model(desc, weights)
-    cfg = mk.make_config(sms=args.sms, rows_in_flight=args.rows_in_flight, attn_chunks=args.chunks,
-                         l2_prefetch_kb=args.l2_prefetch_kb)
+    cfg = mk.make_config(sms=args.sms, rows_in_flight=args.rows_in_flight, attn_chunks=args.chunks)
     dec = mk.Decoder(desc, blob, cfg)
     del blob
     prompt = synthetic.generate_prompt(w)

@@ -43,8 +43,8 @@ class mk_model_desc(ctypes.Structure):
 
 class mk_schedule_config(ctypes.Structure):
     _fields_ = [("sms", ctypes.c_int32), ("rows_in_flight", ctypes.c_int32), ("attn_chunks", ctypes.c_int32),
-                ("watchdog_ms", ctypes.c_int32), ("l2_prefetch_kb", ctypes.c_int32),
-                ("token_select", ctypes.c_int32)]
+                ("watchdog_ms", ctypes.c_int32), ("token_select", ctypes.c_int32),
+                ("prefill_chunk", ctypes.c_int32)]
 
 
 class mk_sampling(ctypes.Structure):
@@ -156,8 +156,8 @@ def make_desc(workload, max_seq=None, wdtype=None, flags=0):
                          workload.rope_theta, max_seq or workload.max_seq, wd, base, flags)
 
 
-def make_config(sms=0, rows_in_flight=0, attn_chunks=0, watchdog_ms=0, l2_prefetch_kb=0, token_select=0):
-    return mk_schedule_config(sms, rows_in_flight, attn_chunks, watchdog_ms, l2_prefetch_kb, token_select)
+def make_config(sms=0, rows_in_flight=0, attn_chunks=0, watchdog_ms=0, token_select=0, prefill_chunk=0):
+    return mk_schedule_config(sms, rows_in_flight, attn_chunks, watchdog_ms, token_select, prefill_chunk)
 
 
 # ------------------------------------------------------------------ host calls

@@ -17,13 +17,13 @@ NVCC = os.path.join(CUDA_HOME, "bin", "nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 CU_SRCS = ["mk_vm_bf16.cu", "mk_vm_fp16.cu", "mk_vm_int8.cu", "mk_vm_int4.cu", "mk_vm_common.cu", "mk_runtime.cu",
-           "mk_static.cu"]
+           "mk_static.cu", "mk_prefill.cu"]
 CPP_SRCS = ["mk_host.cpp", "mk_schedule.cpp", "mk_validate.cpp"]
 
 
 def _sources():
     return [os.path.join(CSRC, f) for f in CU_SRCS + CPP_SRCS] + [
-        os.path.join(CSRC, f) for f in ("mk_internal.h", "mk_host.h", "mk_vm.cuh")] + [os.path.join(INCLUDE, "mk.h")]
+        os.path.join(CSRC, f) for f in ("mk_internal.h", "mk_host.h", "mk_vm.cuh", "mk_prefill.h")] + [os.path.join(INCLUDE, "mk.h")]
 
 
 def up_to_date():

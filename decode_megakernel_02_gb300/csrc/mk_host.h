@@ -24,8 +24,8 @@ BlobLayout blob_layout(const mk_model_desc* d);
 struct Config {
     int sms, rw, C;
     int64_t watchdog_ns;
-    int pf_bytes;             // L2 prefetch of each GEMV task's weights per CTA (0: off)
     bool token_select;        // an OP_SELECT task after the LM head selects each step's token
+    int pf_chunk;             // tensor-core prefill chunk (tokens; 0: prefill by the decode kernel)
 };
 mk_status resolve_config(const mk_model_desc* d, const mk_schedule_config* cfg, int n_sms,
                          Config* out);
@@ -69,7 +69,11 @@ mk_status validate_ir(const mk_ir* ir, std::string* why);
 // Workspace layout (byte offsets).
 struct WsLayout {
     int64_t status, counters, key, tokw, cand, recs, queue_off, inv_freq, x, qkv, part_ml, part_acc, att,
-        h, tok, out_ids, total;
+        h, tok, out_ids;
+    // tensor-core prefill (pf_chunk > 0): residual, q, and the hi / lo halves of
+    // the GEMM inputs (normed x, attention output, SwiGLU output)
+    int64_t pf_x, pf_q, pf_h, pf_hl, pf_ao, pf_aol, pf_gu, pf_gul, pf_err;
+    int64_t total;
 };
 WsLayout ws_layout(const mk_model_desc* d, const Config& c, int64_t n_tasks, int32_t n_counters);
 

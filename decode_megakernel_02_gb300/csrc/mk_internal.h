@@ -138,7 +138,6 @@ struct VmParams {
     int32_t xs_floats;         // shared-memory input vector capacity: max(d, q_dim)
     int32_t tab_cap;           // task records a CTA's shared-memory table holds (longest queue)
     int64_t watchdog_ns;
-    int32_t pf_bytes;          // L2 prefetch of a GEMV task's weights past the rings' lookahead, per CTA (0: off)
     // token selection
     float inv_temp;            // 1 / temperature (0: greedy argmax)
     int32_t top_k;             // > 0: candidates are the top_k logits (token-select task)

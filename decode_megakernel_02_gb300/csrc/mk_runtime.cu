@@ -17,9 +17,10 @@
 #include <vector>
 
 #include "mk_host.h"
+#include "mk_prefill.h"
 
 namespace mk {
-const void* vm_kernel_for(int wdtype, int base, int hd);
+const void* vm_kernel_for(int wdtype, int base, int hd, bool sel);
 size_t vm_shared_bytes(int wdtype, int xs_floats, int tab_cap);
 cudaError_t launch_dequant(int wdtype, const uint8_t* rows, int64_t stride, int first, int step, int nrows,
                            int K, float* out, cudaStream_t st);
@@ -40,7 +41,8 @@ struct mk_handle {
     uint8_t* wsp = nullptr;
     cudaStream_t st = nullptr;
     int device = 0;
-    const void* kfn = nullptr;
+    const void* kfn = nullptr;      // greedy instance
+    const void* kfn_sel = nullptr;  // token-selection instance (sampling, EOS, token-select task)
     size_t smem = 0;
     int32_t pos = 0, pending = -1;
     bool has_seq = false;
@@ -63,8 +65,14 @@ struct mk_handle {
     int32_t launched = 0;                // steps of the last launch
     int32_t last_steps = 0;              // steps it ran (fewer after an EOS stop)
     bool unsettled = false;              // an async launch with EOS whose step count is not read yet
+    // tensor-core prefill: weight maps per layer (QKV, O, gate/up, down) and the
+    // chunk activations' maps (normed x, attention output, SwiGLU output)
+    std::vector<CUtensorMap> pf_w;
+    CUtensorMap pf_a[6]{};               // normed x, attention output, SwiGLU output: hi, lo each
     std::string err;
 };
+
+static mk_status prefill_maps(mk_handle* h);
 
 namespace {
 
@@ -170,7 +178,6 @@ mk_status launch(mk_handle* h, int n_steps, const int32_t* forced, int32_t* out_
     p.xs_floats = h->xs_floats;
     p.tab_cap = h->tab_cap;
     p.watchdog_ns = h->c.watchdog_ns;
-    p.pf_bytes = h->c.pf_bytes;
     const bool sampling = h->temperature > 0.f && !skip_lm;
     p.inv_temp = sampling ? 1.f / h->temperature : 0.f;
     p.top_k = sampling ? h->top_k : 0;
@@ -184,7 +191,8 @@ mk_status launch(mk_handle* h, int n_steps, const int32_t* forced, int32_t* out_
     p.trace = h->trace;
     p.trace_cap = h->trace_cap;
     void* args[] = {&p};
-    CK(h, cudaLaunchCooperativeKernel(h->kfn, dim3(h->c.sms), dim3(THREADS), args, h->smem, h->st));
+    const bool sel = p.inv_temp > 0.f || p.eos >= 0 || p.tokw != nullptr;
+    CK(h, cudaLaunchCooperativeKernel(sel ? h->kfn_sel : h->kfn, dim3(h->c.sms), dim3(THREADS), args, h->smem, h->st));
     h->epoch += (uint32_t)n_steps;
     h->launches++;
     h->launched = n_steps;
@@ -320,7 +328,8 @@ mk_status mk_create(const mk_model_desc* desc, const mk_schedule_config* cfg, co
     h->wsp = (uint8_t*)workspace_dev;
     h->st = (cudaStream_t)stream;
     h->device = dev;
-    h->kfn = vm_kernel_for(desc->wdtype, desc->base_dtype, desc->head_dim);
+    h->kfn = vm_kernel_for(desc->wdtype, desc->base_dtype, desc->head_dim, false);
+    h->kfn_sel = vm_kernel_for(desc->wdtype, desc->base_dtype, desc->head_dim, true);
     h->smem = vm_shared_bytes(desc->wdtype, xs_floats, tab_cap);
     h->xs_floats = xs_floats;
     h->tab_cap = tab_cap;
@@ -329,7 +338,7 @@ mk_status mk_create(const mk_model_desc* desc, const mk_schedule_config* cfg, co
     h->ctr_tok = lw.ctr_tok;
     h->n_tok = lw.n_tok;
     h->lm_rows_max = lw.lm_rows_max;
-    if (!h->kfn) {
+    if (!h->kfn || !h->kfn_sel) {
         delete h;
         set_error("no kernel for wdtype %d / base %d", desc->wdtype, desc->base_dtype);
         return MK_ERR_UNSUPPORTED;
@@ -343,13 +352,15 @@ mk_status mk_create(const mk_model_desc* desc, const mk_schedule_config* cfg, co
     // handles launch the same instantiation with their own (possibly larger)
     // shared memory, so it is raised to the device's opt-in limit instead of
     // this handle's need, and no handle can lower it under another.
-    e = raise_smem_limit(h->kfn, smem_optin);
-    if (e != cudaSuccess) return fail(cuda_fail(h, e, "cudaFuncSetAttribute"));
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, h->kfn, THREADS, h->smem);
-    if (e != cudaSuccess) return fail(cuda_fail(h, e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor"));
-    if (per_sm < 1 || (int64_t)per_sm * n_sms < c.sms)
-        return fail(herr(h, MK_ERR_UNSUPPORTED, "%d CTAs cannot be co-resident (%d per SM)", c.sms, per_sm));
+    for (const void* fn : {h->kfn, h->kfn_sel}) {
+        e = raise_smem_limit(fn, smem_optin);
+        if (e != cudaSuccess) return fail(cuda_fail(h, e, "cudaFuncSetAttribute"));
+        int per_sm = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, THREADS, h->smem);
+        if (e != cudaSuccess) return fail(cuda_fail(h, e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor"));
+        if (per_sm < 1 || (int64_t)per_sm * n_sms < c.sms)
+            return fail(herr(h, MK_ERR_UNSUPPORTED, "%d CTAs cannot be co-resident (%d per SM)", c.sms, per_sm));
+    }
 
     // device tables: task records, queue offsets, RoPE inverse frequencies
     std::vector<float> inv(desc->head_dim / 2);
@@ -360,11 +371,132 @@ mk_status mk_create(const mk_model_desc* desc, const mk_schedule_config* cfg, co
     if (e == cudaSuccess) e = cudaMemcpyAsync(h->wsp + ws.inv_freq, inv.data(), inv.size() * 4, cudaMemcpyHostToDevice, h->st);
     if (e != cudaSuccess) return fail(cuda_fail(h, e, "uploading the schedule"));
     if ((st = reset_sync_state(h))) return fail(st);
+    if (c.pf_chunk > 0 && (st = prefill_maps(h))) return fail(st);
     e = cudaStreamSynchronize(h->st);
     if (e != cudaSuccess) return fail(cuda_fail(h, e, "cudaStreamSynchronize"));
     *out = h;
     return MK_OK;
 }
+
+}  // extern "C"
+
+// Tensor maps of the tensor-core prefill (mk_create, prefill_chunk > 0).
+static mk_status prefill_maps(mk_handle* h) {
+    const mk_model_desc& d = h->d;
+    const BlobLayout& bl = h->bl;
+    const bool f16 = d.base_dtype == MK_W_FP16;
+    const int64_t qd = (int64_t)d.n_q_heads * d.head_dim, kd = (int64_t)d.n_kv_heads * d.head_dim;
+    if (d.wdtype != d.base_dtype || kd % 128 != 0)
+        return herr(h, MK_ERR_UNSUPPORTED, "tensor-core prefill needs 16-bit weights and n_kv_heads * head_dim %% 128 == 0");
+    if (!pf::tensor_map_encoder_ready())
+        return herr(h, MK_ERR_UNSUPPORTED, "the driver offers no tensor-map encoder");
+    const int64_t mc = h->c.pf_chunk;
+    bool ok = pf::make_map_rows(&h->pf_a[0], h->wsp + h->ws.pf_h, mc, d.d_model, d.d_model * 2, pf::BM, f16) &&
+              pf::make_map_rows(&h->pf_a[1], h->wsp + h->ws.pf_hl, mc, d.d_model, d.d_model * 2, pf::BM, f16) &&
+              pf::make_map_rows(&h->pf_a[2], h->wsp + h->ws.pf_ao, mc, qd, qd * 2, pf::BM, f16) &&
+              pf::make_map_rows(&h->pf_a[3], h->wsp + h->ws.pf_aol, mc, qd, qd * 2, pf::BM, f16) &&
+              pf::make_map_rows(&h->pf_a[4], h->wsp + h->ws.pf_gu, mc, d.d_ffn, (int64_t)d.d_ffn * 2, pf::BM, f16) &&
+              pf::make_map_rows(&h->pf_a[5], h->wsp + h->ws.pf_gul, mc, d.d_ffn, (int64_t)d.d_ffn * 2, pf::BM, f16);
+    h->pf_w.assign((size_t)d.n_layers * 4, CUtensorMap{});
+    for (int l = 0; l < d.n_layers && ok; ++l) {
+        const uint8_t* lb = h->w + bl.layer_bytes * l;
+        CUtensorMap* m = &h->pf_w[(size_t)l * 4];
+        ok = pf::make_map_rows(&m[0], lb + bl.l_qkv, qd + 2 * kd, d.d_model, bl.row_qkv, pf::BN, f16) &&
+             pf::make_map_rows(&m[1], lb + bl.l_o, d.d_model, qd, bl.row_o, pf::BN, f16) &&
+             pf::make_map_rows(&m[2], lb + bl.l_gu, 2 * (int64_t)d.d_ffn, d.d_model, bl.row_gu, pf::BN, f16) &&
+             (bl.down_cols ? pf::make_map_blocks(&m[3], lb + bl.l_down, d.d_model, d.d_ffn, pf::BN, f16)
+                           : pf::make_map_rows(&m[3], lb + bl.l_down, d.d_model, d.d_ffn, bl.row_down, pf::BN, f16));
+    }
+    if (!ok) return herr(h, MK_ERR_CUDA, "cuTensorMapEncodeTiled rejected a prefill tensor map");
+    return MK_OK;
+}
+
+// Positions 0 .. n-2 through the layers, pf_chunk tokens at a time (the
+// tokens are already in the workspace).  The last layer stops after its KV
+// append: nothing after it reaches the cache.
+static mk_status prefill_tensor_cores(mk_handle* h, int32_t n) {
+    const mk_model_desc& d = h->d;
+    const BlobLayout& bl = h->bl;
+    const bool f16 = d.base_dtype == MK_W_FP16;
+    const int qd = d.n_q_heads * d.head_dim, kd = d.n_kv_heads * d.head_dim;
+    float* x = (float*)(h->wsp + h->ws.pf_x);
+    uint16_t* hb = (uint16_t*)(h->wsp + h->ws.pf_h);
+    uint16_t* hbl = (uint16_t*)(h->wsp + h->ws.pf_hl);
+    float* q = (float*)(h->wsp + h->ws.pf_q);
+    uint16_t* ao = (uint16_t*)(h->wsp + h->ws.pf_ao);
+    uint16_t* aol = (uint16_t*)(h->wsp + h->ws.pf_aol);
+    uint16_t* gu = (uint16_t*)(h->wsp + h->ws.pf_gu);
+    uint16_t* gul = (uint16_t*)(h->wsp + h->ws.pf_gul);
+    uint32_t* err = (uint32_t*)(h->wsp + h->ws.pf_err);
+    const int32_t* tok = (const int32_t*)(h->wsp + h->ws.tok);
+    CK(h, cudaMemsetAsync(err, 0, 4, h->st));
+    for (int c0 = 0; c0 < n - 1; c0 += h->c.pf_chunk) {
+        const int mv = std::min(h->c.pf_chunk, n - 1 - c0), mr = (mv + pf::BM - 1) / pf::BM * pf::BM;
+        CK(h, pf::launch_embed((const uint16_t*)(h->w + bl.embed), tok + c0, mv, d.d_model, f16, x, h->st));
+        for (int l = 0; l < d.n_layers; ++l) {
+            const uint8_t* lb = h->w + bl.layer_bytes * l;
+            const CUtensorMap* m = &h->pf_w[(size_t)l * 4];
+            pf::GemmArgs g{};
+            g.M = mr;
+            g.m_valid = mv;
+            g.f16 = f16 ? 1 : 0;
+            g.err = err;
+            CK(h, pf::launch_rmsnorm(x, (const uint16_t*)(lb + bl.l_attn_norm), mv, d.d_model, d.rms_eps, f16, hb, hbl,
+                                     h->st));
+            pf::GemmArgs gq = g;
+            gq.N = qd + 2 * kd;
+            gq.K = d.d_model;
+            gq.epi = pf::EPI_QKV;
+            gq.out_f32 = q;
+            gq.ldo = qd;
+            gq.q_dim = qd;
+            gq.kv_dim = kd;
+            gq.hd = d.head_dim;
+            gq.max_seq = d.max_seq;
+            gq.pos0 = c0;
+            gq.layer = l;
+            gq.n_kv_heads = d.n_kv_heads;
+            gq.inv_freq = (const float*)(h->wsp + h->ws.inv_freq);
+            gq.kv = h->kv;
+            CK(h, pf::launch_gemm(h->pf_a[0], h->pf_a[1], m[0], gq, h->st));
+            if (l == d.n_layers - 1) break;
+            CK(h, pf::launch_attention(q, h->kv, l, c0, mv, d.n_q_heads, d.n_kv_heads, d.head_dim, d.max_seq, f16, ao,
+                                       aol, h->st));
+            pf::GemmArgs go = g;
+            go.N = d.d_model;
+            go.K = qd;
+            go.epi = pf::EPI_RESID;
+            go.out_f32 = x;
+            go.ldo = d.d_model;
+            CK(h, pf::launch_gemm(h->pf_a[2], h->pf_a[3], m[1], go, h->st));
+            CK(h, pf::launch_rmsnorm(x, (const uint16_t*)(lb + bl.l_ffn_norm), mv, d.d_model, d.rms_eps, f16, hb, hbl,
+                                     h->st));
+            pf::GemmArgs gg = g;
+            gg.N = 2 * d.d_ffn;
+            gg.K = d.d_model;
+            gg.epi = pf::EPI_SWIGLU;
+            gg.out16 = gu;
+            gg.out16_lo = gul;
+            gg.ld16 = d.d_ffn;
+            CK(h, pf::launch_gemm(h->pf_a[0], h->pf_a[1], m[2], gg, h->st));
+            pf::GemmArgs gd = g;
+            gd.N = d.d_model;
+            gd.K = d.d_ffn;
+            gd.epi = pf::EPI_RESID;
+            gd.out_f32 = x;
+            gd.ldo = d.d_model;
+            gd.b_blocks = bl.down_cols ? 1 : 0;
+            CK(h, pf::launch_gemm(h->pf_a[4], h->pf_a[5], m[3], gd, h->st));
+        }
+    }
+    uint32_t e = 0;
+    CK(h, cudaMemcpyAsync(&e, err, 4, cudaMemcpyDeviceToHost, h->st));
+    CK(h, cudaStreamSynchronize(h->st));
+    if (e) return herr(h, MK_ERR_TIMEOUT, "a prefill GEMM wait gave up (code %u)", e);
+    return MK_OK;
+}
+
+extern "C" {
 
 mk_status mk_prefill(mk_handle* h, const int32_t* tokens_host, int32_t n) {
     if (!h || !tokens_host) {
@@ -380,9 +512,13 @@ mk_status mk_prefill(mk_handle* h, const int32_t* tokens_host, int32_t n) {
     h->has_seq = false;
     if (n > 1) {
         CK(h, cudaMemcpyAsync(h->wsp + h->ws.tok, tokens_host, (size_t)(n - 1) * 4, cudaMemcpyHostToDevice, h->st));
-        mk_status st = launch(h, n - 1, (const int32_t*)(h->wsp + h->ws.tok), nullptr, nullptr, 1);
-        if (st) return st;
-        if ((st = read_status(h))) return st;
+        mk_status st;
+        if (h->c.pf_chunk > 0) {
+            if ((st = prefill_tensor_cores(h, n))) return st;
+        } else {
+            if ((st = launch(h, n - 1, (const int32_t*)(h->wsp + h->ws.tok), nullptr, nullptr, 1))) return st;
+            if ((st = read_status(h))) return st;
+        }
     }
     h->pos = n - 1;
     h->pending = tokens_host[n - 1];
@@ -530,7 +666,7 @@ struct StaticSlot {
     Config c{};
     WsLayout ws{};
     int32_t n_tasks = 0, n_counters = 0;
-    const void* kfn = nullptr;
+    const void* kfn = nullptr, *kfn_sel = nullptr;
     size_t smem = 0;
     int32_t xs_floats = 0, tab_cap = 0;
     int32_t ctr_tok = 0, n_tok = 0;
@@ -570,7 +706,7 @@ mk_status context_id(int dev, unsigned long long* id) {
 
 bool same_config(const Config& a, const Config& b) {
     return a.sms == b.sms && a.rw == b.rw && a.C == b.C && a.watchdog_ns == b.watchdog_ns &&
-           a.pf_bytes == b.pf_bytes && a.token_select == b.token_select;
+           a.token_select == b.token_select;
 }
 
 // Lower, validate and upload the schedule for (desc, c) into the slot's scratch.
@@ -602,8 +738,9 @@ mk_status static_setup(StaticSlot& s, const mk_model_desc* desc, const Config& c
     if ((st = device_tables(lw, c.sms, &recs, &queue, &qoff, &tab_cap))) return st;
     const int xs_floats = std::max(desc->d_model, desc->n_q_heads * desc->head_dim);
     const size_t smem = vm_shared_bytes(desc->wdtype, xs_floats, tab_cap);
-    const void* kfn = vm_kernel_for(desc->wdtype, desc->base_dtype, desc->head_dim);
-    if (!kfn) {
+    const void* kfn = vm_kernel_for(desc->wdtype, desc->base_dtype, desc->head_dim, false);
+    const void* kfn_sel = vm_kernel_for(desc->wdtype, desc->base_dtype, desc->head_dim, true);
+    if (!kfn || !kfn_sel) {
         set_error("no kernel for wdtype %d / base %d", desc->wdtype, desc->base_dtype);
         return MK_ERR_UNSUPPORTED;
     }
@@ -613,6 +750,7 @@ mk_status static_setup(StaticSlot& s, const mk_model_desc* desc, const Config& c
     }
     // the kernel-wide limit, as in mk_create (shared with every handle)
     cudaError_t e = raise_smem_limit(kfn, smem_optin);
+    if (e == cudaSuccess) e = raise_smem_limit(kfn_sel, smem_optin);
     int per_sm = 0;
     if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kfn, THREADS, smem);
     if (e != cudaSuccess) {
@@ -640,6 +778,7 @@ mk_status static_setup(StaticSlot& s, const mk_model_desc* desc, const Config& c
     s.n_tasks = (int32_t)lw.tasks.size();
     s.n_counters = lw.n_counters;
     s.kfn = kfn;
+    s.kfn_sel = kfn_sel;
     s.smem = smem;
     s.xs_floats = xs_floats;
     s.tab_cap = tab_cap;
@@ -708,6 +847,7 @@ mk_status mk_decode_static(const mk_model_desc* desc, const mk_schedule_config* 
     }
     Config c;
     if ((st = resolve_config(desc, cfg, n_sms, &c))) return st;
+    c.pf_chunk = 0;  // this entry point decodes only: no prefill buffers in the scratch
     const cudaStream_t cs = (cudaStream_t)stream;
     if (!s.ready || std::memcmp(&s.d, desc, sizeof s.d) != 0 || !same_config(s.c, c)) {
         if ((st = static_setup(s, desc, c, n_sms, smem_optin, cs))) return st;
@@ -737,6 +877,7 @@ mk_status mk_decode_static(const mk_model_desc* desc, const mk_schedule_config* 
     h.st = cs;
     h.device = dev;
     h.kfn = s.kfn;
+    h.kfn_sel = s.kfn_sel;
     h.smem = s.smem;
     h.xs_floats = s.xs_floats;
     h.tab_cap = s.tab_cap;

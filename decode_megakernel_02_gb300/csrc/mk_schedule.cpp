@@ -51,16 +51,16 @@ mk_status resolve_config(const mk_model_desc* d, const mk_schedule_config* cfg, 
         return MK_ERR_INVALID_ARG;
     }
     c.watchdog_ns = (int64_t)(cfg->watchdog_ms ? cfg->watchdog_ms : 1000) * 1000000;
-    if (cfg->l2_prefetch_kb > (1 << 20)) {
-        set_error("l2_prefetch_kb %d above 1 GiB", cfg->l2_prefetch_kb);
-        return MK_ERR_INVALID_ARG;
-    }
-    c.pf_bytes = cfg->l2_prefetch_kb < 0 ? 0 : (cfg->l2_prefetch_kb ? cfg->l2_prefetch_kb : 1024) * 1024;
     if (cfg->token_select != 0 && cfg->token_select != 1) {
         set_error("token_select %d: 0 or 1", cfg->token_select);
         return MK_ERR_INVALID_ARG;
     }
     c.token_select = cfg->token_select == 1;
+    if (cfg->prefill_chunk < 0 || cfg->prefill_chunk % 128 != 0 || cfg->prefill_chunk > 4096) {
+        set_error("prefill_chunk %d: 0 or a multiple of 128 up to 4096", cfg->prefill_chunk);
+        return MK_ERR_INVALID_ARG;
+    }
+    c.pf_chunk = cfg->prefill_chunk;
     *out = c;
     return MK_OK;
 }
@@ -554,6 +554,18 @@ WsLayout ws_layout(const mk_model_desc* d, const Config& c, int64_t n_tasks, int
     w.h = take((int64_t)d->d_ffn * 4);
     w.tok = take((int64_t)d->max_seq * 4 + 16);
     w.out_ids = take((int64_t)d->max_seq * 4 + 16);
+    if (c.pf_chunk > 0) {  // one chunk's activations
+        const int64_t mc = c.pf_chunk;
+        w.pf_x = take(mc * d->d_model * 4);
+        w.pf_q = take(mc * qd * 4);
+        w.pf_h = take(mc * d->d_model * 2);
+        w.pf_hl = take(mc * d->d_model * 2);
+        w.pf_ao = take(mc * qd * 2);
+        w.pf_aol = take(mc * qd * 2);
+        w.pf_gu = take(mc * d->d_ffn * 2);
+        w.pf_gul = take(mc * d->d_ffn * 2);
+        w.pf_err = take(16);
+    }
     w.total = o;
     return w;
 }

@@ -108,7 +108,8 @@ struct Shared {
     int32_t abort;                  // set when this CTA must stop
     int32_t tok;                    // broadcast of the step's input token
     unsigned long long t_waited;    // trace: when the current task's wait completed
-    unsigned long long t_ph[2];     // trace: input ready (prologue done / q,k,v arrived), compute done
+    unsigned long long t_ph[4];     // trace: input ready (prologue done / q,k,v arrived), compute done,
+                                    // task body done (before the signal), signal released
 };
 
 // Weights per 16-byte chunk of a packed row's codes.
@@ -175,37 +176,6 @@ static __device__ void raise_error(const VmParams& p, uint32_t code, uint32_t ta
         p.status[1] = task;
         p.status[2] = detail;
     }
-}
-
-// ------------------------------------------------------------------ L2 prefetch
-// The warps' rings keep NB - 1 batches of a few KB each in flight, which is
-// short of what HBM needs in flight to stream at full rate, and a task's first
-// ring copies go out only when the previous task frees its slots.  So just
-// before a GEMV task waits for its inputs, thread 0 asks L2 to prefetch the
-// task's weight bytes past the rings' lookahead (up to pf_bytes, in 32 KB bulk
-// requests); weight bytes never depend on activations.  The ring copies then
-// find them in L2.
-constexpr uint32_t PF_PIECE = 32768;
-
-__device__ __forceinline__ void prefetch_l2(const void* gptr, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gptr), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ uint32_t prefetch_range(const uint8_t* a, uint32_t n, uint32_t budget) {
-    n = min(n, budget);
-    for (uint32_t o = 0; o < n; o += PF_PIECE) prefetch_l2(a + o, min(PF_PIECE, n - o));
-    return n;
-}
-
-// Thread 0, before the task's wait.
-template <int WT>
-__device__ __forceinline__ void prefetch_task(const VmParams& p, const TaskRec& t) {
-    const uint32_t rb = (uint32_t)t.row_bytes16 * 16u;
-    const int skip = min(t.nrows, (ring_slots<WT>() - 1) * (NW / t.wpr) * RW);  // the rings' lookahead
-    uint32_t budget = (uint32_t)p.pf_bytes;
-    budget -= prefetch_range(p.w + (size_t)t.w_off16 * 16 + (size_t)skip * rb, (uint32_t)(t.nrows - skip) * rb, budget);
-    if (t.op == OP_FFN && budget)
-        prefetch_range(p.w + p.layer_bytes * t.layer + p.l_down + (size_t)(t.row0 / (2 * FFN_BLOCK)) * p.d * 16,
-                       (uint32_t)(t.nrows / (2 * FFN_BLOCK)) * (uint32_t)p.d * 16u, budget);
 }
 
 // Consumer wait on a counter: thread 0 spins, the rest learn the outcome at
@@ -924,7 +894,7 @@ __device__ __forceinline__ void ffn_down(Ctx& c, const TaskRec& t, int layer) {
 // gate/up pair stays inside one batch.  The batches come from the warp's
 // stream (already requested before the counter wait).  Returns false when
 // the CTA must stop (abort or watchdog), identically in every thread.
-template <int WT, int BASE, int NG>
+template <int WT, int BASE, int NG, bool SEL>
 __device__ bool gemv_run(Ctx& c, const TaskRec& t, int task_id, int step, float& best_v, int& best_i) {
     const VmParams& p = *c.p;
     constexpr int HP = wpc<WT>() / 2;
@@ -1081,9 +1051,12 @@ __device__ bool gemv_run(Ctx& c, const TaskRec& t, int task_id, int step, float&
             if (op == OP_LM) {
                 if (p.logits) p.logits[(size_t)step * p.V + row_g] = tot;
                 float v = tot;
-                if (p.top_k > 0) ffn_h(c)[rb + my_r] = tot;  // the CTA's top-k is taken after the loop
-                else if (p.inv_temp > 0.f)
-                    v = sample_score(tot, (uint32_t)row_g, (uint32_t)(p.pos0 + step), p.inv_temp, p.seed_lo, p.seed_hi);
+                if constexpr (SEL) {
+                    if (p.top_k > 0) ffn_h(c)[rb + my_r] = tot;  // the CTA's top-k is taken after the loop
+                    else if (p.inv_temp > 0.f)
+                        v = sample_score(tot, (uint32_t)row_g, (uint32_t)(p.pos0 + step), p.inv_temp, p.seed_lo,
+                                         p.seed_hi);
+                }
                 if (v > best_v) {  // rows ascend per lane: the first maximum is kept
                     best_v = v;
                     best_i = row_g;
@@ -1115,9 +1088,12 @@ __device__ bool gemv_run(Ctx& c, const TaskRec& t, int task_id, int step, float&
             } else if (op == OP_LM) {
                 if (p.logits) p.logits[(size_t)step * p.V + row_g] = tot;
                 float v = tot;
-                if (p.top_k > 0) ffn_h(c)[rr] = tot;
-                else if (p.inv_temp > 0.f)
-                    v = sample_score(tot, (uint32_t)row_g, (uint32_t)(p.pos0 + step), p.inv_temp, p.seed_lo, p.seed_hi);
+                if constexpr (SEL) {
+                    if (p.top_k > 0) ffn_h(c)[rr] = tot;
+                    else if (p.inv_temp > 0.f)
+                        v = sample_score(tot, (uint32_t)row_g, (uint32_t)(p.pos0 + step), p.inv_temp, p.seed_lo,
+                                         p.seed_hi);
+                }
                 if (v > best_v) {  // rows ascend per thread: the first maximum is kept
                     best_v = v;
                     best_i = row_g;
@@ -1141,11 +1117,11 @@ __device__ bool gemv_run(Ctx& c, const TaskRec& t, int task_id, int step, float&
     return true;
 }
 
-template <int WT, int BASE>
+template <int WT, int BASE, bool SEL>
 __device__ bool gemv_task(Ctx& c, const TaskRec& t, int task_id, int step, float& best_v, int& best_i) {
     const int S = 32 * t.wpr, CH = t.K / wpc<WT>(), ng = (CH + S - 1) / S;
     constexpr int NGMAX = 64 / wpc<WT>();  // 8 (16-bit), 4 (int8), 2 (int4)
-#define MK_RUN(N) return gemv_run<WT, BASE, (N <= NGMAX ? N : NGMAX)>(c, t, task_id, step, best_v, best_i)
+#define MK_RUN(N) return gemv_run<WT, BASE, (N <= NGMAX ? N : NGMAX), SEL>(c, t, task_id, step, best_v, best_i)
     switch (ng) {
         case 1: MK_RUN(1);
         case 2: MK_RUN(2);
@@ -1160,21 +1136,6 @@ __device__ bool gemv_task(Ctx& c, const TaskRec& t, int task_id, int step, float
 }
 
 // ------------------------------------------------------------------ attention
-template <int DPL>
-__device__ __forceinline__ void load_kv_row(const uint16_t* rowp, int lane, float (&f)[DPL]) {
-    if constexpr (DPL == 2) {
-        const uint32_t w = __ldcg((const unsigned int*)(rowp + lane * 2));
-        f[0] = bf16_bits_to_f32(w & 0xFFFFu);
-        f[1] = bf16_bits_to_f32(w >> 16);
-    } else {
-        const uint2 w = __ldcg((const uint2*)(rowp + lane * 4));
-        f[0] = bf16_bits_to_f32(w.x & 0xFFFFu);
-        f[1] = bf16_bits_to_f32(w.x >> 16);
-        f[2] = bf16_bits_to_f32(w.y & 0xFFFFu);
-        f[3] = bf16_bits_to_f32(w.y >> 16);
-    }
-}
-
 // One (KV head, chunk) task: RoPE for the group's queries and this step's
 // key, K/V append at pos (last chunk only), then an online-softmax pass over
 // the chunk's positions in tiles of ATTN_TILE.  Warp w owns positions
@@ -1202,16 +1163,26 @@ static __device__ __forceinline__ bool attn_task(Ctx& c, const TaskRec& t, int t
     uint16_t* kbase = p.kv + (((size_t)l * 2 + 0) * p.Hkv + g) * head_stride;
     uint16_t* vbase = p.kv + (((size_t)l * 2 + 1) * p.Hkv + g) * head_stride;
 
-    float kf[PPW][DPL];
+    uint32_t kraw[PPW][DPL / 2];
     uint32_t vraw[PPW][DPL / 2];
-    // K rows of a tile go to kf, V rows to vraw; the two halves are loaded
-    // separately so that the next tile's rows are in flight while this one
-    // is computed (V once staged in shared memory, K once the scores are done).
+    // K rows of a tile go to kraw, V rows to vraw, as raw bf16 pairs (widened
+    // where they are used, so that a load in flight does not hold the thread
+    // up before its wait); the two halves are loaded separately so that the
+    // next tile's rows are in flight while this one is computed (V once
+    // staged in shared memory, K once the scores are done).
     auto load_k = [&](int jt, int n) {
 #pragma unroll
         for (int k = 0; k < PPW; ++k) {
             const int jj = c.warp + NW * k, j = jt + jj;
-            if (jj < n && j != pos) load_kv_row<DPL>(kbase + (size_t)j * HD, c.lane, kf[k]);
+            if (jj < n && j != pos) {
+                if constexpr (DPL == 2) {
+                    kraw[k][0] = __ldcg((const unsigned int*)(kbase + (size_t)j * HD + c.lane * 2));
+                } else {
+                    const uint2 w = __ldcg((const uint2*)(kbase + (size_t)j * HD + c.lane * 4));
+                    kraw[k][0] = w.x;
+                    kraw[k][1] = w.y;
+                }
+            }
         }
     };
     auto load_v = [&](int jt, int n) {
@@ -1244,9 +1215,11 @@ static __device__ __forceinline__ bool attn_task(Ctx& c, const TaskRec& t, int t
                         dst[i] = vraw[k][i];
                     }
                 }
-                if (j == pos) {
+                if (j == pos) {  // this step's key (already bf16-rounded)
 #pragma unroll
-                    for (int i = 0; i < DPL; ++i) kf[k][i] = at.kcur[c.lane * DPL + i];
+                    for (int i = 0; i < DPL / 2; ++i)
+                        kraw[k][i] = (__float_as_uint(at.kcur[c.lane * DPL + 2 * i]) >> 16) |
+                                     (__float_as_uint(at.kcur[c.lane * DPL + 2 * i + 1]) & 0xFFFF0000u);
                 }
             }
         }
@@ -1320,7 +1293,10 @@ static __device__ __forceinline__ bool attn_task(Ctx& c, const TaskRec& t, int t
                     float sacc = 0.f;
                     if (h0 + hh < rep) {
 #pragma unroll
-                        for (int i = 0; i < DPL; ++i) sacc = fmaf(at.q[(h0 + hh) * HD + c.lane * DPL + i], kf[k][i], sacc);
+                        for (int i = 0; i < DPL; ++i)
+                            sacc = fmaf(at.q[(h0 + hh) * HD + c.lane * DPL + i],
+                                        __uint_as_float((i & 1) ? (kraw[k][i >> 1] & 0xFFFF0000u) : (kraw[k][i >> 1] << 16)),
+                                        sacc);
                     }
                     v[k * 4 + hh] = sacc;
                 }
@@ -1382,18 +1358,8 @@ static __device__ __forceinline__ bool attn_task(Ctx& c, const TaskRec& t, int t
 }
 
 // ------------------------------------------------------------------ top-k selection
-// The selection code runs once per step at most, so it is kept out of line
-// (the hot GEMV and attention code keeps the instruction cache); it gets the
-// block's handles by value instead of the context, which would then have to
-// live in local memory.
-struct Blk {
-    const VmParams* p;
-    Shared* sh;
-    float* xs;
-    int tid, lane, warp;
-};
-__device__ __forceinline__ Blk blk(const Ctx& c) { return Blk{c.p, c.sh, c.xs, c.tid, c.lane, c.warp}; }
-
+// This code exists only in the token-selection instantiation of the kernel
+// (SEL = true); the greedy instantiation carries none of it.
 // Scratch of a block selection, in the input-vector region: the LM-head task
 // holds its input fragments in registers by then (its rows are in the merge
 // scratch), and the select task has no input vector.
@@ -1412,7 +1378,7 @@ static_assert(LM_MAX_ROWS * sizeof(float) <= sizeof(MergeScratch), "LM rows of a
 // the keys that share the prefix found so far, and the bin holding rank k
 // extends the prefix.  Every consumer thread calls it; all get the result.
 template <typename KeyFn>
-__device__ __forceinline__ unsigned long long block_kth_largest(const Blk& b, int n, uint32_t k, KeyFn key) {
+__device__ __forceinline__ unsigned long long block_kth_largest(Ctx& b, int n, uint32_t k, KeyFn key) {
     SelScratch& ss = *reinterpret_cast<SelScratch*>(b.xs);
     if (b.tid == 0) {
         ss.prefix = 0ull;
@@ -1462,7 +1428,7 @@ __device__ __forceinline__ unsigned long long block_kth_largest(const Blk& b, in
 // After an LM-head task under top-k sampling: the CTA's k largest logits
 // (ties: lower index) become its candidates, as selection keys in
 // cand[blockIdx.x][0 .. MAX_TOP_K) (unused slots zero).
-static __device__ __noinline__ void lm_candidates(Blk b, int row0, int n) {
+static __device__ __forceinline__ void lm_candidates(Ctx& b, int row0, int n) {
     const VmParams& p = *b.p;
     const float* v = reinterpret_cast<const float*>(&b.sh->mg);
     auto key = [&](int i) { return sel_key(v[i], (uint32_t)(row0 + i)); };
@@ -1484,7 +1450,7 @@ static __device__ __noinline__ void lm_candidates(Blk b, int row0, int n) {
 // tasks' key; top-k sampling takes the global top k of the candidates (the
 // top k of the vocabulary, since each CTA sent its own top k) and samples it
 // by the largest Gumbel-max score.
-static __device__ __noinline__ void select_task(Blk b, int step) {
+static __device__ __forceinline__ void select_task(Ctx& b, int step) {
     const VmParams& p = *b.p;
     if (p.top_k == 0) {
         if (b.tid == 0) {
@@ -1534,7 +1500,7 @@ static __device__ __noinline__ void select_task(Blk b, int step) {
 // token is final (its counter), reads it, and stops when it is eos.  Every
 // CTA sees the same token at the same step boundary, so all stop together
 // and no task of the stopped step runs.  False also after an abort.
-static __device__ __noinline__ bool eos_continue(Blk b, int step) {
+static __device__ __forceinline__ bool eos_continue(Ctx& b, int step) {
     const VmParams& p = *b.p;
     if (b.tid == 0) {
         int go = b.sh->abort ? 0 : 1;
@@ -1561,28 +1527,31 @@ static __device__ __noinline__ bool eos_continue(Blk b, int step) {
 }
 
 // ------------------------------------------------------------------ consumer
-template <int WT, int BASE, int HD>
+template <int WT, int BASE, int HD, bool SEL>
 __device__ __forceinline__ void consumer(Ctx& c) {
     const VmParams& p = *c.p;
     for (int s = 0; s < p.n_steps && !c.abort; ++s) {
-        if (p.eos >= 0 && s > 0 && !p.skip_lm && !eos_continue(blk(c), s)) break;
+        if constexpr (SEL) {
+            if (p.eos >= 0 && s > 0 && !p.skip_lm && !eos_continue(c, s)) break;
+        }
         for (int qi = 0; qi < c.nrec && !c.abort; ++qi) {
             const TaskRec& t = c.tab[qi];
             const int tid_ = c.q0 + qi;  // queue index: identifies the task in errors and traces
             c.cur = qi;
             const uint64_t t_start = p.trace ? gtimer() : 0;
-            if (p.trace && c.tid == 0) c.sh->t_ph[0] = c.sh->t_ph[1] = 0ull;
+            if (p.trace && c.tid == 0) c.sh->t_ph[0] = c.sh->t_ph[1] = c.sh->t_ph[2] = c.sh->t_ph[3] = 0ull;
             float best_v = -3.0e38f;
             int best_i = 0;
             const bool gemv = t.op == OP_QKV || t.op == OP_O || t.op == OP_GU || t.op == OP_DOWN || t.op == OP_FFN ||
                               (t.op == OP_LM && !p.skip_lm);
             bool ok;
             if (gemv) {
-                if (p.pf_bytes && c.tid == 0) prefetch_task<WT>(p, t);
-                ok = gemv_task<WT, BASE>(c, t, tid_, s, best_v, best_i);
-                if (ok && t.op == OP_LM && p.top_k > 0) {
-                    bar_consumers();  // every row of the task is in shared memory
-                    lm_candidates(blk(c), t.row0, t.nrows);
+                ok = gemv_task<WT, BASE, SEL>(c, t, tid_, s, best_v, best_i);
+                if constexpr (SEL) {
+                    if (ok && t.op == OP_LM && p.top_k > 0) {
+                        bar_consumers();  // every row of the task is in shared memory
+                        lm_candidates(c, t.row0, t.nrows);
+                    }
                 }
                 if constexpr (WT == MK_W_BF16 || WT == MK_W_FP16) {
                     if (ok && t.op == OP_FFN) {
@@ -1593,7 +1562,9 @@ __device__ __forceinline__ void consumer(Ctx& c) {
             } else {
                 ok = t.op == OP_ATTN ? attn_task<HD>(c, t, tid_, s) : wait_counters(c, t, tid_, s);
                 if (ok && t.op == OP_MERGE) merge_task(c, t);
-                if (ok && t.op == OP_SELECT && !p.skip_lm) select_task(blk(c), s);
+                if constexpr (SEL) {
+                    if (ok && t.op == OP_SELECT && !p.skip_lm) select_task(c, s);
+                }
                 if (ok && t.op == OP_FIN && c.tid == 0 && !p.skip_lm) {
                     const unsigned long long k = __ldcg(p.key);
                     if ((k >> 49) != key_tag((uint32_t)(p.epoch0 + s))) {
@@ -1622,6 +1593,7 @@ __device__ __forceinline__ void consumer(Ctx& c) {
                 if (c.lane == 0) c.sh->keys[c.warp] = key;
             }
             const int sw = signal_warp(t, gemv);
+            if (p.trace && c.tid == 0) c.sh->t_ph[2] = gtimer();
             if (c.warp == sw) cp_async_wait<0>();  // its release then has no copies to wait for
             bar_consumers();
             if (gemv && t.op == OP_LM && c.tid == 0) {
@@ -1630,6 +1602,7 @@ __device__ __forceinline__ void consumer(Ctx& c) {
                 atomicMax(p.key, key);
             }
             signal_counter(c, t, sw);
+            if (p.trace && c.warp == sw && c.lane == 0) c.sh->t_ph[3] = gtimer();
             // The copies the task skipped go out now, unless an attention or
             // merge task follows: it does not use the ring, and its own loads
             // are on the layer's critical path, so the copies wait for its end.
@@ -1646,14 +1619,15 @@ __device__ __forceinline__ void consumer(Ctx& c) {
                     r[3] = gtimer();
                     r[4] = c.sh->t_ph[0];
                     r[5] = c.sh->t_ph[1];
-                    r[6] = r[7] = 0;
+                    r[6] = c.sh->t_ph[2];
+                    r[7] = c.sh->t_ph[3];
                 }
             }
         }
     }
 }
 
-template <int WT, int BASE, int HD>
+template <int WT, int BASE, int HD, bool SEL>
 __global__ void __launch_bounds__(THREADS, 1) vm_kernel(const VmParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     Ctx c;
@@ -1682,7 +1656,7 @@ __global__ void __launch_bounds__(THREADS, 1) vm_kernel(const VmParams p) {
         ((uint4*)c.ring)[i] = make_uint4(0, 0, 0, 0);
     __syncthreads();  // the task table is complete
     for (int i = 0; i < ring_slots<WT>() - 1; ++i) stream_issue<WT>(c);
-    consumer<WT, BASE, HD>(c);
+    consumer<WT, BASE, HD, SEL>(c);
     cp_async_wait<0>();  // no copy may land in shared memory after the CTA exits
 }
 

@@ -4,18 +4,19 @@
 namespace mk {
 
 // ------------------------------------------------------------------ launch
-const void* vm_kernel_bf16(int hd);
-const void* vm_kernel_fp16(int hd);
-const void* vm_kernel_int8(int hd);
-const void* vm_kernel_int4(int hd);
+const void* vm_kernel_bf16(int hd, bool sel);
+const void* vm_kernel_fp16(int hd, bool sel);
+const void* vm_kernel_int8(int hd, bool sel);
+const void* vm_kernel_int4(int hd, bool sel);
 
-const void* vm_kernel_for(int wdtype, int base, int hd) {
+// sel: the instance with token selection (sampling, EOS, the token-select task).
+const void* vm_kernel_for(int wdtype, int base, int hd, bool sel) {
     if (hd != 64 && hd != 128) return nullptr;
-    if (base == MK_W_FP16) return wdtype == MK_W_FP16 ? vm_kernel_fp16(hd) : nullptr;
+    if (base == MK_W_FP16) return wdtype == MK_W_FP16 ? vm_kernel_fp16(hd, sel) : nullptr;
     switch (wdtype) {
-        case MK_W_BF16: return vm_kernel_bf16(hd);
-        case MK_W_INT8_ROW: return vm_kernel_int8(hd);
-        case MK_W_INT4_G128: return vm_kernel_int4(hd);
+        case MK_W_BF16: return vm_kernel_bf16(hd, sel);
+        case MK_W_INT8_ROW: return vm_kernel_int8(hd, sel);
+        case MK_W_INT4_G128: return vm_kernel_int4(hd, sel);
         default: return nullptr;
     }
 }

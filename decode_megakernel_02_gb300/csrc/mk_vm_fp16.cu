@@ -1,10 +1,13 @@
-// Decode kernel instances for fp16 GEMV weights (head_dim 64 and 128).
+// Decode kernel instances for fp16 GEMV weights (head_dim 64 and 128, greedy and token-selection).
 #include "mk_vm.cuh"
 
 namespace mk {
 
-const void* vm_kernel_fp16(int hd) {
-    return hd == 64 ? (const void*)vm_kernel<MK_W_FP16, MK_W_FP16, 64> : (const void*)vm_kernel<MK_W_FP16, MK_W_FP16, 128>;
+// sel: the token-selection instance (sampling, EOS, the token-select task).
+const void* vm_kernel_fp16(int hd, bool sel) {
+    if (sel)
+        return hd == 64 ? (const void*)vm_kernel<MK_W_FP16, MK_W_FP16, 64, true> : (const void*)vm_kernel<MK_W_FP16, MK_W_FP16, 128, true>;
+    return hd == 64 ? (const void*)vm_kernel<MK_W_FP16, MK_W_FP16, 64, false> : (const void*)vm_kernel<MK_W_FP16, MK_W_FP16, 128, false>;
 }
 
 }  // namespace mk

@@ -16,8 +16,7 @@ keep the fastest.  This is the deterministic core of that loop, with no agent:
 3. The points that pass are timed with CUDA events over full decode launches.
    The result is printed as JSON, fastest first.
 
-    python -m decode_megakernel_02_gb300.tune --workload llama-1b --chunks 2,3,4,6,8 --sms 0,144 \
-        --prefetch-kb=-1,256,1024
+    python -m decode_megakernel_02_gb300.tune --workload llama-1b --chunks 2,3,4,6,8 --sms 0,144
 """
 import itertools
 import argparse
@@ -86,7 +85,7 @@ def main(argv=None):
     ap.add_argument("--forced", type=int, default=8, help="teacher-forced steps of the agreement check")
     ap.add_argument("--tokens", type=int, default=0, help="tokens per timed launch (default: the workload's)")
     ap.add_argument("--reps", type=int, default=3)
-    ap.add_argument("--prefetch-kb", default="0", help="L2 prefetch KB per CTA per task (0: default, -1: off)")
+    ap.add_argument("--token-select", default="0", help="0 / 1: schedules with the token-select task")
     ap.add_argument("--reference", default=None, help=".npy teacher-forced reference logits [forced, vocab]")
     args = ap.parse_args(argv)
 
@@ -108,9 +107,9 @@ def main(argv=None):
         ref, ref_kind = run_point(desc, blob, mk.make_config(), prompt, forced, 1, 1)[0], "default configuration"
     ints = (lambda v: [int(x) for x in v.split(",")])
     rows = []
-    for sms, ch, kb in itertools.product(ints(args.sms), ints(args.chunks), ints(args.prefetch_kb)):
-        cfg = mk.make_config(sms=sms, attn_chunks=ch, l2_prefetch_kb=kb)
-        point = {"sms": sms, "attn_chunks": ch, "l2_prefetch_kb": kb}
+    for sms, ch, ts in itertools.product(ints(args.sms), ints(args.chunks), ints(args.token_select)):
+        cfg = mk.make_config(sms=sms, attn_chunks=ch, token_select=ts)
+        point = {"sms": sms, "attn_chunks": ch, "token_select": ts}
         st, why = mk.mk_validate_schedule(desc, cfg, sms or 152)
         if st != mk.MK_OK:
             rows.append(dict(point, status="rejected by the validator", why=why))

@@ -92,12 +92,14 @@ typedef struct {
                                value built)                                               */
     int32_t attn_chunks;    /* split-KV chunks per KV head; default from max_seq and sms     */
     int32_t watchdog_ms;    /* a device wait gives up after this long; default 1000          */
-    int32_t l2_prefetch_kb; /* KB of a GEMV task's weights (past what the warps' rings load
-                               first) each CTA asks L2 to prefetch just before the task's
-                               wait; 0 default (1024), < 0 off                              */
     int32_t token_select;   /* 1: one more task per step selects the token after the LM
                                head (needed for top-k sampling); 0 (default): the LM-head
                                tasks' block argmax is the selection                       */
+    int32_t prefill_chunk;  /* 0 (default): mk_prefill runs the decode kernel over the prompt,
+                               one position per step.  A multiple of 128 up to 4096: mk_prefill
+                               runs the prompt through tensor-core GEMMs (tcgen05) in chunks of
+                               this many tokens (16-bit weights only; the workspace grows by the
+                               chunk's activations)                                        */
 } mk_schedule_config;
 
 /* ------------------------------------------------------------------ packing
@@ -244,11 +246,18 @@ mk_status mk_create(const mk_model_desc* desc, const mk_schedule_config* cfg,
                     mk_handle** out);
 
 /* Prefill: positions 0..n-2 of tokens_host go through the decoder (KV writes
- * only, LM head skipped) in one launch; afterwards pos = n-1 and the pending
- * token is tokens_host[n-1], which the first decode step feeds.  Resets the
- * sequence (any earlier tokens are discarded).  Synchronous.  Errors:
- * INVALID_ARG (n < 1, token out of range), CAPACITY (n > max_seq), CUDA,
- * TIMEOUT. */
+ * only, LM head skipped); afterwards pos = n-1 and the pending token is
+ * tokens_host[n-1], which the first decode step feeds.  Resets the sequence
+ * (any earlier tokens are discarded).  Synchronous.
+ * With mk_schedule_config.prefill_chunk = 0 the decode kernel runs the prompt
+ * one position per step in one launch.  With a chunk size C, the prompt goes
+ * through the layers C tokens at a time: RMSNorm, then the QKV, O, gate/up
+ * and down projections as tensor-core GEMMs (tcgen05.mma, operands staged by
+ * TMA, 16-bit activations, fp32 accumulation) with RoPE + KV append, residual
+ * and SwiGLU fused into their epilogues, and causal GQA attention of the chunk
+ * over the cache (Kog monokernel tutorial: prefill in the same runtime as
+ * decode).  Errors: INVALID_ARG (n < 1, token out of range), CAPACITY
+ * (n > max_seq), CUDA, TIMEOUT. */
 mk_status mk_prefill(mk_handle* h, const int32_t* tokens_host, int32_t n);
 
 /* Greedy decode of n_steps tokens in ONE launch.  Step s feeds the pending
@@ -377,9 +386,12 @@ mk_status mk_debug_dequant(const mk_model_desc* desc, const void* weights_dev, i
 
 /* Record %globaltimer stamps of every task of later launches into trace_dev,
  * uint64 [ctas][records_per_cta][8] = {queue index | step << 32, task start,
- * wait done, after signal, input ready, compute done, 0, 0}: "input ready" is
- * the end of a GEMV task's prologue or the arrival of an attention task's
- * q/k/v, "compute done" the end of its row batches or tiles (0 for others).  The queue index is the task's
+ * wait done, task end, input ready, compute done, body done, signal released}:
+ * "input ready" is the end of a GEMV task's prologue or the arrival of an
+ * attention task's q/k/v, "compute done" the end of its row batches or tiles
+ * (both 0 for other tasks), "body done" the end of the instruction before its
+ * signal, "signal released" the counter release (0 for tasks that signal
+ * none); "task end" follows the copies issued after the signal.  The queue index is the task's
  * position in the concatenated per-CTA queues (mk_ir.queue holds the task id
  * at each index).  Record k of a CTA is step * queue_len + queue slot, and
  * records past the capacity are dropped.  NULL disables tracing.  The buffer

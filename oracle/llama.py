@@ -210,12 +210,14 @@ def teacher_forced(m: Model, prompt, forced, max_seq=None):
     return np.stack(out)
 
 
-def forward_full(m: Model, tokens, last=None):
+def forward_full(m: Model, tokens, last=None, kv_out=None):
     """All positions at once with a causal mask (matrix form).
 
     K and V are rounded to bf16 exactly as the cache stores them.  Returns the
     logits for every position [T, V], or for the last ``last`` positions only
-    (the final norm and LM head are then applied to those rows alone)."""
+    (the final norm and LM head are then applied to those rows alone).  With a
+    list ``kv_out``, each layer's cache entries (K, V), float64 arrays
+    [Hkv, T, hd] of bf16 values, are appended to it."""
     s = m.s
     T = len(tokens)
     x = m.W("embed")[np.asarray(tokens)].copy()
@@ -229,6 +231,8 @@ def forward_full(m: Model, tokens, last=None):
         q = np.stack([rope(q[p], p, s.rope_theta) for p in range(T)])
         k = round_to_bf16(np.stack([rope(k[p], p, s.rope_theta) for p in range(T)]))
         v = round_to_bf16(v)
+        if kv_out is not None:
+            kv_out.append((k.transpose(1, 0, 2).copy(), v.transpose(1, 0, 2).copy()))
         o = np.empty((T, s.n_q_heads, s.head_dim))
         for i in range(s.n_q_heads):
             g = i // rep

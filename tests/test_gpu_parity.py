@@ -377,7 +377,7 @@ def test_schedule_grid_search_on_tiny(mk, capsys, tmp_path):
     ref = L.forward_full(oracle_model(w, weights), np.concatenate([prompt, forced[1:]]), last=8)
     np.save(tmp_path / "ref.npy", ref.astype(np.float32))
     tune.main(["--workload", "tiny", "--chunks", "0,2,4", "--sms", "0,7", "--reps", "1",
-               "--prefetch-kb=-1,0", "--reference", str(tmp_path / "ref.npy")])
+               "--token-select", "0,1", "--reference", str(tmp_path / "ref.npy")])
     out = json.loads(capsys.readouterr().out)
     assert out["agreement_reference"] == "reference file"
     assert len(out["points"]) == 12

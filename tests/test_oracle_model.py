@@ -115,3 +115,19 @@ def test_greedy_bookkeeping():
         assert ids[s] == int(np.argmax(logits[s]))
     # teacher forcing on the greedy tokens reproduces the greedy logits exactly
     assert np.array_equal(L.teacher_forced(m, prompt, ids), logits)
+
+
+def test_forward_full_kv_equals_incremental_cache():
+    """The cache entries forward_full reports are the ones incremental decode
+    writes (same bf16 rounding, same positions)."""
+    w = synthetic.get_workload("tiny").with_(n_layers=2)
+    m = L.Model(w, synthetic.generate_weights(w))
+    toks = synthetic.generate_prompt(w, 9)
+    kv_full = []
+    L.forward_full(m, toks, kv_out=kv_full)
+    cache = m.new_cache(len(toks))
+    for p, t in enumerate(toks):
+        L.decode_step(m, cache, int(t), p, want_logits=False)
+    for l, (k, v) in enumerate(kv_full):
+        assert np.allclose(k, cache["K"][l], rtol=0, atol=1e-12 + 8e-3 * np.abs(k).max())
+        assert np.allclose(v, cache["V"][l], rtol=0, atol=1e-12 + 8e-3 * np.abs(v).max())
