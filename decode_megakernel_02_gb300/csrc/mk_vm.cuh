@@ -108,8 +108,8 @@ struct Shared {
     int32_t abort;                  // set when this CTA must stop
     int32_t tok;                    // broadcast of the step's input token
     unsigned long long t_waited;    // trace: when the current task's wait completed
-    unsigned long long t_ph[4];     // trace: input ready (prologue done / q,k,v arrived), compute done,
-                                    // task body done (before the signal), signal released
+    unsigned long long t_ph[3];     // trace: input ready (prologue done / q,k,v arrived), compute done,
+                                    // task body done (before the signal)
 };
 
 // Weights per 16-byte chunk of a packed row's codes.
@@ -1539,7 +1539,7 @@ __device__ __forceinline__ void consumer(Ctx& c) {
             const int tid_ = c.q0 + qi;  // queue index: identifies the task in errors and traces
             c.cur = qi;
             const uint64_t t_start = p.trace ? gtimer() : 0;
-            if (p.trace && c.tid == 0) c.sh->t_ph[0] = c.sh->t_ph[1] = c.sh->t_ph[2] = c.sh->t_ph[3] = 0ull;
+            if (p.trace && c.tid == 0) c.sh->t_ph[0] = c.sh->t_ph[1] = c.sh->t_ph[2] = 0ull;
             float best_v = -3.0e38f;
             int best_i = 0;
             const bool gemv = t.op == OP_QKV || t.op == OP_O || t.op == OP_GU || t.op == OP_DOWN || t.op == OP_FFN ||
@@ -1602,7 +1602,10 @@ __device__ __forceinline__ void consumer(Ctx& c) {
                 atomicMax(p.key, key);
             }
             signal_counter(c, t, sw);
-            if (p.trace && c.warp == sw && c.lane == 0) c.sh->t_ph[3] = gtimer();
+            if (p.trace && c.warp == sw && c.lane == 0) {  // the releasing lane stamps its own slot
+                const int k = s * c.nrec + qi;
+                if (k < p.trace_cap) p.trace[((size_t)blockIdx.x * p.trace_cap + k) * 8 + 7] = gtimer();
+            }
             // The copies the task skipped go out now, unless an attention or
             // merge task follows: it does not use the ring, and its own loads
             // are on the layer's critical path, so the copies wait for its end.
@@ -1619,8 +1622,7 @@ __device__ __forceinline__ void consumer(Ctx& c) {
                     r[3] = gtimer();
                     r[4] = c.sh->t_ph[0];
                     r[5] = c.sh->t_ph[1];
-                    r[6] = c.sh->t_ph[2];
-                    r[7] = c.sh->t_ph[3];
+                    r[6] = c.sh->t_ph[2];  // r[7]: written by the releasing lane
                 }
             }
         }
