@@ -88,6 +88,67 @@ def dequant_int4(q, s16, group=128):
     return (np.asarray(q).astype(np.float32) * s).astype(np.float32)
 
 
+# ----------------------------------------------------------------- FP8 E4M3, block-scaled
+# The Netra Kernel summary ("TL;DR": FP8 serving ops) and BASELINE's next rows
+# name FP8 weights; the pages fix no format details.  Readings: the OCP FP8
+# E4M3 format (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; exponent 0
+# holds the subnormals m * 2^-9; S.1111.111 is NaN and there is no infinity, so
+# the largest finite magnitude is 1.75 * 2^8 = 448), one fp16 scale per 128
+# consecutive k of a row (as for int4): s = fp16(fp32(max|w|) / 448), codes =
+# E4M3 nearest to fp32(w) / fp32(s), ties to the even code, s == 0 -> 0.
+
+def e4m3_values():
+    """float64 value of each of the 256 codes (NaN for the two NaN codes)."""
+    v = np.empty(256)
+    for c in range(256):
+        sign = -1.0 if c & 0x80 else 1.0
+        e, m = (c >> 3) & 0xF, c & 7
+        if e == 15 and m == 7:
+            v[c] = np.nan
+        elif e == 0:
+            v[c] = sign * m * 2.0 ** -9
+        else:
+            v[c] = sign * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+    return v
+
+
+def f32_to_e4m3(x):
+    """Round float32 values to the nearest E4M3 code (ties to the even code),
+    clamping magnitudes to 448; returns uint8 codes."""
+    x = np.asarray(x, np.float32).astype(np.float64)
+    vals = e4m3_values()[:0x7F]              # the 127 non-negative finite codes, ascending
+    a = np.minimum(np.abs(x), 448.0)
+    hi = np.searchsorted(vals, a, side="left").clip(0, len(vals) - 1)
+    lo = (hi - 1).clip(0, len(vals) - 1)
+    dlo, dhi = a - vals[lo], vals[hi] - a
+    pick_hi = (dhi < dlo) | ((dhi == dlo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo).astype(np.uint8)
+    code = np.where(a == vals[lo], lo, code).astype(np.uint8)
+    return np.where(np.signbit(x) & (code != 0), code | 0x80, code).astype(np.uint8)
+
+
+def quantize_fp8_g128(w, group=128):
+    """w: float32 [N, K], K % 128 == 0.  Returns (codes uint8 [N, K], s float16 [N, K/128])."""
+    w = np.asarray(w, np.float32)
+    n, k = w.shape
+    assert k % group == 0
+    g = w.reshape(n, k // group, group)
+    amax = np.max(np.abs(g), axis=2)
+    s16 = _fp16_of_fp32(amax / np.float32(448.0))
+    s32 = s16.astype(np.float32)[:, :, None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = (g / s32).astype(np.float32)
+    r = np.where(s32 == 0, np.float32(0), r)
+    return f32_to_e4m3(r).reshape(n, k), s16
+
+
+def dequant_fp8(codes, s16, group=128):
+    """w' = fp32(e4m3(code)) * fp32(s): exact in float32 (4 + 11 significant bits)."""
+    v = e4m3_values()[np.asarray(codes, np.uint8)].astype(np.float32)
+    s = np.repeat(s16.astype(np.float32), group, axis=1)
+    return (v * s).astype(np.float32)
+
+
 GEMV_TENSORS = ("wq", "wk", "wv", "wo", "wgate", "wup", "wdown")
 
 
@@ -109,6 +170,9 @@ def quantised_model_weights(shape, weights, wdtype, base_dtype="bf16"):
         elif wdtype == "int4":
             q, s = quantize_int4_g128(w32)
             deq[nm] = dequant_int4(q, s).astype(np.float64)
+        elif wdtype == "fp8":
+            q, s = quantize_fp8_g128(w32)
+            deq[nm] = dequant_fp8(q, s).astype(np.float64)
         else:
             raise ValueError(wdtype)
         raw[nm] = (q, s)

@@ -219,3 +219,66 @@ def test_dequant_exact_in_fp32():
     d = Q.dequant_int8(q, s)
     exact = q.astype(np.float64) * s.astype(np.float64)[:, None]
     assert np.array_equal(d.astype(np.float64), exact)
+
+
+# ----------------------------------------------------------------- FP8 E4M3
+def test_e4m3_golden_values():
+    import os
+    from oracle import quant as Q
+    v = Q.e4m3_values()
+    path = os.path.join(os.path.dirname(__file__), "golden", "e4m3_values.txt")
+    for ln in open(path):
+        if ln.startswith("#") or not ln.strip():
+            continue
+        code, want = ln.split()
+        got = v[int(code, 16)]
+        if want == "nan":
+            assert np.isnan(got)
+        else:
+            assert got == float(want) and np.signbit(got) == want.startswith("-"), (code, got, want)
+    assert np.sum(np.isnan(v)) == 2 and np.nanmax(v) == 448.0
+
+
+def test_e4m3_rounding_brute_force():
+    """Every value rounds to the nearest finite E4M3 value, ties to the even
+    code, magnitudes above 448 to 448 (brute force over the whole table)."""
+    from oracle import quant as Q
+    v = Q.e4m3_values()
+    finite = [c for c in range(256) if not np.isnan(v[c])]
+    rng = np.random.default_rng(11)
+    x = np.concatenate([rng.standard_normal(4000) * 40, rng.standard_normal(2000) * 0.01,
+                        (v[finite] + np.roll(v[finite], 1)) / 2,  # midpoints: the ties
+                        np.array([500.0, -1000.0, 2.0 ** -10, 3 * 2.0 ** -11])]).astype(np.float32)
+    codes = Q.f32_to_e4m3(x)
+    for xi, c in zip(x.astype(np.float64), codes):
+        a = min(abs(xi), 448.0) * (1 if xi >= 0 else -1)
+        d = np.array([abs(v[f] - a) for f in finite])
+        best = np.flatnonzero(d == d.min())
+        cands = [finite[i] for i in best]
+        if len(cands) > 1:  # a tie: the even code (the zeros count as one value)
+            cands = [f for f in cands if f % 2 == 0 and not (f == 0x80)] or cands
+        assert int(c) in cands or (v[int(c)] == 0 and all(v[f] == 0 for f in cands)), (xi, hex(c), cands)
+
+
+def test_fp8_quantiser_properties():
+    from oracle import quant as Q
+    rng = np.random.default_rng(3)
+    w = (rng.standard_normal((6, 256)) * 0.02).astype(np.float32)
+    w[2, 128:] = 0.0  # an all-zero group: scale 0, codes 0
+    codes, s = Q.quantize_fp8_g128(w)
+    deq = Q.dequant_fp8(codes, s)
+    assert s[2, 1] == 0 and not codes[2, 128:].any()
+    # the dequantised value is exact in fp32 and within half a code spacing of w
+    v = Q.e4m3_values()
+    for r in range(6):
+        for g in range(2):
+            sc = float(s[r, g])
+            if sc == 0:
+                continue
+            x = w[r, 128 * g:128 * g + 128].astype(np.float64) / sc
+            q = v[codes[r, 128 * g:128 * g + 128]]
+            spacing = np.maximum(2.0 ** (np.floor(np.log2(np.maximum(np.abs(x), 2.0 ** -6))) - 3), 2.0 ** -9)
+            assert np.all(np.abs(x - q) <= spacing / 2 + 1e-12)
+    # idempotent on grid values
+    c2, s2 = Q.quantize_fp8_g128(deq)
+    assert np.array_equal(c2, codes) and np.array_equal(s2, s)
