@@ -45,7 +45,8 @@ UNIT = "tokens/s"
 def algorithmic_bytes(w, pos0, n_steps):
     """Bytes the decode path must move per launch (see the module docstring)."""
     def rb(K):
-        return {"bf16": 2 * K, "fp16": 2 * K, "int8": K + 2, "int4": K // 2 + 2 * (K // 128)}[w.wdtype]
+        return {"bf16": 2 * K, "fp16": 2 * K, "int8": K + 2, "int4": K // 2 + 2 * (K // 128),
+                "fp8": K + 2 * (K // 128)}[w.wdtype]
     d, qd, kd, F, V, L = w.d_model, w.q_dim, w.kv_dim, w.d_ffn, w.vocab, w.n_layers
     gemv = L * ((qd + 2 * kd) * rb(d) + d * rb(qd) + 2 * F * rb(d) + d * rb(F)) + V * rb(d)
     fixed = gemv + 2 * d + (2 * L + 1) * 2 * d
@@ -186,7 +187,7 @@ def oracle_rate(w, weights, budget_s=12.0, min_steps=2, max_steps=64):
     from oracle import llama as L
     from oracle import quant as Q
     deq = None
-    if w.wdtype in ("int8", "int4"):
+    if w.wdtype in ("int8", "int4", "fp8"):
         deq, _ = Q.quantised_model_weights(w, weights, w.wdtype)
     m = L.Model(w, weights, w.base_dtype, dequantised=deq)
     prompt = synthetic.generate_prompt(w)
@@ -340,7 +341,7 @@ def main():
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": {"bf16": "bf16", "fp16": "fp16", "int8": "int8w-f32acc",
-                                           "int4": "int4w-f32acc"}[w.wdtype],
+                                           "int4": "int4w-f32acc", "fp8": "fp8e4m3w-f32acc"}[w.wdtype],
             "data": "synthetic", "config": config,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,

@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(HERE, "libmk.so")
 # ------------------------------------------------------------------ constants (include/mk.h)
 MK_OK, MK_ERR_INVALID_ARG, MK_ERR_UNSUPPORTED, MK_ERR_SCHEDULE_INVALID = 0, 1, 2, 3
 MK_ERR_CAPACITY, MK_ERR_CUDA, MK_ERR_TIMEOUT, MK_ERR_DEVICE = 4, 5, 6, 7
-MK_W_BF16, MK_W_FP16, MK_W_INT8_ROW, MK_W_INT4_G128 = 0, 1, 2, 3
+MK_W_BF16, MK_W_FP16, MK_W_INT8_ROW, MK_W_INT4_G128, MK_W_FP8_E4M3 = 0, 1, 2, 3, 4
 MK_FLAG_PROJ_BIAS, MK_FLAG_TIED_HEAD, MK_FLAG_ROPE_SCALING = 1, 2, 4
 (MK_T_EMBED, MK_T_LM_HEAD, MK_T_FINAL_NORM, MK_T_ATTN_NORM, MK_T_FFN_NORM, MK_T_WQ, MK_T_WK, MK_T_WV,
  MK_T_WO, MK_T_WGATE, MK_T_WUP, MK_T_WDOWN) = range(12)
@@ -27,7 +27,8 @@ MK_IR_MAX_WAITS = 2
 MK_STATIC_SCRATCH_BYTES = 8 << 20
 OPS = {1: "qkv", 2: "attn", 3: "o", 4: "gu", 5: "down", 6: "lm", 7: "fin", 8: "ffn", 9: "merge", 10: "select"}
 MK_MAX_TOP_K = 64
-WDTYPES = {"bf16": MK_W_BF16, "fp16": MK_W_FP16, "int8": MK_W_INT8_ROW, "int4": MK_W_INT4_G128}
+WDTYPES = {"bf16": MK_W_BF16, "fp16": MK_W_FP16, "int8": MK_W_INT8_ROW, "int4": MK_W_INT4_G128,
+           "fp8": MK_W_FP8_E4M3}
 STATUS_NAMES = {0: "MK_OK", 1: "MK_ERR_INVALID_ARG", 2: "MK_ERR_UNSUPPORTED", 3: "MK_ERR_SCHEDULE_INVALID",
                 4: "MK_ERR_CAPACITY", 5: "MK_ERR_CUDA", 6: "MK_ERR_TIMEOUT", 7: "MK_ERR_DEVICE"}
 THREADS_PER_CTA = 256  # eight warps
@@ -88,6 +89,7 @@ SIGNATURES = {
                                 ctypes.POINTER(_I32), ctypes.POINTER(_I32), ctypes.POINTER(_I32)]),
     "mk_quantize_int8": (_I32, [_P, _I64, _I64, _P, _P]),
     "mk_quantize_int4": (_I32, [_P, _I64, _I64, _P, _P]),
+    "mk_quantize_fp8": (_I32, [_P, _I64, _I64, _P, _P]),
     "mk_kv_cache_size": (_I32, [_DESC, ctypes.POINTER(_SZ)]),
     "mk_workspace_size": (_I32, [_DESC, _CFG, _I32, ctypes.POINTER(_SZ)]),
     "mk_build_ir": (_I32, [_DESC, _CFG, _I32, ctypes.POINTER(ctypes.POINTER(mk_ir))]),
@@ -210,6 +212,15 @@ def mk_quantize_int4(w):
     q = np.empty((n, k), np.int8)
     s = np.empty((n, k // 128), np.uint16)
     _check(load().mk_quantize_int4(w.ctypes.data, n, k, q.ctypes.data, s.ctypes.data))
+    return q, s.view(np.float16)
+
+
+def mk_quantize_fp8(w):
+    w = np.ascontiguousarray(w, np.float32)
+    n, k = w.shape
+    q = np.empty((n, k), np.uint8)
+    s = np.empty((n, k // 128), np.uint16)
+    _check(load().mk_quantize_fp8(w.ctypes.data, n, k, q.ctypes.data, s.ctypes.data))
     return q, s.view(np.float16)
 
 

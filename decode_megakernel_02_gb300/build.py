@@ -16,7 +16,8 @@ CUDA_HOME = os.environ.get("CUDA_HOME", "/usr/local/cuda")
 NVCC = os.path.join(CUDA_HOME, "bin", "nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
-CU_SRCS = ["mk_vm_bf16.cu", "mk_vm_fp16.cu", "mk_vm_int8.cu", "mk_vm_int4.cu", "mk_vm_common.cu", "mk_runtime.cu",
+CU_SRCS = ["mk_vm_bf16.cu", "mk_vm_fp16.cu", "mk_vm_int8.cu", "mk_vm_int4.cu", "mk_vm_fp8.cu", "mk_vm_common.cu",
+           "mk_runtime.cu",
            "mk_static.cu", "mk_prefill.cu"]
 CPP_SRCS = ["mk_host.cpp", "mk_schedule.cpp", "mk_validate.cpp"]
 

@@ -127,6 +127,44 @@ void quant_row_int4(const float* w, int64_t k, int8_t* q, uint16_t* s16) {
     }
 }
 
+// FP8 E4M3 (OCP 8-bit floating point: 1 sign, 4 exponent bits with bias 7, 3
+// mantissa bits; exponent 0 holds the subnormals m * 2^-9; S.1111.111 is NaN;
+// 448 is the largest magnitude), rounded to nearest, ties to even, clamped to
+// 448.  Codes ascend with the value, so the code is the rounded mantissa step
+// count on the 2^-9 grid (subnormals) or (e + 7) * 8 + round(a * 2^(3 - e)) - 8
+// for a in [2^e, 2^(e+1)): a carry past 8 lands on the next exponent's code.
+uint8_t f32_to_e4m3_rne(float f) {
+    uint32_t x;
+    std::memcpy(&x, &f, 4);
+    const uint8_t sign = (uint8_t)((x >> 24) & 0x80u);
+    const float a = std::fabs(f);
+    if (a >= 448.f) return sign | 0x7Eu;
+    int code;
+    if (a < 0.015625f) {  // below 2^-6: the subnormal grid
+        code = (int)std::nearbyint(a * 512.f);
+    } else {
+        int e;
+        std::frexp(a, &e);  // a = m * 2^e with m in [0.5, 1)
+        e -= 1;             // a in [2^e, 2^(e+1))
+        code = (e + 7) * 8 + (int)std::nearbyint(std::ldexp(a, 3 - e)) - 8;
+    }
+    if (code > 0x7E) code = 0x7E;
+    return code == 0 ? 0 : (uint8_t)(sign | code);
+}
+
+// FP8 E4M3 with one scale per 128 consecutive k: s = fp16(fp32(max|w|) / 448).
+void quant_row_fp8(const float* w, int64_t k, uint8_t* q, uint16_t* s16) {
+    for (int64_t g = 0; g < k / 128; ++g) {
+        const float* wg = w + g * 128;
+        float amax = 0.f;
+        for (int i = 0; i < 128; ++i) amax = std::max(amax, std::fabs(wg[i]));
+        const uint16_t sh = f32_to_f16_rne(amax / 448.0f);
+        const float s = f16_to_f32(sh);
+        s16[g] = sh;
+        for (int i = 0; i < 128; ++i) q[g * 128 + i] = s == 0.f ? 0 : f32_to_e4m3_rne(wg[i] / s);
+    }
+}
+
 // ------------------------------------------------------------------ contract
 static bool pow2_le(int v, int hi) { return v >= 1 && v <= hi; }
 
@@ -173,11 +211,12 @@ mk_status check_desc(const mk_model_desc* d) {
         set_error("base_dtype %d must be MK_W_BF16 or MK_W_FP16", d->base_dtype);
         return MK_ERR_UNSUPPORTED;
     }
-    if (d->wdtype != d->base_dtype && d->wdtype != MK_W_INT8_ROW && d->wdtype != MK_W_INT4_G128) {
+    const bool quant = d->wdtype == MK_W_INT8_ROW || d->wdtype == MK_W_INT4_G128 || d->wdtype == MK_W_FP8_E4M3;
+    if (d->wdtype != d->base_dtype && !quant) {
         set_error("wdtype %d must equal base_dtype or be a quantised type", d->wdtype);
         return MK_ERR_UNSUPPORTED;
     }
-    if ((d->wdtype == MK_W_INT8_ROW || d->wdtype == MK_W_INT4_G128) && d->base_dtype != MK_W_BF16) {
+    if (quant && d->base_dtype != MK_W_BF16) {
         set_error("quantised weights are packed from bf16 sources only");
         return MK_ERR_UNSUPPORTED;
     }
@@ -191,6 +230,7 @@ int64_t row_stride(int64_t K, int wdtype) {
     switch (wdtype) {
         case MK_W_INT8_ROW: return up(K + 2, 16);                 // codes + fp16 scale
         case MK_W_INT4_G128: return up(K / 2 + 2 * (K / 128), 16); // nibbles + fp16 scales
+        case MK_W_FP8_E4M3: return up(K + 2 * (K / 128), 16);      // E4M3 codes + fp16 scales
         default: return up(2 * K, 16);
     }
 }
@@ -320,12 +360,12 @@ mk_status mk_pack_tensor(const mk_model_desc* desc, int32_t tensor, int32_t laye
     for (int32_t r = 0; r < p.rows; ++r) {
         uint8_t* dst = blob + p.off + (int64_t)(p.first + (int64_t)r * p.step) * p.stride;
         const uint16_t* row = src + (int64_t)r * K;
-        if (p.stride == 0) {  // W_down in column blocks: row r of block c at (c * rows + r) * 16 bytes
-            for (int64_t c = 0; c < K / FFN_BLOCK; ++c)
-                std::memcpy(blob + p.off + (c * p.rows + r) * 16, row + c * FFN_BLOCK, 16);
+        if (p.stride == 0 && desc->wdtype == desc->base_dtype) {
+            // W_down in column blocks: row r of block c at (c * rows + r) * 16 bytes
+            for (int64_t c = 0; c < K / 8; ++c) std::memcpy(blob + p.off + (c * p.rows + r) * 16, row + c * 8, 16);
             continue;
         }
-        std::memset(dst, 0, (size_t)p.stride);
+        if (p.stride) std::memset(dst, 0, (size_t)p.stride);
         if (desc->wdtype == desc->base_dtype) {
             std::memcpy(dst, row, (size_t)K * 2);
             continue;
@@ -333,11 +373,45 @@ mk_status mk_pack_tensor(const mk_model_desc* desc, int32_t tensor, int32_t laye
         wf.resize(K);
         q.resize(K);
         for (int64_t k = 0; k < K; ++k) wf[k] = base_to_f32(row[k], desc->base_dtype);
+        if (p.stride == 0) {
+            // Quantised W_down in column blocks of 16 bytes: block c holds the
+            // codes of units [c * BU, (c + 1) * BU) of every row r at
+            // (c * rows + r) * 16; after the blocks come the fp16 scales, per
+            // row (int8, [rows]) or per 128-unit group ([K / 128][rows]).
+            const int64_t BU = ffn_block(desc->wdtype), rows = p.rows;
+            uint8_t* codes = blob + p.off;
+            uint16_t* scales = (uint16_t*)(blob + p.off + rows * K * 16 / BU);
+            if (desc->wdtype == MK_W_INT8_ROW) {
+                uint16_t sc;
+                quant_row_int8(wf.data(), K, q.data(), &sc);
+                for (int64_t c = 0; c < K / BU; ++c) std::memcpy(codes + (c * rows + r) * 16, q.data() + c * BU, 16);
+                std::memcpy(scales + r, &sc, 2);
+            } else if (desc->wdtype == MK_W_FP8_E4M3) {
+                s16.resize(K / 128);
+                quant_row_fp8(wf.data(), K, (uint8_t*)q.data(), s16.data());
+                for (int64_t c = 0; c < K / BU; ++c) std::memcpy(codes + (c * rows + r) * 16, q.data() + c * BU, 16);
+                for (int64_t g = 0; g < K / 128; ++g) std::memcpy(scales + g * rows + r, &s16[g], 2);
+            } else {
+                s16.resize(K / 128);
+                quant_row_int4(wf.data(), K, q.data(), s16.data());
+                for (int64_t c = 0; c < K / BU; ++c)
+                    for (int64_t k = 0; k < BU; k += 2)
+                        codes[(c * rows + r) * 16 + k / 2] = (uint8_t)(((uint8_t)q[c * BU + k] & 0xF) |
+                                                                       (((uint8_t)q[c * BU + k + 1] & 0xF) << 4));
+                for (int64_t g = 0; g < K / 128; ++g) std::memcpy(scales + g * rows + r, &s16[g], 2);
+            }
+            continue;
+        }
         if (desc->wdtype == MK_W_INT8_ROW) {
             uint16_t s;
             quant_row_int8(wf.data(), K, q.data(), &s);
             std::memcpy(dst, q.data(), (size_t)K);
             std::memcpy(dst + K, &s, 2);
+        } else if (desc->wdtype == MK_W_FP8_E4M3) {
+            s16.resize(K / 128);
+            quant_row_fp8(wf.data(), K, (uint8_t*)q.data(), s16.data());
+            std::memcpy(dst, q.data(), (size_t)K);
+            std::memcpy(dst + K, s16.data(), s16.size() * 2);
         } else {
             s16.resize(K / 128);
             quant_row_int4(wf.data(), K, q.data(), s16.data());
@@ -364,6 +438,15 @@ mk_status mk_quantize_int4(const float* w, int64_t n, int64_t k, int8_t* q, uint
         return MK_ERR_INVALID_ARG;
     }
     for (int64_t r = 0; r < n; ++r) quant_row_int4(w + r * k, k, q + r * k, s16 + r * (k / 128));
+    return MK_OK;
+}
+
+mk_status mk_quantize_fp8(const float* w, int64_t n, int64_t k, uint8_t* q, uint16_t* s16) {
+    if (!w || !q || !s16 || n < 0 || k < 128 || k % 128) {
+        set_error("bad quantiser arguments (k must be a positive multiple of 128)");
+        return MK_ERR_INVALID_ARG;
+    }
+    for (int64_t r = 0; r < n; ++r) quant_row_fp8(w + r * k, k, q + r * k, s16 + r * (k / 128));
     return MK_OK;
 }
 

@@ -37,22 +37,43 @@ constexpr int ATTN_TILE = 32;           // positions per online-softmax tile
 constexpr int PART_COPIES = 4;
 constexpr int CTR_STRIDE = 32;          // u32 words between counters (128 B lines)
 constexpr int MAX_HC = 1024;            // query heads x split-KV chunks (merge scratch)
-constexpr int FFN_BLOCK = 8;            // hidden units per 16-byte column block of a fused down projection
 constexpr int FFN_MAX_UNITS = 2 * MAX_HC;  // hidden units of one OP_FFN task (its SwiGLU outputs reuse the merge scratch)
 constexpr int MAX_TOP_K = MK_MAX_TOP_K;     // top-k candidates per CTA
 constexpr int LM_MAX_ROWS = 2 * MAX_HC;     // LM-head rows of one CTA under top-k sampling (kept in the merge scratch)
 
-// The FFN runs fused (OP_FFN) for 16-bit weights when every warp's share of
-// the d_model output rows is a whole number of 32-row lines (d_model % 256
-// == 0), a column block of a warp's rows fits one 16-line ring slot, and the
-// lines per block (d_model / 256) is one the kernel is built for.
+// Hidden units per 16-byte column chunk of a fused down projection: 8
+// (16-bit), 16 (int8) or 32 (int4) codes.
+#ifdef __CUDACC__
+__host__ __device__
+#endif
+constexpr int ffn_block(int wdtype) {
+    return wdtype == MK_W_INT8_ROW || wdtype == MK_W_FP8_E4M3 ? 16 : wdtype == MK_W_INT4_G128 ? 32 : 8;
+}
+
+// 512-byte lines a ring slot holds in the column phase of the fused FFN.
+#ifdef __CUDACC__
+__host__ __device__
+#endif
+constexpr int ffn_slot_lines(int wdtype) {
+    return wdtype == MK_W_INT8_ROW || wdtype == MK_W_FP8_E4M3 ? 8 : wdtype == MK_W_INT4_G128 ? 4 : 16;
+}
+
+// The FFN runs fused (OP_FFN) when every warp's share of the d_model output
+// rows is a whole number of 32-row lines (d_model % 256 == 0) and the lines
+// per column block of a warp's rows (d_model / 256) is one the kernel is built
+// for; a block whose lines exceed a ring slot spans several batches.
 #ifdef __CUDACC__
 __host__ __device__
 #endif
 constexpr bool ffn_fused(int wdtype, int base_dtype, int d_model) {
-    return wdtype == base_dtype && d_model % 256 == 0 &&
-           (d_model / 256 == 1 || d_model / 256 == 2 || d_model / 256 == 4 || d_model / 256 == 8 ||
-            d_model / 256 == 10 || d_model / 256 == 12 || d_model / 256 == 16);
+    return wdtype == base_dtype
+               ? d_model % 256 == 0 && (d_model / 256 == 1 || d_model / 256 == 2 || d_model / 256 == 4 ||
+                                        d_model / 256 == 8 || d_model / 256 == 10 || d_model / 256 == 12 ||
+                                        d_model / 256 == 16)
+               : (wdtype == MK_W_INT8_ROW || wdtype == MK_W_INT4_G128 || wdtype == MK_W_FP8_E4M3) &&
+                     d_model % 256 == 0 &&
+                     (d_model / 256 == 1 || d_model / 256 == 2 || d_model / 256 == 4 || d_model / 256 == 8 ||
+                      d_model / 256 == 16);
 }
 
 // Warps that share one weight row: enough that each lane holds at most
@@ -99,7 +120,7 @@ static_assert(sizeof(TaskRec) == 32, "TaskRec layout");
 
 // Byte offsets of the packed weight blob.
 struct BlobLayout {
-    bool down_cols;     // W_down stored as FFN_BLOCK-column blocks (fused FFN) instead of rows
+    bool down_cols;     // W_down stored in 16-byte column blocks (fused FFN) instead of rows
     int64_t row_qkv, row_o, row_gu, row_down, row_lm;   // row strides
     int64_t norm_bytes;                                 // bytes per norm-gain vector (padded)
     int64_t layer_bytes;                                // one layer block

@@ -905,8 +905,11 @@ mk_status mk_debug_dequant(const mk_model_desc* desc, const void* weights_dev, i
     int32_t first = 0, step = 1, rows = 0;
     mk_status st = mk_tensor_layout(desc, tensor, layer, &off, &stride, &first, &step, &rows);
     if (st) return st;
-    if (!weights_dev || !out_dev || stride == 0) {
-        set_error("NULL pointer or not a GEMV tensor");
+    const bool cols = stride == 0 && tensor == MK_T_WDOWN &&
+                      (desc->wdtype == MK_W_INT8_ROW || desc->wdtype == MK_W_INT4_G128 ||
+                       desc->wdtype == MK_W_FP8_E4M3);  // column blocks
+    if (!weights_dev || !out_dev || (stride == 0 && !cols)) {
+        set_error("NULL pointer or not a quantisable GEMV tensor");
         return MK_ERR_INVALID_ARG;
     }
     int K = 0;

@@ -335,16 +335,18 @@ mk_status lower(const mk_model_desc* d, const Config& c, Lowering* lw) {
         prev_ctr = ctr(l, 2);
 
         if (fused) {
-            // ---- fused FFN: each CTA owns blocks of FFN_BLOCK hidden units: their
-            // gate/up rows, SwiGLU in shared memory, and their down-projection
-            // column block, added into the next residual buffer
+            // ---- fused FFN: each CTA owns blocks of BU hidden units (one 16-byte
+            // column chunk of the down projection): their gate/up rows, SwiGLU
+            // in shared memory, and their down-projection column block, added
+            // into the next residual buffer
             ids.clear();
-            const int64_t blocks = F / FFN_BLOCK, max_blocks = FFN_MAX_UNITS / FFN_BLOCK;
-            const int64_t block_bytes = FFN_BLOCK * (2 * bl.row_gu + 2 * dm);
+            const int64_t BU = ffn_block(d->wdtype);
+            const int64_t blocks = F / BU, max_blocks = FFN_MAX_UNITS / BU;
+            const int64_t block_bytes = BU * 2 * bl.row_gu + dm * 16;
             for (auto& p : B.split(blocks, block_bytes)) {
                 for (int64_t b0 = p.second.first; b0 < p.second.second; b0 += max_blocks) {
                     const int64_t b1 = std::min(p.second.second, b0 + max_blocks);
-                    const int64_t u0 = b0 * FFN_BLOCK, u1 = b1 * FFN_BLOCK;
+                    const int64_t u0 = b0 * BU, u1 = b1 * BU;
                     DevTask t = gemv_task(OP_FFN, l, 2 * u0, 2 * (u1 - u0), dm, bl.row_gu, lb + bl.l_gu, 2, ctr(l, 3));
                     std::vector<mk_ir_access> acc;
                     acc.push_back(A(B_X, MK_ACC_READ, xm, xm + 4 * dm));

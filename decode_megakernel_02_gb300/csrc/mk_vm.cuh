@@ -28,6 +28,7 @@
 //    launches.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -81,6 +82,14 @@ __device__ __forceinline__ float i8_to_f32(uint32_t word_xor80, int k) {
 __device__ __forceinline__ float i4_to_f32(uint32_t word_xor88, int n) {
     return __uint_as_float(((word_xor88 >> (4 * n)) & 0xFu) | 0x4B000000u) - 8388616.0f;
 }
+// Two FP8 E4M3 codes (the low 16 bits, first code in the low byte) -> exact
+// floats, through the hardware conversion to a half pair (every E4M3 value is
+// a half value).
+__device__ __forceinline__ unsigned long long e4m3x2_pair(uint32_t two) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xFFFFu), __NV_E4M3);
+    const float2 f = __half22float2(*(const __half2*)&h);
+    return (unsigned long long)__float_as_uint(f.x) | ((unsigned long long)__float_as_uint(f.y) << 32);
+}
 
 // ------------------------------------------------------------------ shared memory
 // Layout: [input vector of a GEMV task | attention scratch] (one region: a
@@ -114,7 +123,12 @@ struct Shared {
 
 // Weights per 16-byte chunk of a packed row's codes.
 template <int WT>
-__host__ __device__ constexpr int wpc() { return WT == MK_W_INT8_ROW ? 16 : WT == MK_W_INT4_G128 ? 32 : 8; }
+__host__ __device__ constexpr int wpc() {
+    return WT == MK_W_INT8_ROW || WT == MK_W_FP8_E4M3 ? 16 : WT == MK_W_INT4_G128 ? 32 : 8;
+}
+// Weights with one fp16 scale per 128 consecutive k of a row.
+template <int WT>
+__host__ __device__ constexpr bool group_scaled() { return WT == MK_W_INT4_G128 || WT == MK_W_FP8_E4M3; }
 
 constexpr int RW = 2;           // rows per batch
 constexpr int TRAILER = 256;    // max trailer bytes per row (fp16 scales of a K <= 16384 int4 row)
@@ -125,7 +139,7 @@ __host__ __device__ constexpr int ring_slot_bytes() {
 }
 template <int WT>
 __host__ __device__ constexpr int ring_slots() {  // slots that fit beside the other shared memory
-    return WT == MK_W_INT4_G128 ? 9 : WT == MK_W_INT8_ROW ? 5 : 3;
+    return WT == MK_W_INT4_G128 ? 9 : WT == MK_W_INT8_ROW || WT == MK_W_FP8_E4M3 ? 5 : 3;
 }
 
 struct WarpStream {
@@ -567,8 +581,8 @@ __device__ __forceinline__ float sum2(unsigned long long v) {
 
 // The lane's partial dot product over its chunks of one row: w[j] is chunk
 // L + S*j of the row's codes, xr holds the matching input values as fp32
-// pairs (WPC/2 pairs per chunk).  int4 chunks carry their group-128 scale in
-// sc[j] (a chunk of 32 codes never straddles a group).
+// pairs (WPC/2 pairs per chunk).  int4 and fp8 chunks carry their group-128
+// scale in sc[j] (a chunk of 32 or 16 codes never straddles a group).
 template <int WT, int NG>
 __device__ __forceinline__ float chunks_dot(const uint4 (&w)[NG], const float (&sc)[NG],
                                             const unsigned long long (&xr)[NG * wpc<WT>() / 2]) {
@@ -598,6 +612,15 @@ __device__ __forceinline__ float chunks_dot(const uint4 (&w)[NG], const float (&
                 a0 = ffma2(pack2(i8_to_f32(u, 0), i8_to_f32(u, 1)), xr[j * HP + 2 * i], a0);
                 a1 = ffma2(pack2(i8_to_f32(u, 2), i8_to_f32(u, 3)), xr[j * HP + 2 * i + 1], a1);
             }
+        } else if constexpr (WT == MK_W_FP8_E4M3) {
+            unsigned long long pa = 0ull, pb = 0ull;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                pa = ffma2(e4m3x2_pair(wv[i]), xr[j * HP + 2 * i], pa);
+                pb = ffma2(e4m3x2_pair(wv[i] >> 16), xr[j * HP + 2 * i + 1], pb);
+            }
+            if (j & 1) f1 = fmaf(sc[j], sum2(pa) + sum2(pb), f1);
+            else f0 = fmaf(sc[j], sum2(pa) + sum2(pb), f0);
         } else {  // int4
             unsigned long long pa = 0ull, pb = 0ull;
 #pragma unroll
@@ -612,7 +635,7 @@ __device__ __forceinline__ float chunks_dot(const uint4 (&w)[NG], const float (&
             else f0 = fmaf(sc[j], sum2(pa) + sum2(pb), f0);
         }
     }
-    if constexpr (WT == MK_W_INT4_G128) return f0 + f1;
+    if constexpr (group_scaled<WT>()) return f0 + f1;
     else return sum2(a0) + sum2(a1);
 }
 
@@ -676,14 +699,15 @@ __device__ __forceinline__ bool stream_next(const Ctx& c, WarpStream& w) {
         if (w.q < w.nb) return true;
         if (w.ffn_blocks) {  // the row phase of an OP_FFN task is done: its column blocks follow
             const int R = p.d / NW;  // output rows of this warp
+            const int SL = ffn_slot_lines(p.wdtype);
             w.cols = 1;
-            w.nl = R / 32;
-            w.tlc = 16 / w.nl;
-            w.nrows = w.ffn_blocks;
+            w.nl = R / 32;                                      // 512-byte lines per block of this warp's rows
+            w.tlc = w.nl <= SL ? (SL / w.nl) * w.nl : SL;       // lines per batch (whole blocks, or a part)
+            w.nrows = w.ffn_blocks * w.nl;                      // lines of the task
             w.row_bytes = p.d * 16;
             w.base = w.base2 + (size_t)c.warp * R * 16;
             w.lofs = c.lane * 16;
-            w.nb = (w.ffn_blocks + w.tlc - 1) / w.tlc;
+            w.nb = (w.nrows + w.tlc - 1) / w.tlc;
             w.q = 0;
             w.ngroups = 1;
             w.ffn_blocks = 0;
@@ -702,8 +726,9 @@ __device__ __forceinline__ bool stream_next(const Ctx& c, WarpStream& w) {
               (op == OP_LM && !p.skip_lm)))
             continue;
         if (op == OP_FFN) {
-            w.ffn_blocks = t.nrows / (2 * FFN_BLOCK);
-            w.base2 = p.w + p.layer_bytes * t.layer + p.l_down + (size_t)(t.row0 / (2 * FFN_BLOCK)) * p.d * 16;
+            const int BU = ffn_block(p.wdtype);
+            w.ffn_blocks = t.nrows / (2 * BU);
+            w.base2 = p.w + p.layer_bytes * t.layer + p.l_down + (size_t)(t.row0 / (2 * BU)) * p.d * 16;
         }
         const int K = t.K, g = t.wpr;
         const int L = (c.warp % g) * 32 + c.lane;
@@ -712,7 +737,9 @@ __device__ __forceinline__ bool stream_next(const Ctx& c, WarpStream& w) {
         w.ngroups = NW / g;
         w.grp = c.warp / g;
         w.S = 32 * g;
-        const int code_bytes = p.wdtype == MK_W_INT8_ROW ? K : p.wdtype == MK_W_INT4_G128 ? K / 2 : 2 * K;
+        const int code_bytes = p.wdtype == MK_W_INT8_ROW || p.wdtype == MK_W_FP8_E4M3 ? K
+                               : p.wdtype == MK_W_INT4_G128                             ? K / 2
+                                                                                        : 2 * K;
         const int CHc = code_bytes / 16;
         w.nl = L < CHc ? (CHc - L + w.S - 1) / w.S : 0;  // this lane's chunks of a row
         w.tlc = (w.row_bytes - code_bytes) / 16;
@@ -734,13 +761,24 @@ __device__ __forceinline__ void stream_issue(Ctx& c) {
     if (!w.done && stream_next(c, w)) {
         uint8_t* slot = c.ring + (size_t)w.si * ring_slot_bytes<WT>() + lane * 16;
         const int64_t jstep = (int64_t)w.S * 16;
-        if (w.cols) {  // tlc blocks of nl lines: line k of the slot <- line m of block seg
-            int seg = w.q * w.tlc, m = 0;
-            const int lines = w.tlc * w.nl;
+        if (w.cols) {  // lines q*tlc .. of the task: line i is line i % nl of block i / nl
+            int seg, m = 0, lines;
+            if constexpr (WT == MK_W_BF16 || WT == MK_W_FP16) {  // whole blocks: tlc / nl of them
+                seg = w.q * (16 / w.nl);
+                lines = min(w.tlc, w.nrows - w.q * w.tlc);
+            } else {
+                if (w.tlc >= w.nl) {  // whole blocks per batch
+                    seg = w.q * (w.tlc / w.nl);
+                } else {              // a block spans nl / tlc batches
+                    const int bpb = w.nl / w.tlc;
+                    seg = w.q / bpb;
+                    m = (w.q - seg * bpb) * w.tlc;
+                }
+                lines = min(w.tlc, w.nrows - w.q * w.tlc);
+            }
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
-                if (k < lines && seg < w.nrows)
-                    cp_async16(slot + k * 512, w.base + (size_t)seg * w.row_bytes + m * 512 + w.lofs);
+                if (k < lines) cp_async16(slot + k * 512, w.base + (size_t)seg * w.row_bytes + m * 512 + w.lofs);
                 if (++m == w.nl) {
                     m = 0;
                     ++seg;
@@ -823,17 +861,78 @@ __device__ __forceinline__ void red_add_f32(float* p, float v) {
 // Down projection of an OP_FFN task: y[r] = sum over the task's hidden units
 // u of Wdown[r][u] * h[u], for every output row r, added into the next
 // layer's residual buffer (which O initialised to x_mid).  W_down is packed in
-// column blocks of FFN_BLOCK units: block b holds, for r = 0..d-1, the 16
-// bytes Wdown[r][8b .. 8b+8).  Warp w owns rows [w*R, (w+1)*R), R = d/8, so a
-// block gives it NL = R/32 lines of 512 bytes: lane l of line m holds row
-// w*R + 32m + l.  The lane keeps NL packed accumulators and ends with one
-// red.add per row; the ring batches hold 16/NL blocks each.
+// 16-byte column chunks of BU units (8 bf16/fp16, 16 int8/fp8 or 32 int4 codes):
+// block b holds, for r = 0..d-1, the codes of Wdown[r][BU b .. BU (b+1)).
+// Warp w owns rows [w*R, (w+1)*R), R = d/8, so a block gives it NL = R/32
+// lines of 512 bytes: lane l of line m holds row w*R + 32m + l.  The lane
+// keeps one accumulator per line and ends with one red.add per row.  A ring
+// batch holds SEGB whole blocks, or (when a block has more lines than a slot
+// holds) the part bb of a block.  Scales of quantised codes follow the
+// blocks: one per row for int8 (applied before the red.add), one per row and
+// 128-unit group for int4 and fp8 (applied to each block's dot product).
+template <int WT>
+__device__ __forceinline__ unsigned long long col_pair(uint32_t word, int i) {
+    if constexpr (WT == MK_W_BF16) {
+        (void)i;
+        return pack2(__uint_as_float(word << 16), __uint_as_float(word & 0xFFFF0000u));
+    } else {
+        const float2 f = __half22float2(*(const __half2*)&word);
+        (void)i;
+        return pack2(f.x, f.y);
+    }
+}
+// The BU inputs of a column block as fp32 pairs (loaded once per block).
+template <int WT>
+__device__ __forceinline__ void load_h(const float* hs, unsigned long long (&hx)[ffn_block(WT) / 2]) {
+#pragma unroll
+    for (int i = 0; i < ffn_block(WT) / 4; ++i) {
+        const float4 h = *(const float4*)(hs + 4 * i);
+        hx[2 * i] = pack2(h.x, h.y);
+        hx[2 * i + 1] = pack2(h.z, h.w);
+    }
+}
+// Accumulate one 16-byte column chunk times its inputs into the packed pair
+// accumulator a.
+template <int WT>
+__device__ __forceinline__ void chunk_fma(const uint4 w, const unsigned long long (&hx)[ffn_block(WT) / 2],
+                                          unsigned long long& a) {
+    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+    if constexpr (WT == MK_W_BF16 || WT == MK_W_FP16) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) a = ffma2(col_pair<WT>(wv[i], i), hx[i], a);
+    } else if constexpr (WT == MK_W_INT8_ROW) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t u = wv[i] ^ 0x80808080u;
+            a = ffma2(pack2(i8_to_f32(u, 0), i8_to_f32(u, 1)), hx[2 * i], a);
+            a = ffma2(pack2(i8_to_f32(u, 2), i8_to_f32(u, 3)), hx[2 * i + 1], a);
+        }
+    } else if constexpr (WT == MK_W_FP8_E4M3) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            a = ffma2(e4m3x2_pair(wv[i]), hx[2 * i], a);
+            a = ffma2(e4m3x2_pair(wv[i] >> 16), hx[2 * i + 1], a);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t u = wv[i] ^ 0x88888888u;
+            a = ffma2(pack2(i4_to_f32(u, 0), i4_to_f32(u, 1)), hx[4 * i], a);
+            a = ffma2(pack2(i4_to_f32(u, 2), i4_to_f32(u, 3)), hx[4 * i + 1], a);
+            a = ffma2(pack2(i4_to_f32(u, 4), i4_to_f32(u, 5)), hx[4 * i + 2], a);
+            a = ffma2(pack2(i4_to_f32(u, 6), i4_to_f32(u, 7)), hx[4 * i + 3], a);
+        }
+    }
+}
+
+// 16-bit weights: SEGB = 16 / NL whole blocks per batch and packed pair
+// accumulators, no scales.
 template <int WT, int NL>
-__device__ __forceinline__ void ffn_cols(Ctx& c, const TaskRec& t, int layer) {
+__device__ __forceinline__ void ffn_cols16(Ctx& c, const TaskRec& t, int layer) {
     const VmParams& p = *c.p;
     constexpr int NB = ring_slots<WT>();
     constexpr int SEGB = 16 / NL;
-    const int kc = t.nrows / (2 * FFN_BLOCK);
+    const int kc = t.nrows / (2 * ffn_block(WT));
     const int nb2 = (kc + SEGB - 1) / SEGB;
     const float* hs = ffn_h(c);
     unsigned long long acc[NL];
@@ -846,26 +945,10 @@ __device__ __forceinline__ void ffn_cols(Ctx& c, const TaskRec& t, int layer) {
         for (int sg = 0; sg < SEGB; ++sg) {
             const int seg = b * SEGB + sg;
             if (seg < kc) {
-                const float4 h0 = *(const float4*)(hs + seg * FFN_BLOCK);
-                const float4 h1 = *(const float4*)(hs + seg * FFN_BLOCK + 4);
-                const unsigned long long hx[4] = {pack2(h0.x, h0.y), pack2(h0.z, h0.w), pack2(h1.x, h1.y),
-                                                  pack2(h1.z, h1.w)};
+                unsigned long long hx[4];
+                load_h<WT>(hs + seg * 8, hx);
 #pragma unroll
-                for (int m = 0; m < NL; ++m) {
-                    const uint4 w = *(const uint4*)(slot + (sg * NL + m) * 512);
-                    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        unsigned long long wp;
-                        if constexpr (WT == MK_W_BF16) {
-                            wp = pack2(__uint_as_float(wv[i] << 16), __uint_as_float(wv[i] & 0xFFFF0000u));
-                        } else {
-                            const float2 f = __half22float2(*(const __half2*)&wv[i]);
-                            wp = pack2(f.x, f.y);
-                        }
-                        acc[m] = ffma2(wp, hx[i], acc[m]);
-                    }
-                }
+                for (int m = 0; m < NL; ++m) chunk_fma<WT>(*(const uint4*)(slot + (sg * NL + m) * 512), hx, acc[m]);
             }
         }
         __syncwarp();  // the slot is reused by a later issue of this warp
@@ -876,6 +959,97 @@ __device__ __forceinline__ void ffn_cols(Ctx& c, const TaskRec& t, int layer) {
     for (int m = 0; m < NL; ++m) red_add_f32(xo + 32 * m, sum2(acc[m]));
 }
 
+template <int WT, int NL>
+__device__ __forceinline__ void ffn_cols(Ctx& c, const TaskRec& t, int layer) {
+    if constexpr (WT == MK_W_BF16 || WT == MK_W_FP16) {
+        ffn_cols16<WT, NL>(c, t, layer);
+        return;
+    }
+    const VmParams& p = *c.p;
+    constexpr int NB = ring_slots<WT>();
+    constexpr int BU = ffn_block(WT), SL = ffn_slot_lines(WT);
+    constexpr bool QUANT = !(WT == MK_W_BF16 || WT == MK_W_FP16);
+    const int kc = t.nrows / (2 * BU);
+    const float* hs = ffn_h(c);
+    const int r0 = c.warp * (p.d / NW) + c.lane;  // row of line 0 of this lane
+    // quantised scales: after the codes of all F / BU blocks (d x 16 bytes each)
+    const uint16_t* scales =
+        QUANT ? (const uint16_t*)(p.w + p.layer_bytes * layer + p.l_down + (size_t)p.d * (p.F / BU) * 16) : nullptr;
+    const int u0 = t.row0 / 2;  // first hidden unit of the task
+    // 16-bit and int8: packed pair accumulators over the whole task; int4: a
+    // float accumulator per line that takes each block's scaled dot product
+    unsigned long long acc2[NL];
+    float acc[NL], sc[NL];
+    int sc_group = -1;
+#pragma unroll
+    for (int m = 0; m < NL; ++m) {
+        acc2[m] = 0ull;
+        acc[m] = 0.f;
+    }
+    unsigned long long hx[BU / 2];
+    auto line = [&](int m, const uint8_t* src) {
+        if constexpr (group_scaled<WT>()) {
+            unsigned long long a = 0ull;
+            chunk_fma<WT>(*(const uint4*)src, hx, a);
+            acc[m] = fmaf(sc[m], sum2(a), acc[m]);
+        } else {
+            chunk_fma<WT>(*(const uint4*)src, hx, acc2[m]);
+        }
+    };
+    auto block_scales = [&](int seg) {  // int4, fp8: the scales of block seg's group for this lane's rows
+        if constexpr (group_scaled<WT>()) {
+            const int g = (u0 + seg * BU) >> 7;
+            if (g != sc_group) {
+                sc_group = g;
+#pragma unroll
+                for (int m = 0; m < NL; ++m) sc[m] = half_bits_to_f32(__ldg(scales + (size_t)g * p.d + r0 + 32 * m));
+            }
+        }
+    };
+    if constexpr (NL <= SL) {
+        constexpr int SEGB = SL / NL;  // whole blocks per batch
+        const int nb2 = (kc + SEGB - 1) / SEGB;
+        for (int b = 0; b < nb2; ++b) {
+            ring_acquire<WT>(c, b == nb2 - 1);
+            const uint8_t* slot = c.ring + (size_t)c.rs * ring_slot_bytes<WT>() + c.lane * 16;
+#pragma unroll
+            for (int sg = 0; sg < SEGB; ++sg) {
+                const int seg = b * SEGB + sg;
+                if (seg < kc) {
+                    block_scales(seg);
+                    load_h<WT>(hs + seg * BU, hx);
+#pragma unroll
+                    for (int m = 0; m < NL; ++m) line(m, slot + (sg * NL + m) * 512);
+                }
+            }
+            __syncwarp();  // the slot is reused by a later issue of this warp
+            if (++c.rs == NB) c.rs = 0;
+        }
+    } else {
+        constexpr int BPB = NL / SL;  // batches per block
+        for (int seg = 0; seg < kc; ++seg) {
+            block_scales(seg);
+            load_h<WT>(hs + seg * BU, hx);
+#pragma unroll
+            for (int bb = 0; bb < BPB; ++bb) {
+                ring_acquire<WT>(c, seg == kc - 1 && bb == BPB - 1);
+                const uint8_t* slot = c.ring + (size_t)c.rs * ring_slot_bytes<WT>() + c.lane * 16;
+#pragma unroll
+                for (int k = 0; k < SL; ++k) line(bb * SL + k, slot + k * 512);
+                __syncwarp();
+                if (++c.rs == NB) c.rs = 0;
+            }
+        }
+    }
+    float* xo = xbuf(p, layer + 1) + r0;
+#pragma unroll
+    for (int m = 0; m < NL; ++m) {
+        float v = group_scaled<WT>() ? acc[m] : sum2(acc2[m]);
+        if constexpr (WT == MK_W_INT8_ROW) v *= half_bits_to_f32(__ldg(scales + r0 + 32 * m));
+        red_add_f32(xo + 32 * m, v);
+    }
+}
+
 template <int WT>
 __device__ __forceinline__ void ffn_down(Ctx& c, const TaskRec& t, int layer) {
     switch (c.p->d / 256) {  // lines per block; the host only fuses these shapes
@@ -883,8 +1057,12 @@ __device__ __forceinline__ void ffn_down(Ctx& c, const TaskRec& t, int layer) {
         case 2: ffn_cols<WT, 2>(c, t, layer); break;
         case 4: ffn_cols<WT, 4>(c, t, layer); break;
         case 8: ffn_cols<WT, 8>(c, t, layer); break;
-        case 10: ffn_cols<WT, 10>(c, t, layer); break;
-        case 12: ffn_cols<WT, 12>(c, t, layer); break;
+        case 10:
+            if constexpr (WT == MK_W_BF16 || WT == MK_W_FP16) ffn_cols<WT, 10>(c, t, layer);
+            break;
+        case 12:
+            if constexpr (WT == MK_W_BF16 || WT == MK_W_FP16) ffn_cols<WT, 12>(c, t, layer);
+            break;
         default: ffn_cols<WT, 16>(c, t, layer); break;
     }
 }
@@ -1006,9 +1184,10 @@ __device__ bool gemv_run(Ctx& c, const TaskRec& t, int task_id, int step, float&
 #pragma unroll
             for (int j = 0; j < NG; ++j) {
                 w[j] = *(const uint4*)(slot + (r * NGM + j) * 512 + c.lane * 16);
-                if constexpr (WT == MK_W_INT4_G128)
-                    sc[j] = half_bits_to_f32(
-                        *(const uint16_t*)(slot + RW * NGM * 512 + r * TRAILER + 2 * (((L + S * j) >> 2) & (TRAILER / 2 - 1))));
+                if constexpr (group_scaled<WT>())  // chunks per 128-k group: 4 (int4), 8 (fp8)
+                    sc[j] = half_bits_to_f32(*(const uint16_t*)(slot + RW * NGM * 512 + r * TRAILER +
+                                                                2 * (((L + S * j) >> (WT == MK_W_INT4_G128 ? 2 : 3)) &
+                                                                     (TRAILER / 2 - 1))));
                 else
                     sc[j] = 0.f;
             }
@@ -1553,11 +1732,9 @@ __device__ __forceinline__ void consumer(Ctx& c) {
                         lm_candidates(c, t.row0, t.nrows);
                     }
                 }
-                if constexpr (WT == MK_W_BF16 || WT == MK_W_FP16) {
-                    if (ok && t.op == OP_FFN) {
-                        bar_consumers();  // every SwiGLU output of the task is in shared memory
-                        ffn_down<WT>(c, t, t.layer);
-                    }
+                if (ok && t.op == OP_FFN) {
+                    bar_consumers();  // every SwiGLU output of the task is in shared memory
+                    ffn_down<WT>(c, t, t.layer);
                 }
             } else {
                 ok = t.op == OP_ATTN ? attn_task<HD>(c, t, tid_, s) : wait_counters(c, t, tid_, s);

@@ -58,7 +58,8 @@ enum {
     MK_W_BF16 = 0,      /* bf16 rows                                                      */
     MK_W_FP16 = 1,      /* IEEE fp16 rows                                                 */
     MK_W_INT8_ROW = 2,  /* int8, one fp16 scale per output row (W8A16)                     */
-    MK_W_INT4_G128 = 3  /* int4 nibbles, one fp16 scale per 128 k of a row (W4A16)         */
+    MK_W_INT4_G128 = 3, /* int4 nibbles, one fp16 scale per 128 k of a row (W4A16)         */
+    MK_W_FP8_E4M3 = 4   /* FP8 E4M3 codes (OCP format), one fp16 scale per 128 k of a row  */
 };
 
 /* Model variants the contract rejects (mk_model_desc.flags). */
@@ -74,7 +75,8 @@ enum {
  * d_model % 128 == 0, d_ffn % 128 == 0, n_q_heads * head_dim % 128 == 0,
  * vocab < 131072, max_seq >= 1.  base_dtype (MK_W_BF16 or MK_W_FP16) is the
  * storage type of the embedding, the norm gains and the packer's source rows;
- * wdtype may be base_dtype, MK_W_INT8_ROW or MK_W_INT4_G128 (bf16 source). */
+ * wdtype may be base_dtype, MK_W_INT8_ROW, MK_W_INT4_G128 or MK_W_FP8_E4M3
+ * (bf16 source). */
 typedef struct {
     int32_t n_layers, d_model, n_q_heads, n_kv_heads, head_dim, d_ffn, vocab;
     float rms_eps, rope_theta;
@@ -108,10 +110,13 @@ typedef struct {
  * [gate/up rows interleaved: gate_j, up_j] [down], then the LM head, the
  * norm gains and the embedding.  Quantised rows carry their fp16 scales after
  * the codes; every row starts on a 16-byte boundary.
- * Down projection: rows [d_model][d_ffn] for quantised weights; for 16-bit
- * weights with d_model / 256 in {1, 2, 4, 8, 10, 12, 16} (the fused FFN) it is
- * stored in column blocks of 8: block b holds, for r = 0 .. d_model-1, the
- * 16 bytes Wdown[r][8b .. 8b+8), at offset (b * d_model + r) * 16. */
+ * Down projection, when the FFN is fused (d_model / 256 in {1, 2, 4, 8, 16},
+ * and also 10 and 12 for 16-bit weights): column blocks of 16 bytes, block b
+ * holding for r = 0 .. d_model-1 the codes of Wdown[r][BU b .. BU (b+1)) at
+ * offset (b * d_model + r) * 16, BU = 8 (bf16/fp16), 16 (int8) or 32 (int4,
+ * even k in the low nibble); quantised blocks are followed by their fp16
+ * scales, [d_model] (int8, one per row) or [d_ffn / 128][d_model] (int4).
+ * Otherwise rows [d_model][d_ffn] like the other tensors. */
 enum {
     MK_T_EMBED = 0, MK_T_LM_HEAD = 1, MK_T_FINAL_NORM = 2, MK_T_ATTN_NORM = 3, MK_T_FFN_NORM = 4,
     MK_T_WQ = 5, MK_T_WK = 6, MK_T_WV = 7, MK_T_WO = 8, MK_T_WGATE = 9, MK_T_WUP = 10,
@@ -146,6 +151,11 @@ mk_status mk_tensor_layout(const mk_model_desc* desc, int32_t tensor, int32_t la
  * q = clamp(round_half_even(fp32(w)/fp32(s)), +-127 or +-7), s == 0 -> q == 0. */
 mk_status mk_quantize_int8(const float* w, int64_t n, int64_t k, int8_t* q, uint16_t* s16);
 mk_status mk_quantize_int4(const float* w, int64_t n, int64_t k, int8_t* q, uint16_t* s16);
+/* FP8 E4M3 block-scaled (Netra Kernel summary, "TL;DR": FP8 ops): per 128 k,
+ * s = fp16(fp32(max|w|) / 448); q = the E4M3 code nearest to fp32(w) /
+ * fp32(s) (ties to the even code, magnitudes clamped to 448), s == 0 -> 0;
+ * q: uint8 codes [n][k], s16 [n][k/128]. */
+mk_status mk_quantize_fp8(const float* w, int64_t n, int64_t k, uint8_t* q, uint16_t* s16);
 
 /* ------------------------------------------------------------------ sizes */
 /* KV cache bytes: bf16 [n_layers][2 (K,V)][n_kv_heads][max_seq][head_dim]. */

@@ -23,7 +23,7 @@ class Workload:
     seed: int
     prompt_len: int
     decode_steps: int
-    wdtype: str = "bf16"          # storage type of the GEMV weights: bf16 | fp16 | int8 | int4
+    wdtype: str = "bf16"          # storage type of the GEMV weights: bf16 | fp16 | int8 | int4 | fp8
     rms_eps: float = 1e-5
     rope_theta: float = 1e4
     base_dtype: str = "bf16"      # storage type the random weights are drawn into
@@ -60,6 +60,9 @@ WORKLOADS = {
                               prompt_len=128, decode_steps=256, wdtype="int8"),
     "llama-1b-int4": Workload("llama-1b-int4", 16, 2048, 32, 8, 64, 8192, 32000, seed=1,
                               prompt_len=128, decode_steps=256, wdtype="int4"),
+    # The same model with FP8 E4M3 GEMV weights, one fp16 scale per 128 k.
+    "llama-1b-fp8": Workload("llama-1b-fp8", 16, 2048, 32, 8, 64, 8192, 32000, seed=1,
+                             prompt_len=128, decode_steps=256, wdtype="fp8"),
     # Llama-3-8B shape, 8192-token prefilled KV cache, decode 128.
     "llama3-8b-8k": Workload("llama3-8b-8k", 32, 4096, 32, 8, 128, 14336, 128256, seed=4,
                              prompt_len=8192, decode_steps=128, rope_theta=5e5),

@@ -70,9 +70,16 @@ def test_quantisers_match_oracle_bytes(mk):
     q, s = mk.mk_quantize_int4(w)
     qo, so = Q.quantize_int4_g128(w)
     assert np.array_equal(q, qo) and np.array_equal(s.view(np.uint16), so.view(np.uint16))
+    # FP8 E4M3: the C++ round-to-nearest-even from the format definition and the
+    # oracle's nearest-value search agree byte for byte, ties and clamping included
+    q, s = mk.mk_quantize_fp8(w)
+    qo, so = Q.quantize_fp8_g128(w)
+    assert np.array_equal(q, qo) and np.array_equal(s.view(np.uint16), so.view(np.uint16))
+    wide = (rng.standard_normal((8, 256)) * 50).astype(np.float32)  # many scales, ties by chance
+    assert np.array_equal(mk.mk_quantize_fp8(wide)[0], Q.quantize_fp8_g128(wide)[0])
 
 
-@pytest.mark.parametrize("wd", ["int8", "int4"])
+@pytest.mark.parametrize("wd", ["int8", "int4", "fp8"])
 def test_packed_quantised_rows_match_oracle(mk, wd):
     w = synthetic.get_workload("tiny").with_(wdtype=wd)
     weights = synthetic.generate_weights(w)
@@ -82,11 +89,34 @@ def test_packed_quantised_rows_match_oracle(mk, wd):
         src = synthetic.bits_to_f32(weights[f"l1.{name}"], "bf16")
         lay = mk.mk_tensor_layout(desc, tid, 1)
         K = src.shape[1]
+        if lay["stride"] == 0:  # the fused FFN's down projection: column blocks, then the scales
+            assert name == "wdown"
+            n, BU = src.shape[0], 32 if wd == "int4" else 16
+            if wd == "int8":
+                q, s = Q.quantize_int8_rows(src)
+                codes = q.view(np.uint8).reshape(n, K // BU, 16)
+                scales = s.view(np.uint8)
+            elif wd == "fp8":
+                q, s = Q.quantize_fp8_g128(src)
+                codes = q.reshape(n, K // BU, 16)
+                scales = np.ascontiguousarray(s.T).view(np.uint8).reshape(-1)
+            else:
+                q, s = Q.quantize_int4_g128(src)
+                codes = Q.pack_int4_nibbles(q).reshape(n, K // BU, 16)
+                scales = np.ascontiguousarray(s.T).view(np.uint8).reshape(-1)
+            nb = n * K * 16 // BU
+            region = blob[lay["offset"]:lay["offset"] + nb].reshape(K // BU, n, 16)
+            assert np.array_equal(region, codes.transpose(1, 0, 2)), (wd, name)
+            assert np.array_equal(blob[lay["offset"] + nb:lay["offset"] + nb + scales.size], scales.reshape(-1))
+            continue
         for r in (0, 1, src.shape[0] - 1):
             row = blob[lay["offset"] + (lay["first_row"] + r * lay["row_step"]) * lay["stride"]:][:lay["stride"]]
             if wd == "int8":
                 q, s = Q.quantize_int8_rows(src[r:r + 1])
                 want = np.concatenate([q.view(np.uint8)[0], s.view(np.uint8)])
+            elif wd == "fp8":
+                q, s = Q.quantize_fp8_g128(src[r:r + 1])
+                want = np.concatenate([q[0], s.view(np.uint8)[0]])
             else:
                 q, s = Q.quantize_int4_g128(src[r:r + 1])
                 want = np.concatenate([Q.pack_int4_nibbles(q)[0], s.view(np.uint8)[0]])
@@ -112,7 +142,8 @@ def test_packed_down_column_blocks(mk):
 @pytest.mark.parametrize("name,sms,chunks", [("tiny", 152, 0), ("tiny", 7, 3), ("tiny", 1, 1), ("tiny", 2, 4),
                                              ("tiny", 152, 64),
                                              ("llama-1b", 152, 0), ("llama-1b-int8", 152, 0),
-                                             ("llama-1b-int4", 64, 2), ("llama-2b-fp16", 152, 0)])
+                                             ("llama-1b-int4", 64, 2), ("llama-1b-fp8", 152, 0),
+                                             ("llama-2b-fp16", 152, 0)])
 def test_validator_accepts_real_lowerings(mk, name, sms, chunks):
     w = synthetic.get_workload(name)
     st, why = mk.mk_validate_schedule(mk.make_desc(w), mk.make_config(sms=sms, attn_chunks=chunks), sms)

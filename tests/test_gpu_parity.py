@@ -48,7 +48,7 @@ def weights_for(name):
 
 
 def oracle_model(w, weights):
-    if w.wdtype in ("int8", "int4"):
+    if w.wdtype in ("int8", "int4", "fp8"):
         deq, _ = Q.quantised_model_weights(w, weights, w.wdtype)
         return L.Model(w, weights, w.base_dtype, dequantised=deq)
     return L.Model(w, weights, w.base_dtype)
@@ -73,7 +73,11 @@ def check_logits(gpu, ref, tol=TOL, label=""):
 
 
 # ------------------------------------------------------------------ dequantisation
-@pytest.mark.parametrize("wd", ["int8", "int4"])
+QUANTISE = {"int8": (Q.quantize_int8_rows, Q.dequant_int8), "int4": (Q.quantize_int4_g128, Q.dequant_int4),
+            "fp8": (Q.quantize_fp8_g128, Q.dequant_fp8)}
+
+
+@pytest.mark.parametrize("wd", ["int8", "int4", "fp8"])
 def test_device_dequant_bit_exact(mk, wd):
     torch = _torch()
     w = synthetic.get_workload("tiny").with_(wdtype=wd)
@@ -84,13 +88,13 @@ def test_device_dequant_bit_exact(mk, wd):
     for name, tid in mk.GEMV_SOURCES:
         for layer in range(w.n_layers):
             src = synthetic.bits_to_f32(weights[f"l{layer}.{name}"], "bf16")
-            q, s = (Q.quantize_int8_rows if wd == "int8" else Q.quantize_int4_g128)(src)
-            want = Q.dequant_int8(q, s) if wd == "int8" else Q.dequant_int4(q, s)
+            q, s = QUANTISE[wd][0](src)
+            want = QUANTISE[wd][1](q, s)
             got = mk.debug_dequant(desc, dev, tid, layer, *src.shape).cpu().numpy()
             assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), (name, layer)
     src = synthetic.bits_to_f32(weights["lm_head"], "bf16")
-    q, s = (Q.quantize_int8_rows if wd == "int8" else Q.quantize_int4_g128)(src)
-    want = Q.dequant_int8(q, s) if wd == "int8" else Q.dequant_int4(q, s)
+    q, s = QUANTISE[wd][0](src)
+    want = QUANTISE[wd][1](q, s)
     got = mk.debug_dequant(desc, dev, mk.MK_T_LM_HEAD, 0, *src.shape).cpu().numpy()
     assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
 
@@ -201,13 +205,44 @@ def _full_size(mk, name, n_forced, sms=0, prompt_len=None, workload=None, cfg=No
     return lg, ref, ids
 
 
-@pytest.mark.parametrize("name", ["llama-1b", "llama-1b-int8", "llama-1b-int4"])
+@pytest.mark.parametrize("name", ["llama-1b", "llama-1b-int8", "llama-1b-int4", "llama-1b-fp8"])
 def test_1b_teacher_forced(mk, name):
     # every step of the bench's timed window: positions 127..382, split-KV
     # chunks growing from ~22 to 64 positions (two tiles and the next-tile prefetch)
     w = synthetic.get_workload(name)
     lg, ref, ids = _full_size(mk, name, w.decode_steps)
     check_logits(lg, ref, label=name)
+    assert np.array_equal(ids, lg.argmax(axis=1))
+
+
+@pytest.mark.parametrize("wd", ["int8", "int4", "fp8"])
+@pytest.mark.parametrize("sms", [0, 7])
+def test_tiny_quantised_teacher_forced(mk, wd, sms):
+    # the fused FFN with quantised codes: one 512-byte line per column block
+    w = synthetic.get_workload("tiny").with_(wdtype=wd)
+    weights = weights_for("tiny")
+    desc = mk.make_desc(w)
+    dec = mk.Decoder(desc, mk.pack_model(desc, weights), mk.make_config(sms=sms))
+    ir = mk.mk_build_ir(desc, mk.make_config(sms=sms), dec.launch_info()["ctas"])
+    assert "ffn" in {mk.OPS[t["op"]] for t in ir["tasks"]}
+    prompt = synthetic.generate_prompt(w)
+    om = oracle_model(w, weights)
+    ids_o, logits_o = L.greedy(om, prompt, w.decode_steps)
+    dec.prefill(prompt)
+    lg, ids = dec.teacher_forced(np.concatenate([prompt[-1:], ids_o[:-1]]).astype(np.int32))
+    check_logits(lg, logits_o, label=f"tiny-{wd}-sms{sms}")
+    assert np.array_equal(ids, lg.argmax(axis=1))
+    dec.close()
+
+
+@pytest.mark.parametrize("wd", ["int8", "int4", "fp8"])
+def test_8b_shape_quantised_teacher_forced(mk, wd):
+    # d_model 4096: 16 lines per column block, i.e. a block spans 2 (int8) or
+    # 4 (int4) ring batches; the int4 group scales change every 4 blocks
+    w = synthetic.get_workload("llama3-8b-8k").with_(n_layers=2, prompt_len=96, decode_steps=128, wdtype=wd,
+                                                     vocab=32000)
+    lg, ref, ids = _full_size(mk, w.name, w.decode_steps, workload=w)
+    check_logits(lg, ref, label=f"8b-shape-2L-{wd}")
     assert np.array_equal(ids, lg.argmax(axis=1))
 
 
