@@ -109,6 +109,7 @@ struct MergeScratch {
 
 struct Shared {
     float norm[NW];                 // RMSNorm sum of squares
+    float nmax[NW];                 // per-warp max |input| of an integer-dot task
     float gpart[NW][2][8][NW];      // [group][parity][row][warp]: partial sums of shared rows
     unsigned long long keys[NW];    // per-warp LM argmax keys
     MergeScratch mg;
@@ -177,6 +178,7 @@ struct Ctx {
     int rs;             // ring slot of the next batch to compute
     float* xs;          // the task's input vector (K floats, shared memory)
     float rstd;         // scale of xs applied when the fragments are loaded (RMSNorm)
+    float xscale;       // step D of the input planes of an integer-dot task
     int tid, lane, warp;
     bool abort;
     int deferred;       // batches of this task that issued no copy: issued after the signal
@@ -400,6 +402,128 @@ static __device__ __forceinline__ int step_token(const VmParams& p, int step) {
     return tok;
 }
 
+// ------------------------------------------------------------------ integer dot products
+// int8 and int4 rows multiply their codes in 32-bit integers.  The GEMV input
+// is held as a fixed-point copy X = rint(x / D), D a power of two with
+// max|x| / D in [2^21, 2^22), stored as three byte planes: byte 0 and byte 1
+// of X (unsigned) and byte 2 (signed), so that X = b2 2^16 + b1 2^8 + b0
+// exactly.  X keeps 24 significant bits against max|x|, as many as fp32 keeps
+// for the largest elements.  A 16-byte chunk of codes then takes dp4a
+// instructions against the planes: int8 codes are signed bytes as stored, and
+// each int4 nibble, masked into the high half of its byte, is the signed byte
+// 16 q.  Every product and sum is exact, and one fp32 combination per row
+// (int8) or per chunk (int4, whose group scale changes from chunk to chunk)
+// rebuilds the dot product.
+template <int WT>
+__host__ __device__ constexpr bool idot_type() { return WT == MK_W_INT8_ROW || WT == MK_W_INT4_G128; }
+constexpr int PIECE_IT = 2;  // groups of 8 inputs a thread holds while the step D is found: K <= 8 NT PIECE_IT
+
+// Byte offset of element k inside a plane.  int8 chunks take k in order.  An
+// int4 code word holds 8 k with the even k in the low nibbles, so each 8 k of
+// an int4 plane are stored as [k0 k2 k4 k6 | k1 k3 k5 k7]: the even word
+// pairs with the low nibbles of the code word, the odd word with the high.
+template <int WT>
+__device__ __forceinline__ int plane_pos(int k) {
+    if constexpr (WT == MK_W_INT4_G128) return (k & ~7) | ((k & 1) << 2) | ((k >> 1) & 3);
+    else return k;
+}
+__device__ __forceinline__ int dp4a_su(uint32_t a, uint32_t b, int c) {  // signed bytes of a, unsigned of b
+    int d;
+    asm("dp4a.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int c) {  // signed bytes of both
+    int d;
+    asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+// 1 / D for a vector whose largest magnitude is m (1 when m is 0).  D = 2^E
+// with m / D in [2^21, 2^22), so |X| <= 2^22 and byte 2 of X is X >> 16.
+__device__ __forceinline__ float fixed_inv_step(float m) {
+    if (!(m > 0.f)) return 1.f;
+    const int e = (int)((__float_as_uint(m) >> 23) & 0xFFu) - 127;  // floor(log2 m) for normal m
+    const int E = max(-126, min(e - 21, 126));
+    return __uint_as_float((uint32_t)(127 - E) << 23);
+}
+// Planes of four values: P[p] holds byte p of a, b, c, d (in that order).
+__device__ __forceinline__ void planes4(uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint32_t (&P)[3]) {
+    const uint32_t ab_lo = __byte_perm(a, b, 0x5140), cd_lo = __byte_perm(c, d, 0x5140);  // [a0 b0 a1 b1]
+    const uint32_t ab_hi = __byte_perm(a, b, 0x7362), cd_hi = __byte_perm(c, d, 0x7362);  // [a2 b2 a3 b3]
+    P[0] = __byte_perm(ab_lo, cd_lo, 0x5410);
+    P[1] = __byte_perm(ab_lo, cd_lo, 0x7632);
+    P[2] = __byte_perm(ab_hi, cd_hi, 0x5410);
+}
+// Stores the planes of elements 8g .. 8g+7 (X: their fixed-point values) of a
+// K-element vector whose plane p starts at pl + p K.
+template <int WT>
+__device__ __forceinline__ void put_planes8(uint8_t* pl, int K, int g, const int (&X)[8]) {
+    uint32_t A[3], B[3];
+    if constexpr (WT == MK_W_INT4_G128) {
+        planes4(X[0], X[2], X[4], X[6], A);
+        planes4(X[1], X[3], X[5], X[7], B);
+    } else {
+        planes4(X[0], X[1], X[2], X[3], A);
+        planes4(X[4], X[5], X[6], X[7], B);
+    }
+#pragma unroll
+    for (int p = 0; p < 3; ++p) *(uint2*)(pl + (size_t)p * K + 8 * g) = make_uint2(A[p], B[p]);
+}
+// sum over a chunk pair of 4 words of 4-byte products, as an fp32 value of
+// the fixed-point sum: S0 + 2^8 S1 + 2^16 S2
+__device__ __forceinline__ float planes_combine(int s0, int s1, int s2) {
+    return fmaf((float)s2, 65536.f, fmaf((float)s1, 256.f, (float)s0));
+}
+// The lane's partial dot product of one row, in units of D: xp holds the
+// planes of the lane's chunks L + S*j (int8: one uint4 per plane; int4: two,
+// plane p at xp[j][2p], xp[j][2p + 1]).  int4 chunks carry their group
+// scale in sc[j]; int8 takes its row scale after the warp reduction.
+template <int WT, int NG>
+__device__ __forceinline__ float chunks_idot(const uint4 (&w)[NG], const float (&sc)[NG],
+                                             const uint4 (&xp)[NG][WT == MK_W_INT4_G128 ? 6 : 3]) {
+    if constexpr (WT == MK_W_INT8_ROW) {
+        int s[2][3] = {{0, 0, 0}, {0, 0, 0}};  // two sets: shorter dependency chains
+#pragma unroll
+        for (int j = 0; j < NG; ++j) {
+            const uint32_t wv[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
+            const uint32_t p0[4] = {xp[j][0].x, xp[j][0].y, xp[j][0].z, xp[j][0].w};
+            const uint32_t p1[4] = {xp[j][1].x, xp[j][1].y, xp[j][1].z, xp[j][1].w};
+            const uint32_t p2[4] = {xp[j][2].x, xp[j][2].y, xp[j][2].z, xp[j][2].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                s[j & 1][0] = dp4a_su(wv[i], p0[i], s[j & 1][0]);
+                s[j & 1][1] = dp4a_su(wv[i], p1[i], s[j & 1][1]);
+                s[j & 1][2] = dp4a_ss(wv[i], p2[i], s[j & 1][2]);
+            }
+        }
+        return planes_combine(s[0][0] + s[1][0], s[0][1] + s[1][1], s[0][2] + s[1][2]);
+    } else {  // int4: lo = 16 q of the even k, hi = 16 q of the odd k
+        float acc = 0.f;
+#pragma unroll
+        for (int j = 0; j < NG; ++j) {
+            const uint32_t wv[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
+            int s[3] = {0, 0, 0};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t lo = (wv[i] << 4) & 0xF0F0F0F0u, hi = wv[i] & 0xF0F0F0F0u;
+#pragma unroll
+                for (int p = 0; p < 3; ++p) {
+                    const uint4 A = xp[j][2 * p + (i >> 1)];
+                    const uint32_t ev = (i & 1) ? A.z : A.x, od = (i & 1) ? A.w : A.y;
+                    if (p < 2) {
+                        s[p] = dp4a_su(lo, ev, s[p]);
+                        s[p] = dp4a_su(hi, od, s[p]);
+                    } else {
+                        s[p] = dp4a_ss(lo, ev, s[p]);
+                        s[p] = dp4a_ss(hi, od, s[p]);
+                    }
+                }
+            }
+            acc = fmaf(sc[j], planes_combine(s[0], s[1], s[2]), acc);
+        }
+        return acc * 0.0625f;
+    }
+}
+
 // ------------------------------------------------------------------ GEMV inputs
 // Position (in floats) of float4 unit u of a K-float input vector in c.xs.
 // Unit u belongs to the 16-byte weight chunk u >> lq4 of a row (2^lq4 units
@@ -410,18 +534,51 @@ __device__ __forceinline__ int xs_pos(int u, int K, int lq4) {
     const int nch = K >> (lq4 + 2);
     return ((u & ((1 << lq4) - 1)) * nch + (u >> lq4)) * 4;
 }
-// Each prologue writes the task's input vector (K floats) into c.xs with all
-// consumer threads and ends with a consumer barrier.
+// Each prologue writes the task's input vector into c.xs with all consumer
+// threads and ends with a consumer barrier: K floats in planes (IW = 0), or
+// for an integer-dot task (IW = the weight type) the three byte planes of its
+// fixed-point copy and the step D in c.xscale.  An integer-dot prologue keeps
+// its inputs in registers (groups 8g .. 8g+7 for g = tid + it NT) until the
+// block-wide max |x| fixes D.
+
+// The planes of the kept inputs times f0, given m = max |kept input|.
+template <int IW>
+__device__ __forceinline__ void write_planes(Ctx& c, const float (&keep)[PIECE_IT][8], int K, float f0, float m) {
+    const float inv = fixed_inv_step(m * f0);
+    const float f = f0 * inv;
+#pragma unroll
+    for (int it = 0; it < PIECE_IT; ++it) {
+        const int g = c.tid + it * NT;
+        if (g < (K >> 3)) {
+            int X[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) X[i] = __float2int_rn(keep[it][i] * f);
+            put_planes8<IW>((uint8_t*)c.xs, K, g, X);
+        }
+    }
+    c.xscale = 1.f / inv;  // a power of two: exact
+    bar_consumers();
+}
+// Block-wide max of the threads' m (one consumer barrier); every thread gets it.
+__device__ __forceinline__ float block_max(Ctx& c, float m) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if (c.lane == 0) c.sh->nmax[c.warp] = m;
+    bar_consumers();
+    float r = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) r = fmaxf(r, c.sh->nmax[w]);
+    return r;
+}
 
 // RMSNorm(x) * gain, x from the residual stream or (layer 0) an embedding row.
 // The gain loads are issued together with the x loads (one memory round trip).
-template <int BASE>
+template <int BASE, int IW>
 static __device__ __forceinline__ void prologue_rmsnorm(Ctx& c, const float* x, const uint16_t* emb_row, const uint16_t* gain, int K,
                                  float eps, int lq4) {
-    float ss = 0.f;
-    for (int g = c.tid; g < (K >> 3); g += NT) {
+    float ss = 0.f, mx = 0.f;
+    auto load8 = [&](int g, float (&v)[8]) {  // v = x[8g, 8g + 8) * gain, ss += x^2
         const uint4 graw = __ldg((const uint4*)(gain + 8 * g));
-        float v[8];
         if (emb_row) {
             const uint4 raw = __ldg((const uint4*)(emb_row + 8 * g));
             const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
@@ -440,74 +597,124 @@ static __device__ __forceinline__ void prologue_rmsnorm(Ctx& c, const float* x, 
         for (int i = 0; i < 8; ++i) ss = fmaf(v[i], v[i], ss);
         const uint32_t gv[4] = {graw.x, graw.y, graw.z, graw.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {  // x * gain now; the common 1/rms factor is applied below
+        for (int i = 0; i < 4; ++i) {  // x * gain now; the common 1/rms factor is applied later
             v[2 * i] *= base_to_f32<BASE>(gv[i] & 0xFFFFu);
             v[2 * i + 1] *= base_to_f32<BASE>(gv[i] >> 16);
         }
-        *(float4*)(c.xs + xs_pos(2 * g, K, lq4)) = make_float4(v[0], v[1], v[2], v[3]);
-        *(float4*)(c.xs + xs_pos(2 * g + 1, K, lq4)) = make_float4(v[4], v[5], v[6], v[7]);
+    };
+    float keep[IW ? PIECE_IT : 1][8];
+    if constexpr (IW == 0) {
+        for (int g = c.tid; g < (K >> 3); g += NT) {
+            float v[8];
+            load8(g, v);
+            *(float4*)(c.xs + xs_pos(2 * g, K, lq4)) = make_float4(v[0], v[1], v[2], v[3]);
+            *(float4*)(c.xs + xs_pos(2 * g + 1, K, lq4)) = make_float4(v[4], v[5], v[6], v[7]);
+        }
+    } else {
+#pragma unroll
+        for (int it = 0; it < PIECE_IT; ++it) {
+            const int g = c.tid + it * NT;
+            if (g < (K >> 3)) {
+                load8(g, keep[it]);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx = fmaxf(mx, fabsf(keep[it][i]));
+            }
+        }
     }
 #pragma unroll
-    for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
-    if (c.lane == 0) c.sh->norm[c.warp] = ss;
+    for (int o = 16; o; o >>= 1) {
+        ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+        if constexpr (IW != 0) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+    }
+    if (c.lane == 0) {
+        c.sh->norm[c.warp] = ss;
+        if constexpr (IW != 0) c.sh->nmax[c.warp] = mx;
+    }
     bar_consumers();
     float tot = 0.f;
 #pragma unroll
     for (int w = 0; w < NW; ++w) tot += c.sh->norm[w];
     c.rstd = rsqrtf(tot / (float)K + eps);  // applied to the fragments by gemv_rows
+    if constexpr (IW != 0) {
+        float m = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) m = fmaxf(m, c.sh->nmax[w]);
+        write_planes<IW>(c, keep, K, c.rstd, m);
+    }
 }
 
 // Merge the split-KV partials of every query head into the attention output:
 // o = sum_c e^(m_c - M) l_c a_c / sum_c e^(m_c - M) l_c, M = max_c m_c, where
 // a_c is chunk c's output normalised by its own sum l_c.
-static __device__ __forceinline__ void prologue_attention(Ctx& c, int lq4) {
-    const VmParams& p = *c.p;
+// One pass with a running maximum: each thread reads, for its 8 outputs,
+// every chunk's (max, sum) and partial accumulators itself (up to 8 chunks'
+// loads in flight at once) and rescales as the maximum grows, so the merge
+// costs about one round trip to L2 and no block barrier.
+__device__ __forceinline__ void merge8(const VmParams& p, int g, float (&o)[8]) {
     const int C = p.C;
-    // One pass with a running maximum: each thread reads, for its 8 outputs,
-    // every chunk's (max, sum) and partial accumulators itself (up to 8
-    // chunks' loads in flight at once) and rescales as the maximum grows, so
-    // the merge costs about one round trip to L2 and no block barrier.
-    for (int g = c.tid; g < (p.q_dim >> 3); g += NT) {
-        const int hq = (8 * g) / p.hd, d0 = (8 * g) % p.hd;
-        const int cp = blockIdx.x % PART_COPIES;  // this CTA's copy of the partials
-        const float* ml = p.part_ml + ((size_t)cp * p.Hq + hq) * C * 2;
-        const uint16_t* base = p.part_acc + ((size_t)cp * p.Hq + hq) * C * p.hd + d0;
-        float M = -3.0e38f, den = 0.f;
-        float o[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        for (int c0 = 0; c0 < C; c0 += 8) {
-            float mm[8], ll[8];
-            uint4 a[8];  // eight fp16 accumulators
+    const int hq = (8 * g) / p.hd, d0 = (8 * g) % p.hd;
+    const int cp = blockIdx.x % PART_COPIES;  // this CTA's copy of the partials
+    const float* ml = p.part_ml + ((size_t)cp * p.Hq + hq) * C * 2;
+    const uint16_t* base = p.part_acc + ((size_t)cp * p.Hq + hq) * C * p.hd + d0;
+    float M = -3.0e38f, den = 0.f;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int ch = min(c0 + k, C - 1);
-                const float2 v = __ldcg((const float2*)(ml + 2 * ch));  // (max, sum) in one load
-                mm[k] = v.x;
-                ll[k] = v.y;
-                a[k] = __ldcg((const uint4*)(base + (size_t)ch * p.hd));
-            }
+    for (int i = 0; i < 8; ++i) o[i] = 0.f;
+    for (int c0 = 0; c0 < C; c0 += 8) {
+        float mm[8], ll[8];
+        uint4 a[8];  // eight fp16 accumulators
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                if (c0 + k >= C) break;
-                const float Mn = fmaxf(M, mm[k]);
-                const float r = expf(M - Mn), w = expf(mm[k] - Mn);
-                M = Mn;
-                const float wl = w * ll[k];  // the chunk's weight: its partials are acc / l
-                den = fmaf(den, r, wl);
-                const uint32_t h4[4] = {a[k].x, a[k].y, a[k].z, a[k].w};
+        for (int k = 0; k < 8; ++k) {
+            const int ch = min(c0 + k, C - 1);
+            const float2 v = __ldcg((const float2*)(ml + 2 * ch));  // (max, sum) in one load
+            mm[k] = v.x;
+            ll[k] = v.y;
+            a[k] = __ldcg((const uint4*)(base + (size_t)ch * p.hd));
+        }
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    o[2 * i] = fmaf(o[2 * i], r, wl * half_bits_to_f32(h4[i] & 0xFFFFu));
-                    o[2 * i + 1] = fmaf(o[2 * i + 1], r, wl * half_bits_to_f32(h4[i] >> 16));
-                }
+        for (int k = 0; k < 8; ++k) {
+            if (c0 + k >= C) break;
+            const float Mn = fmaxf(M, mm[k]);
+            const float r = expf(M - Mn), w = expf(mm[k] - Mn);
+            M = Mn;
+            const float wl = w * ll[k];  // the chunk's weight: its partials are acc / l
+            den = fmaf(den, r, wl);
+            const uint32_t h4[4] = {a[k].x, a[k].y, a[k].z, a[k].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                o[2 * i] = fmaf(o[2 * i], r, wl * half_bits_to_f32(h4[i] & 0xFFFFu));
+                o[2 * i + 1] = fmaf(o[2 * i + 1], r, wl * half_bits_to_f32(h4[i] >> 16));
             }
         }
-        const float inv = 1.f / den;
-        *(float4*)(c.xs + xs_pos(2 * g, p.q_dim, lq4)) = make_float4(o[0] * inv, o[1] * inv, o[2] * inv, o[3] * inv);
-        *(float4*)(c.xs + xs_pos(2 * g + 1, p.q_dim, lq4)) =
-            make_float4(o[4] * inv, o[5] * inv, o[6] * inv, o[7] * inv);
     }
+    const float inv = 1.f / den;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] *= inv;
+}
+template <int IW>
+static __device__ __forceinline__ void prologue_attention(Ctx& c, int lq4) {
+    const VmParams& p = *c.p;
     c.rstd = 1.f;
-    bar_consumers();
+    if constexpr (IW == 0) {
+        for (int g = c.tid; g < (p.q_dim >> 3); g += NT) {
+            float o[8];
+            merge8(p, g, o);
+            *(float4*)(c.xs + xs_pos(2 * g, p.q_dim, lq4)) = make_float4(o[0], o[1], o[2], o[3]);
+            *(float4*)(c.xs + xs_pos(2 * g + 1, p.q_dim, lq4)) = make_float4(o[4], o[5], o[6], o[7]);
+        }
+        bar_consumers();
+    } else {
+        float keep[PIECE_IT][8], mx = 0.f;
+#pragma unroll
+        for (int it = 0; it < PIECE_IT; ++it) {
+            const int g = c.tid + it * NT;
+            if (g < (p.q_dim >> 3)) {
+                merge8(p, g, keep[it]);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx = fmaxf(mx, fabsf(keep[it][i]));
+            }
+        }
+        write_planes<IW>(c, keep, p.q_dim, 1.f, block_max(c, mx));
+    }
 }
 
 // OP_MERGE: the split-KV merge of KV group g's query heads, written once to
@@ -555,13 +762,30 @@ static __device__ __forceinline__ void merge_task(Ctx& c, const TaskRec& t) {
 
 // O prologue when merge tasks ran: the merged attention output, copied from
 // att into c.xs (planes).
+template <int IW>
 static __device__ __forceinline__ void prologue_att_copy(Ctx& c, int lq4) {
     const VmParams& p = *c.p;
-    for (int u = c.tid; u < (p.q_dim >> 2); u += NT)
-        *(float4*)(c.xs + xs_pos(u, p.q_dim, lq4)) =
-            __ldcg((const float4*)(p.att + (size_t)(blockIdx.x % PART_COPIES) * p.q_dim + 4 * u));
+    const float* att = p.att + (size_t)(blockIdx.x % PART_COPIES) * p.q_dim;
     c.rstd = 1.f;
-    bar_consumers();
+    if constexpr (IW == 0) {
+        for (int u = c.tid; u < (p.q_dim >> 2); u += NT)
+            *(float4*)(c.xs + xs_pos(u, p.q_dim, lq4)) = __ldcg((const float4*)(att + 4 * u));
+        bar_consumers();
+    } else {
+        float keep[PIECE_IT][8], mx = 0.f;
+#pragma unroll
+        for (int it = 0; it < PIECE_IT; ++it) {
+            const int g = c.tid + it * NT;
+            if (g < (p.q_dim >> 3)) {
+                const float4 a = __ldcg((const float4*)(att + 8 * g)), b = __ldcg((const float4*)(att + 8 * g + 4));
+                keep[it][0] = a.x; keep[it][1] = a.y; keep[it][2] = a.z; keep[it][3] = a.w;
+                keep[it][4] = b.x; keep[it][5] = b.y; keep[it][6] = b.z; keep[it][7] = b.w;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx = fmaxf(mx, fabsf(keep[it][i]));
+            }
+        }
+        write_planes<IW>(c, keep, p.q_dim, 1.f, block_max(c, mx));
+    }
 }
 
 // ------------------------------------------------------------------ GEMV rows
@@ -959,10 +1183,154 @@ __device__ __forceinline__ void ffn_cols16(Ctx& c, const TaskRec& t, int layer) 
     for (int m = 0; m < NL; ++m) red_add_f32(xo + 32 * m, sum2(acc[m]));
 }
 
+// int8 and int4 codes: integer dot products against byte planes of the
+// task's SwiGLU outputs (a fixed-point copy with step D_h, built here in the
+// input region, which every row batch of the task has finished with).  Each
+// lane keeps one int32 sum per line and plane; int8 combines them once per
+// row, int4 at each change of 128-unit group (its scale changes there).
+static_assert(3 * FFN_MAX_UNITS <= sizeof(AttnScratch), "planes of an OP_FFN task's SwiGLU outputs in the input region");
+template <int WT, int NL>
+__device__ __forceinline__ void ffn_cols_idot(Ctx& c, const TaskRec& t, int layer) {
+    const VmParams& p = *c.p;
+    constexpr int NB = ring_slots<WT>();
+    constexpr int BU = ffn_block(WT), SL = ffn_slot_lines(WT);
+    constexpr int CB = WT == MK_W_INT4_G128 ? 2 : 1;  // 16-byte words of a block per plane
+    const int kc = t.nrows / (2 * BU);
+    const int units = kc * BU;
+    const float* hs = ffn_h(c);
+    float mx = 0.f;
+    for (int u = c.tid; u < units; u += NT) mx = fmaxf(mx, fabsf(hs[u]));
+    const float inv = fixed_inv_step(block_max(c, mx));
+    uint8_t* hp = (uint8_t*)c.xs;
+    for (int u = c.tid; u < units; u += NT) {
+        const int X = __float2int_rn(hs[u] * inv);
+        const int q = plane_pos<WT>(u);
+        hp[q] = (uint8_t)X;
+        hp[units + q] = (uint8_t)(X >> 8);
+        hp[2 * units + q] = (uint8_t)(X >> 16);
+    }
+    bar_consumers();
+    const float hstep = 1.f / inv;
+    const int r0 = c.warp * (p.d / NW) + c.lane;  // row of line 0 of this lane
+    const uint16_t* scales = (const uint16_t*)(p.w + p.layer_bytes * layer + p.l_down + (size_t)p.d * (p.F / BU) * 16);
+    const int u0 = t.row0 / 2;  // first hidden unit of the task
+    int S[NL][3];
+    float acc[NL], sc[NL];
+    int sc_group = -1;
+#pragma unroll
+    for (int m = 0; m < NL; ++m) {
+        S[m][0] = S[m][1] = S[m][2] = 0;
+        acc[m] = 0.f;
+        sc[m] = 0.f;
+    }
+    uint4 hb[3 * CB];  // the planes of the current block
+    auto flush = [&]() {  // int4: the group's sums, scaled
+#pragma unroll
+        for (int m = 0; m < NL; ++m) {
+            acc[m] = fmaf(sc[m], planes_combine(S[m][0], S[m][1], S[m][2]), acc[m]);
+            S[m][0] = S[m][1] = S[m][2] = 0;
+        }
+    };
+    auto begin_block = [&](int seg) {
+        if constexpr (WT == MK_W_INT4_G128) {
+            const int g = (u0 + seg * BU) >> 7;
+            if (g != sc_group) {
+                if (sc_group >= 0) flush();
+                sc_group = g;
+#pragma unroll
+                for (int m = 0; m < NL; ++m) sc[m] = half_bits_to_f32(__ldg(scales + (size_t)g * p.d + r0 + 32 * m));
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < 3 * CB; ++q)
+            hb[q] = *(const uint4*)(hp + (size_t)(q / CB) * units + (size_t)seg * BU + 16 * (q % CB));
+    };
+    auto line = [&](int m, const uint8_t* src) {
+        const uint4 wq = *(const uint4*)src;
+        const uint32_t wv[4] = {wq.x, wq.y, wq.z, wq.w};
+        if constexpr (WT == MK_W_INT8_ROW) {
+            const uint32_t p0[4] = {hb[0].x, hb[0].y, hb[0].z, hb[0].w};
+            const uint32_t p1[4] = {hb[1].x, hb[1].y, hb[1].z, hb[1].w};
+            const uint32_t p2[4] = {hb[2].x, hb[2].y, hb[2].z, hb[2].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                S[m][0] = dp4a_su(wv[i], p0[i], S[m][0]);
+                S[m][1] = dp4a_su(wv[i], p1[i], S[m][1]);
+                S[m][2] = dp4a_ss(wv[i], p2[i], S[m][2]);
+            }
+        } else {  // 16 q of the even units (low nibbles) and of the odd units
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t lo = (wv[i] << 4) & 0xF0F0F0F0u, hi = wv[i] & 0xF0F0F0F0u;
+#pragma unroll
+                for (int q = 0; q < 3; ++q) {
+                    const uint4 A = hb[2 * q + (i >> 1)];
+                    const uint32_t ev = (i & 1) ? A.z : A.x, od = (i & 1) ? A.w : A.y;
+                    if (q < 2) {
+                        S[m][q] = dp4a_su(lo, ev, S[m][q]);
+                        S[m][q] = dp4a_su(hi, od, S[m][q]);
+                    } else {
+                        S[m][q] = dp4a_ss(lo, ev, S[m][q]);
+                        S[m][q] = dp4a_ss(hi, od, S[m][q]);
+                    }
+                }
+            }
+        }
+    };
+    if constexpr (NL <= SL) {
+        constexpr int SEGB = SL / NL;  // whole blocks per batch
+        const int nb2 = (kc + SEGB - 1) / SEGB;
+        for (int b = 0; b < nb2; ++b) {
+            ring_acquire<WT>(c, b == nb2 - 1);
+            const uint8_t* slot = c.ring + (size_t)c.rs * ring_slot_bytes<WT>() + c.lane * 16;
+#pragma unroll
+            for (int sg = 0; sg < SEGB; ++sg) {
+                const int seg = b * SEGB + sg;
+                if (seg < kc) {
+                    begin_block(seg);
+#pragma unroll
+                    for (int m = 0; m < NL; ++m) line(m, slot + (sg * NL + m) * 512);
+                }
+            }
+            __syncwarp();  // the slot is reused by a later issue of this warp
+            if (++c.rs == NB) c.rs = 0;
+        }
+    } else {
+        constexpr int BPB = NL / SL;  // batches per block
+        for (int seg = 0; seg < kc; ++seg) {
+            begin_block(seg);
+#pragma unroll
+            for (int bb = 0; bb < BPB; ++bb) {
+                ring_acquire<WT>(c, seg == kc - 1 && bb == BPB - 1);
+                const uint8_t* slot = c.ring + (size_t)c.rs * ring_slot_bytes<WT>() + c.lane * 16;
+#pragma unroll
+                for (int k = 0; k < SL; ++k) line(bb * SL + k, slot + k * 512);
+                __syncwarp();
+                if (++c.rs == NB) c.rs = 0;
+            }
+        }
+    }
+    if constexpr (WT == MK_W_INT4_G128) flush();
+    float* xo = xbuf(p, layer + 1) + r0;
+#pragma unroll
+    for (int m = 0; m < NL; ++m) {
+        float v;
+        if constexpr (WT == MK_W_INT8_ROW)
+            v = planes_combine(S[m][0], S[m][1], S[m][2]) * hstep * half_bits_to_f32(__ldg(scales + r0 + 32 * m));
+        else
+            v = acc[m] * (hstep * 0.0625f);
+        red_add_f32(xo + 32 * m, v);
+    }
+}
+
 template <int WT, int NL>
 __device__ __forceinline__ void ffn_cols(Ctx& c, const TaskRec& t, int layer) {
     if constexpr (WT == MK_W_BF16 || WT == MK_W_FP16) {
         ffn_cols16<WT, NL>(c, t, layer);
+        return;
+    }
+    if constexpr (idot_type<WT>()) {
+        ffn_cols_idot<WT, NL>(c, t, layer);
         return;
     }
     const VmParams& p = *c.p;
@@ -1072,7 +1440,7 @@ __device__ __forceinline__ void ffn_down(Ctx& c, const TaskRec& t, int layer) {
 // gate/up pair stays inside one batch.  The batches come from the warp's
 // stream (already requested before the counter wait).  Returns false when
 // the CTA must stop (abort or watchdog), identically in every thread.
-template <int WT, int BASE, int NG, bool SEL>
+template <int WT, int BASE, int NG, bool SEL, int IW>
 __device__ bool gemv_run(Ctx& c, const TaskRec& t, int task_id, int step, float& best_v, int& best_i) {
     const VmParams& p = *c.p;
     constexpr int HP = wpc<WT>() / 2;
@@ -1099,20 +1467,20 @@ __device__ bool gemv_run(Ctx& c, const TaskRec& t, int task_id, int step, float&
         case OP_QKV: {
             const uint16_t* gain = (const uint16_t*)(p.w + p.layer_bytes * layer + p.l_attn_norm);
             const uint16_t* emb = layer == 0 ? (const uint16_t*)(p.w + p.embed) + (size_t)tok * p.d : nullptr;
-            prologue_rmsnorm<BASE>(c, xbuf(p, layer), emb, gain, p.d, p.eps, LQ4);
+            prologue_rmsnorm<BASE, IW>(c, xbuf(p, layer), emb, gain, p.d, p.eps, LQ4);
             break;
         }
         case OP_GU:
         case OP_FFN:
-            prologue_rmsnorm<BASE>(c, xmid(p), nullptr,
+            prologue_rmsnorm<BASE, IW>(c, xmid(p), nullptr,
                                    (const uint16_t*)(p.w + p.layer_bytes * layer + p.l_ffn_norm), p.d, p.eps, LQ4);
             break;
         case OP_LM:
-            prologue_rmsnorm<BASE>(c, xbuf(p, p.L), nullptr, (const uint16_t*)(p.w + p.final_norm), p.d, p.eps, LQ4);
+            prologue_rmsnorm<BASE, IW>(c, xbuf(p, p.L), nullptr, (const uint16_t*)(p.w + p.final_norm), p.d, p.eps, LQ4);
             break;
         case OP_O:
-            if (p.merge_tasks) prologue_att_copy(c, LQ4);
-            else prologue_attention(c, LQ4);
+            if (p.merge_tasks) prologue_att_copy<IW>(c, LQ4);
+            else prologue_attention<IW>(c, LQ4);
             break;
         default:  // down reads h straight from device memory
             xin = p.h;
@@ -1120,9 +1488,23 @@ __device__ bool gemv_run(Ctx& c, const TaskRec& t, int task_id, int step, float&
             break;
     }
     if (p.trace && c.tid == 0) c.sh->t_ph[0] = gtimer();
-    // the lane's fragment of the input vector: k of chunk L + S*j
-    unsigned long long xr[NG * HP];
-    {
+    // the lane's fragment of the input vector: k of chunk L + S*j (an
+    // integer-dot task: the bytes of the three planes for those k)
+    unsigned long long xr[IW ? 1 : NG * HP];
+    uint4 xp[NG][IW == MK_W_INT4_G128 ? 6 : 3];
+    if constexpr (IW != 0) {
+        constexpr int CB = IW == MK_W_INT4_G128 ? 2 : 1;  // 16-byte words per chunk and plane
+        const uint8_t* pl = (const uint8_t*)c.xs;
+#pragma unroll
+        for (int j = 0; j < NG; ++j) {
+            const int cidx = L + S * j;
+            const bool ok = cidx < CH;
+#pragma unroll
+            for (int q = 0; q < 3 * CB; ++q)
+                xp[j][q] = ok ? *(const uint4*)(pl + (size_t)(q / CB) * K + (size_t)cidx * 16 * CB + 16 * (q % CB))
+                              : make_uint4(0, 0, 0, 0);
+        }
+    } else {
         const float f = from_global ? 1.f : c.rstd;
 #pragma unroll
         for (int j = 0; j < NG; ++j) {
@@ -1191,7 +1573,8 @@ __device__ bool gemv_run(Ctx& c, const TaskRec& t, int task_id, int step, float&
                 else
                     sc[j] = 0.f;
             }
-            v[r] = chunks_dot<WT, NG>(w, sc, xr);
+            if constexpr (IW != 0) v[r] = chunks_idot<WT, NG>(w, sc, xp) * c.xscale;
+            else v[r] = chunks_dot<WT, NG>(w, sc, xr);
             if constexpr (WT == MK_W_INT8_ROW)
                 rsv[r] = half_bits_to_f32(*(const uint16_t*)(slot + RW * NGM * 512 + r * TRAILER));
             else
@@ -1297,10 +1680,18 @@ __device__ bool gemv_run(Ctx& c, const TaskRec& t, int task_id, int step, float&
 }
 
 template <int WT, int BASE, bool SEL>
-__device__ bool gemv_task(Ctx& c, const TaskRec& t, int task_id, int step, float& best_v, int& best_i) {
+__device__ __forceinline__ bool gemv_task(Ctx& c, const TaskRec& t, int task_id, int step, float& best_v, int& best_i) {
     const int S = 32 * t.wpr, CH = t.K / wpc<WT>(), ng = (CH + S - 1) / S;
     constexpr int NGMAX = 64 / wpc<WT>();  // 8 (16-bit), 4 (int8), 2 (int4)
-#define MK_RUN(N) return gemv_run<WT, BASE, (N <= NGMAX ? N : NGMAX), SEL>(c, t, task_id, step, best_v, best_i)
+    if constexpr (idot_type<WT>()) {
+        // integer dot products for every task whose input vector a prologue
+        // builds in shared memory (not the down rows of an unfused FFN) and
+        // whose threads can hold it while the step D is found.  One instance
+        // (NGMAX chunks per lane): chunks past a row's end meet zero planes.
+        if (t.op != OP_DOWN && t.K <= 8 * NT * PIECE_IT)
+            return gemv_run<WT, BASE, NGMAX, SEL, WT>(c, t, task_id, step, best_v, best_i);
+    }
+#define MK_RUN(N) return gemv_run<WT, BASE, (N <= NGMAX ? N : NGMAX), SEL, 0>(c, t, task_id, step, best_v, best_i)
     switch (ng) {
         case 1: MK_RUN(1);
         case 2: MK_RUN(2);
