@@ -203,6 +203,14 @@ mk_status check_desc(const mk_model_desc* d) {
         set_error("a GEMV reduction length exceeds %d", MAX_K);
         return MK_ERR_UNSUPPORTED;
     }
+    if (d->wdtype == MK_W_INT4_G128) {  // the rows a GEMV task streams: d_model, q_dim, and d_ffn when the FFN is not fused
+        const int kmax = std::max(std::max(d->d_model, qd),
+                                  ffn_fused(d->wdtype, d->base_dtype, d->d_model) ? 0 : d->d_ffn);
+        if (kmax > INT4_MAX_ROW_K) {
+            set_error("int4 rows of %d codes: at most %d are supported", kmax, INT4_MAX_ROW_K);
+            return MK_ERR_UNSUPPORTED;
+        }
+    }
     if (d->vocab >= (1 << KEY_IDX_BITS)) {
         set_error("vocab %d >= %d", d->vocab, 1 << KEY_IDX_BITS);
         return MK_ERR_UNSUPPORTED;

@@ -28,6 +28,7 @@ constexpr int NW = NT / 32;             // warps per CTA
 constexpr int THREADS = NT;
 constexpr int MAXG = 8;                 // 8-element k groups per lane
 constexpr int MAX_K = 8 * NT * MAXG;    // 16384: eight warps x 32 lanes x MAXG groups
+constexpr int INT4_MAX_ROW_K = 8192;    // int4 GEMV rows: their fp16 scales (one per 128 k) fill a 128-byte slot trailer
 constexpr int MAX_REP = 8;              // query heads per KV head
 constexpr int ATTN_TILE = 32;           // positions per online-softmax tile
 // Copies of the split-KV partials (and of the merged attention output) that
@@ -55,7 +56,16 @@ constexpr int ffn_block(int wdtype) {
 __host__ __device__
 #endif
 constexpr int ffn_slot_lines(int wdtype) {
-    return wdtype == MK_W_INT8_ROW || wdtype == MK_W_FP8_E4M3 ? 8 : wdtype == MK_W_INT4_G128 ? 4 : 16;
+    return wdtype == MK_W_FP8_E4M3 ? 8 : wdtype == MK_W_INT4_G128 ? 8 : 16;
+}
+// Rows of one GEMV batch (a ring slot): 4 for int8 and int4 codes, whose
+// batches would otherwise carry a quarter or half of a 16-bit batch's bytes
+// for the same fixed cost per batch; 2 otherwise.
+#ifdef __CUDACC__
+__host__ __device__
+#endif
+constexpr int gemv_batch_rows(int wdtype) {
+    return wdtype == MK_W_INT8_ROW || wdtype == MK_W_INT4_G128 ? 4 : 2;
 }
 
 // The FFN runs fused (OP_FFN) when every warp's share of the d_model output

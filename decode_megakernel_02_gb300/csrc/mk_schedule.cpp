@@ -34,9 +34,9 @@ mk_status resolve_config(const mk_model_desc* d, const mk_schedule_config* cfg, 
         set_error("negative schedule knob");
         return MK_ERR_INVALID_ARG;
     }
-    c.rw = cfg->rows_in_flight ? cfg->rows_in_flight : 2;
-    if (c.rw != 2) {
-        set_error("rows_in_flight %d: only 2 is built", cfg->rows_in_flight);
+    c.rw = gemv_batch_rows(d->wdtype);  // the kernel's batch for this weight type
+    if (cfg->rows_in_flight && cfg->rows_in_flight != c.rw) {
+        set_error("rows_in_flight %d: only %d is built for this weight type", cfg->rows_in_flight, c.rw);
         return MK_ERR_INVALID_ARG;
     }
     if (cfg->attn_chunks) {

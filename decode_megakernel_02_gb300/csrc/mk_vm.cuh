@@ -131,17 +131,32 @@ __host__ __device__ constexpr int wpc() {
 template <int WT>
 __host__ __device__ constexpr bool group_scaled() { return WT == MK_W_INT4_G128 || WT == MK_W_FP8_E4M3; }
 
-constexpr int RW = 2;           // rows per batch
-constexpr int TRAILER = 256;    // max trailer bytes per row (fp16 scales of a K <= 16384 int4 row)
+template <int WT>
+__host__ __device__ constexpr int rw_of() {  // rows per batch
+    return gemv_batch_rows(WT);
+}
+// Trailer bytes per row in a slot: the row's scales (int8: one fp16, copied
+// as one 16-byte chunk; int4 and fp8: one fp16 per 128 k of a row of at most
+// INT4_MAX_ROW_K (int4) or MAX_K (fp8) codes).
+template <int WT>
+__host__ __device__ constexpr int trailer_of() {
+    return WT == MK_W_INT8_ROW    ? 16
+           : WT == MK_W_INT4_G128 ? 2 * INT4_MAX_ROW_K / 128
+           : WT == MK_W_FP8_E4M3  ? 2 * MAX_K / 128
+                                  : 0;
+}
 
 template <int WT>
 __host__ __device__ constexpr int ring_slot_bytes() {
-    return RW * (64 / wpc<WT>()) * 512 + (WT == MK_W_BF16 || WT == MK_W_FP16 ? 0 : RW * TRAILER);
+    return rw_of<WT>() * (64 / wpc<WT>()) * 512 + rw_of<WT>() * trailer_of<WT>();
 }
 template <int WT>
 __host__ __device__ constexpr int ring_slots() {  // slots that fit beside the other shared memory
-    return WT == MK_W_INT4_G128 ? 9 : WT == MK_W_INT8_ROW || WT == MK_W_FP8_E4M3 ? 5 : 3;
+    return WT == MK_W_INT4_G128 || WT == MK_W_FP8_E4M3 ? 5 : 3;
 }
+static_assert(ring_slot_bytes<MK_W_INT8_ROW>() >= ffn_slot_lines(MK_W_INT8_ROW) * 512, "column lines of a slot");
+static_assert(ring_slot_bytes<MK_W_INT4_G128>() >= ffn_slot_lines(MK_W_INT4_G128) * 512, "column lines of a slot");
+static_assert(ring_slot_bytes<MK_W_FP8_E4M3>() >= ffn_slot_lines(MK_W_FP8_E4M3) * 512, "column lines of a slot");
 
 struct WarpStream {
     int s, qi;               // cursor: step, next record of the CTA's table
@@ -416,6 +431,10 @@ static __device__ __forceinline__ int step_token(const VmParams& p, int step) {
 // rebuilds the dot product.
 template <int WT>
 __host__ __device__ constexpr bool idot_type() { return WT == MK_W_INT8_ROW || WT == MK_W_INT4_G128; }
+// Byte planes of the input (24 bits).  Two planes (16 bits) against int4
+// codes lose too much: the teacher-forced gate fails on the tiny model.
+template <int WT>
+__host__ __device__ constexpr int n_planes() { return 3; }
 constexpr int PIECE_IT = 2;  // groups of 8 inputs a thread holds while the step D is found: K <= 8 NT PIECE_IT
 
 // Byte offset of element k inside a plane.  int8 chunks take k in order.  An
@@ -438,11 +457,13 @@ __device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int c) {  // sign
     return d;
 }
 // 1 / D for a vector whose largest magnitude is m (1 when m is 0).  D = 2^E
-// with m / D in [2^21, 2^22), so |X| <= 2^22 and byte 2 of X is X >> 16.
+// with m / D in [2^(8 NP - 3), 2^(8 NP - 2)), so |X| <= 2^(8 NP - 2) and the
+// top byte of X (signed) is X >> 8 (NP - 1).
+template <int NP>
 __device__ __forceinline__ float fixed_inv_step(float m) {
     if (!(m > 0.f)) return 1.f;
     const int e = (int)((__float_as_uint(m) >> 23) & 0xFFu) - 127;  // floor(log2 m) for normal m
-    const int E = max(-126, min(e - 21, 126));
+    const int E = max(-126, min(e - (8 * NP - 3), 126));
     return __uint_as_float((uint32_t)(127 - E) << 23);
 }
 // Planes of four values: P[p] holds byte p of a, b, c, d (in that order).
@@ -466,12 +487,17 @@ __device__ __forceinline__ void put_planes8(uint8_t* pl, int K, int g, const int
         planes4(X[4], X[5], X[6], X[7], B);
     }
 #pragma unroll
-    for (int p = 0; p < 3; ++p) *(uint2*)(pl + (size_t)p * K + 8 * g) = make_uint2(A[p], B[p]);
+    for (int p = 0; p < n_planes<WT>(); ++p) *(uint2*)(pl + (size_t)p * K + 8 * g) = make_uint2(A[p], B[p]);
 }
 // sum over a chunk pair of 4 words of 4-byte products, as an fp32 value of
 // the fixed-point sum: S0 + 2^8 S1 + 2^16 S2
 __device__ __forceinline__ float planes_combine(int s0, int s1, int s2) {
     return fmaf((float)s2, 65536.f, fmaf((float)s1, 256.f, (float)s0));
+}
+template <int NP>
+__device__ __forceinline__ float planes_sum(const int (&s)[NP]) {
+    if constexpr (NP == 3) return planes_combine(s[0], s[1], s[2]);
+    else return fmaf((float)s[1], 256.f, (float)s[0]);
 }
 // The lane's partial dot product of one row, in units of D: xp holds the
 // planes of the lane's chunks L + S*j (int8: one uint4 per plane; int4: two,
@@ -479,7 +505,7 @@ __device__ __forceinline__ float planes_combine(int s0, int s1, int s2) {
 // scale in sc[j]; int8 takes its row scale after the warp reduction.
 template <int WT, int NG>
 __device__ __forceinline__ float chunks_idot(const uint4 (&w)[NG], const float (&sc)[NG],
-                                             const uint4 (&xp)[NG][WT == MK_W_INT4_G128 ? 6 : 3]) {
+                                             const uint4 (&xp)[NG][WT == MK_W_INT4_G128 ? 2 * n_planes<WT>() : 3]) {
     if constexpr (WT == MK_W_INT8_ROW) {
         int s[2][3] = {{0, 0, 0}, {0, 0, 0}};  // two sets: shorter dependency chains
 #pragma unroll
@@ -501,15 +527,18 @@ __device__ __forceinline__ float chunks_idot(const uint4 (&w)[NG], const float (
 #pragma unroll
         for (int j = 0; j < NG; ++j) {
             const uint32_t wv[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
-            int s[3] = {0, 0, 0};
+            constexpr int NP = n_planes<WT>();
+            int s[NP];
+#pragma unroll
+            for (int p = 0; p < NP; ++p) s[p] = 0;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const uint32_t lo = (wv[i] << 4) & 0xF0F0F0F0u, hi = wv[i] & 0xF0F0F0F0u;
 #pragma unroll
-                for (int p = 0; p < 3; ++p) {
+                for (int p = 0; p < NP; ++p) {  // the top plane is signed
                     const uint4 A = xp[j][2 * p + (i >> 1)];
                     const uint32_t ev = (i & 1) ? A.z : A.x, od = (i & 1) ? A.w : A.y;
-                    if (p < 2) {
+                    if (p < NP - 1) {
                         s[p] = dp4a_su(lo, ev, s[p]);
                         s[p] = dp4a_su(hi, od, s[p]);
                     } else {
@@ -518,7 +547,7 @@ __device__ __forceinline__ float chunks_idot(const uint4 (&w)[NG], const float (
                     }
                 }
             }
-            acc = fmaf(sc[j], planes_combine(s[0], s[1], s[2]), acc);
+            acc = fmaf(sc[j], planes_sum<NP>(s), acc);
         }
         return acc * 0.0625f;
     }
@@ -544,7 +573,7 @@ __device__ __forceinline__ int xs_pos(int u, int K, int lq4) {
 // The planes of the kept inputs times f0, given m = max |kept input|.
 template <int IW>
 __device__ __forceinline__ void write_planes(Ctx& c, const float (&keep)[PIECE_IT][8], int K, float f0, float m) {
-    const float inv = fixed_inv_step(m * f0);
+    const float inv = fixed_inv_step<n_planes<IW>()>(m * f0);
     const float f = f0 * inv;
 #pragma unroll
     for (int it = 0; it < PIECE_IT; ++it) {
@@ -917,6 +946,7 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 // Move the cursor to this warp's next batch; false at the end of the launch.
+template <int WT>
 __device__ __forceinline__ bool stream_next(const Ctx& c, WarpStream& w) {
     const VmParams& p = *c.p;
     for (;;) {
@@ -970,7 +1000,7 @@ __device__ __forceinline__ bool stream_next(const Ctx& c, WarpStream& w) {
         w.base = p.w + (size_t)t.w_off16 * 16;
         w.lofs = L * 16;
         w.code_bytes = code_bytes;
-        w.nb = (w.nrows + RW - 1) / RW;
+        w.nb = (w.nrows + rw_of<WT>() - 1) / rw_of<WT>();
         w.q = w.grp;
     }
 }
@@ -982,7 +1012,7 @@ __device__ __forceinline__ void stream_issue(Ctx& c) {
     constexpr int NGM = 64 / wpc<WT>();
     WarpStream& w = c.ws;
     const int lane = c.lane;
-    if (!w.done && stream_next(c, w)) {
+    if (!w.done && stream_next<WT>(c, w)) {
         uint8_t* slot = c.ring + (size_t)w.si * ring_slot_bytes<WT>() + lane * 16;
         const int64_t jstep = (int64_t)w.S * 16;
         if (w.cols) {  // lines q*tlc .. of the task: line i is line i % nl of block i / nl
@@ -1009,6 +1039,7 @@ __device__ __forceinline__ void stream_issue(Ctx& c) {
                 }
             }
         }
+        constexpr int RW = rw_of<WT>(), TRAILER = trailer_of<WT>();
 #pragma unroll
         for (int r = 0; r < RW; ++r) {
             if (w.cols) break;
@@ -1195,40 +1226,42 @@ __device__ __forceinline__ void ffn_cols_idot(Ctx& c, const TaskRec& t, int laye
     constexpr int NB = ring_slots<WT>();
     constexpr int BU = ffn_block(WT), SL = ffn_slot_lines(WT);
     constexpr int CB = WT == MK_W_INT4_G128 ? 2 : 1;  // 16-byte words of a block per plane
+    constexpr int NP = n_planes<WT>();
     const int kc = t.nrows / (2 * BU);
     const int units = kc * BU;
     const float* hs = ffn_h(c);
     float mx = 0.f;
     for (int u = c.tid; u < units; u += NT) mx = fmaxf(mx, fabsf(hs[u]));
-    const float inv = fixed_inv_step(block_max(c, mx));
+    const float inv = fixed_inv_step<NP>(block_max(c, mx));
     uint8_t* hp = (uint8_t*)c.xs;
     for (int u = c.tid; u < units; u += NT) {
         const int X = __float2int_rn(hs[u] * inv);
         const int q = plane_pos<WT>(u);
-        hp[q] = (uint8_t)X;
-        hp[units + q] = (uint8_t)(X >> 8);
-        hp[2 * units + q] = (uint8_t)(X >> 16);
+#pragma unroll
+        for (int pp = 0; pp < NP; ++pp) hp[pp * units + q] = (uint8_t)(X >> (8 * pp));
     }
     bar_consumers();
     const float hstep = 1.f / inv;
     const int r0 = c.warp * (p.d / NW) + c.lane;  // row of line 0 of this lane
     const uint16_t* scales = (const uint16_t*)(p.w + p.layer_bytes * layer + p.l_down + (size_t)p.d * (p.F / BU) * 16);
     const int u0 = t.row0 / 2;  // first hidden unit of the task
-    int S[NL][3];
+    int S[NL][NP];
     float acc[NL], sc[NL];
     int sc_group = -1;
 #pragma unroll
     for (int m = 0; m < NL; ++m) {
-        S[m][0] = S[m][1] = S[m][2] = 0;
+#pragma unroll
+        for (int pp = 0; pp < NP; ++pp) S[m][pp] = 0;
         acc[m] = 0.f;
         sc[m] = 0.f;
     }
-    uint4 hb[3 * CB];  // the planes of the current block
+    uint4 hb[NP * CB];  // the planes of the current block
     auto flush = [&]() {  // int4: the group's sums, scaled
 #pragma unroll
         for (int m = 0; m < NL; ++m) {
-            acc[m] = fmaf(sc[m], planes_combine(S[m][0], S[m][1], S[m][2]), acc[m]);
-            S[m][0] = S[m][1] = S[m][2] = 0;
+            acc[m] = fmaf(sc[m], planes_sum<NP>(S[m]), acc[m]);
+#pragma unroll
+            for (int pp = 0; pp < NP; ++pp) S[m][pp] = 0;
         }
     };
     auto begin_block = [&](int seg) {
@@ -1242,7 +1275,7 @@ __device__ __forceinline__ void ffn_cols_idot(Ctx& c, const TaskRec& t, int laye
             }
         }
 #pragma unroll
-        for (int q = 0; q < 3 * CB; ++q)
+        for (int q = 0; q < NP * CB; ++q)
             hb[q] = *(const uint4*)(hp + (size_t)(q / CB) * units + (size_t)seg * BU + 16 * (q % CB));
     };
     auto line = [&](int m, const uint8_t* src) {
@@ -1263,10 +1296,10 @@ __device__ __forceinline__ void ffn_cols_idot(Ctx& c, const TaskRec& t, int laye
             for (int i = 0; i < 4; ++i) {
                 const uint32_t lo = (wv[i] << 4) & 0xF0F0F0F0u, hi = wv[i] & 0xF0F0F0F0u;
 #pragma unroll
-                for (int q = 0; q < 3; ++q) {
+                for (int q = 0; q < NP; ++q) {  // the top plane is signed
                     const uint4 A = hb[2 * q + (i >> 1)];
                     const uint32_t ev = (i & 1) ? A.z : A.x, od = (i & 1) ? A.w : A.y;
-                    if (q < 2) {
+                    if (q < NP - 1) {
                         S[m][q] = dp4a_su(lo, ev, S[m][q]);
                         S[m][q] = dp4a_su(hi, od, S[m][q]);
                     } else {
@@ -1316,7 +1349,7 @@ __device__ __forceinline__ void ffn_cols_idot(Ctx& c, const TaskRec& t, int laye
     for (int m = 0; m < NL; ++m) {
         float v;
         if constexpr (WT == MK_W_INT8_ROW)
-            v = planes_combine(S[m][0], S[m][1], S[m][2]) * hstep * half_bits_to_f32(__ldg(scales + r0 + 32 * m));
+            v = planes_combine(S[m][0], S[m][1], S[m][NP - 1]) * hstep * half_bits_to_f32(__ldg(scales + r0 + 32 * m));
         else
             v = acc[m] * (hstep * 0.0625f);
         red_add_f32(xo + 32 * m, v);
@@ -1446,6 +1479,7 @@ __device__ bool gemv_run(Ctx& c, const TaskRec& t, int task_id, int step, float&
     constexpr int HP = wpc<WT>() / 2;
     constexpr int NGM = 64 / wpc<WT>();
     constexpr int NB = ring_slots<WT>();
+    constexpr int RW = rw_of<WT>(), TRAILER = trailer_of<WT>();
     const int op = t.op, layer = t.layer, row0 = t.row0, nrows = t.nrows, K = t.K;
     const int g = t.wpr, ngroups = NW / g;
     const int grp = c.warp / g, wig = c.warp % g;
@@ -1491,7 +1525,7 @@ __device__ bool gemv_run(Ctx& c, const TaskRec& t, int task_id, int step, float&
     // the lane's fragment of the input vector: k of chunk L + S*j (an
     // integer-dot task: the bytes of the three planes for those k)
     unsigned long long xr[IW ? 1 : NG * HP];
-    uint4 xp[NG][IW == MK_W_INT4_G128 ? 6 : 3];
+    uint4 xp[NG][IW == MK_W_INT4_G128 ? 2 * n_planes<IW>() : 3];
     if constexpr (IW != 0) {
         constexpr int CB = IW == MK_W_INT4_G128 ? 2 : 1;  // 16-byte words per chunk and plane
         const uint8_t* pl = (const uint8_t*)c.xs;
@@ -1500,7 +1534,7 @@ __device__ bool gemv_run(Ctx& c, const TaskRec& t, int task_id, int step, float&
             const int cidx = L + S * j;
             const bool ok = cidx < CH;
 #pragma unroll
-            for (int q = 0; q < 3 * CB; ++q)
+            for (int q = 0; q < n_planes<IW>() * CB; ++q)
                 xp[j][q] = ok ? *(const uint4*)(pl + (size_t)(q / CB) * K + (size_t)cidx * 16 * CB + 16 * (q % CB))
                               : make_uint4(0, 0, 0, 0);
         }

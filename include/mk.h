@@ -90,8 +90,8 @@ typedef struct {
  * SM assignment, pipelining depth).  0 selects the default. */
 typedef struct {
     int32_t sms;            /* CTAs (= SMs used); default all SMs of the device              */
-    int32_t rows_in_flight; /* weight rows each warp group keeps loading ahead; 2 (the only  
-                               value built)                                               */
+    int32_t rows_in_flight; /* weight rows of one batch of a warp group; the only value built
+                               is 4 for int8/int4 weights and 2 otherwise (0 selects it)  */
     int32_t attn_chunks;    /* split-KV chunks per KV head; default from max_seq and sms     */
     int32_t watchdog_ms;    /* a device wait gives up after this long; default 1000          */
     int32_t token_select;   /* 1: one more task per step selects the token after the LM
