@@ -1749,7 +1749,9 @@ __device__ __forceinline__ bool gemv_task(Ctx& c, const TaskRec& t, int task_id,
 // queries are rotated, so cache reads overlap the qkv reads.  Writes, per
 // query head, the chunk's running max m, its sum l = sum e^(s - m), and its
 // output normalised by l (bounded by max|v|, so fp16 holds it at any chunk
-// length); a merge weights each chunk by e^(m - M) * l.
+// length); a merge weights each chunk by e^(m - M) * l.  Two tiles of cache
+// rows are in flight: the first two are requested before this step's q/k/v
+// are polled, and each later one as the tile two ahead of it finishes.
 template <int HD>
 static __device__ __forceinline__ bool attn_task(Ctx& c, const TaskRec& t, int task_id, int step) {
     const VmParams& p = *c.p;
@@ -1767,39 +1769,24 @@ static __device__ __forceinline__ bool attn_task(Ctx& c, const TaskRec& t, int t
     uint16_t* kbase = p.kv + (((size_t)l * 2 + 0) * p.Hkv + g) * head_stride;
     uint16_t* vbase = p.kv + (((size_t)l * 2 + 1) * p.Hkv + g) * head_stride;
 
-    uint32_t kraw[PPW][DPL / 2];
-    uint32_t vraw[PPW][DPL / 2];
+    uint32_t kraw[PPW][DPL / 2], kn[PPW][DPL / 2];  // this tile's K and V rows, the next tile's
+    uint32_t vraw[PPW][DPL / 2], vn[PPW][DPL / 2];
     // K rows of a tile go to kraw, V rows to vraw, as raw bf16 pairs (widened
     // where they are used, so that a load in flight does not hold the thread
     // up before its wait); the two halves are loaded separately so that the
     // next tile's rows are in flight while this one is computed (V once
     // staged in shared memory, K once the scores are done).
-    auto load_k = [&](int jt, int n) {
+    auto load_rows = [&](uint32_t (&dst)[PPW][DPL / 2], const uint16_t* base, int jt, int n) {
 #pragma unroll
         for (int k = 0; k < PPW; ++k) {
             const int jj = c.warp + NW * k, j = jt + jj;
             if (jj < n && j != pos) {
                 if constexpr (DPL == 2) {
-                    kraw[k][0] = __ldcg((const unsigned int*)(kbase + (size_t)j * HD + c.lane * 2));
+                    dst[k][0] = __ldcg((const unsigned int*)(base + (size_t)j * HD + c.lane * 2));
                 } else {
-                    const uint2 w = __ldcg((const uint2*)(kbase + (size_t)j * HD + c.lane * 4));
-                    kraw[k][0] = w.x;
-                    kraw[k][1] = w.y;
-                }
-            }
-        }
-    };
-    auto load_v = [&](int jt, int n) {
-#pragma unroll
-        for (int k = 0; k < PPW; ++k) {
-            const int jj = c.warp + NW * k, j = jt + jj;
-            if (jj < n && j != pos) {
-                if constexpr (DPL == 2) {
-                    vraw[k][0] = __ldcg((const unsigned int*)(vbase + (size_t)j * HD + c.lane * 2));
-                } else {
-                    const uint2 w = __ldcg((const uint2*)(vbase + (size_t)j * HD + c.lane * 4));
-                    vraw[k][0] = w.x;
-                    vraw[k][1] = w.y;
+                    const uint2 w = __ldcg((const uint2*)(base + (size_t)j * HD + c.lane * 4));
+                    dst[k][0] = w.x;
+                    dst[k][1] = w.y;
                 }
             }
         }
@@ -1832,8 +1819,12 @@ static __device__ __forceinline__ bool attn_task(Ctx& c, const TaskRec& t, int t
     // arrive: rows of earlier positions were written by earlier steps, whose
     // writers the wait of this CTA's previous task already ordered before us.
     if (j1 > j0) {
-        load_k(j0, min(ATTN_TILE, j1 - j0));
-        load_v(j0, min(ATTN_TILE, j1 - j0));
+        load_rows(kraw, kbase, j0, min(ATTN_TILE, j1 - j0));
+        load_rows(vraw, vbase, j0, min(ATTN_TILE, j1 - j0));
+    }
+    if (j0 + ATTN_TILE < j1) {
+        load_rows(kn, kbase, j0 + ATTN_TILE, min(ATTN_TILE, j1 - j0 - ATTN_TILE));
+        load_rows(vn, vbase, j0 + ATTN_TILE, min(ATTN_TILE, j1 - j0 - ATTN_TILE));
     }
     if (!wait_counters(c, t, task_id, step)) return false;  // counter waits, if any, and aborts
 
@@ -1883,9 +1874,7 @@ static __device__ __forceinline__ bool attn_task(Ctx& c, const TaskRec& t, int t
 
     for (int jt = j0; jt < j1; jt += ATTN_TILE) {
         const int n = min(ATTN_TILE, j1 - jt);
-        const int jn = jt + ATTN_TILE, nn = min(ATTN_TILE, j1 - jn);  // next tile
         stage_v(jt, n);
-        if (nn > 0) load_v(jn, nn);
         // scores for (position k, head h), four heads at a time: PPW*4 partial
         // sums per lane, transposed so that lane pairs hold the totals
         for (int h0 = 0; h0 < rep; h0 += 4) {
@@ -1909,7 +1898,6 @@ static __device__ __forceinline__ bool attn_task(Ctx& c, const TaskRec& t, int t
             const int idx = c.lane >> SH, k = idx >> 2, hh = idx & 3, jj = c.warp + NW * k;
             if ((c.lane & ((1 << SH) - 1)) == 0 && h0 + hh < rep && jj < n) at.sc[(h0 + hh) * ATTN_TILE + jj] = sc;
         }
-        if (nn > 0) load_k(jn, nn);  // the scores no longer need this tile's K rows
         bar_consumers();
         if (c.warp < rep) {  // online softmax statistics: warp h owns query head h
             const int h = c.warp;
@@ -1940,6 +1928,20 @@ static __device__ __forceinline__ bool attn_task(Ctx& c, const TaskRec& t, int t
             }
         }
         bar_consumers();  // the next tile overwrites scores and V rows
+        // the next tile's rows (requested one tile ago) become current; the
+        // tile after it is requested now
+        const int j2 = jt + 2 * ATTN_TILE;
+#pragma unroll
+        for (int k = 0; k < PPW; ++k)
+#pragma unroll
+            for (int i = 0; i < DPL / 2; ++i) {
+                kraw[k][i] = kn[k][i];
+                vraw[k][i] = vn[k][i];
+            }
+        if (j2 < j1) {
+            load_rows(kn, kbase, j2, min(ATTN_TILE, j1 - j2));
+            load_rows(vn, vbase, j2, min(ATTN_TILE, j1 - j2));
+        }
     }
     if (p.trace && c.tid == 0) c.sh->t_ph[1] = gtimer();
 #pragma unroll
