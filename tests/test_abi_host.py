@@ -58,6 +58,25 @@ def test_errors_without_a_device(mk):
     assert e.value.status == mk.MK_ERR_UNSUPPORTED
 
 
+def test_int4_row_length_limit(mk):
+    # int4 rows carry one fp16 scale per 128 codes in a 128-byte slot trailer,
+    # so they are limited to 8192 codes: an unfused FFN (d_model 2560 is not a
+    # fused shape for quantised codes) with d_ffn 8320 would need longer down
+    # rows.  The fused shapes and rows up to the limit are accepted.
+    w = synthetic.get_workload("tiny")
+    d = mk.make_desc(w.with_(wdtype="int4", d_model=2560, n_q_heads=20, n_kv_heads=4, d_ffn=8320))
+    with pytest.raises(mk.MKError) as e:
+        mk.mk_packed_size(d)
+    assert e.value.status == mk.MK_ERR_UNSUPPORTED
+    assert "int4 rows" in str(e.value)
+    assert mk.mk_packed_size(mk.make_desc(w.with_(wdtype="int4", d_model=2560, n_q_heads=20, n_kv_heads=4,
+                                                  d_ffn=8192))) > 0
+    assert mk.mk_packed_size(mk.make_desc(w.with_(wdtype="int4", d_model=4096, n_q_heads=32, n_kv_heads=8,
+                                                  d_ffn=14336))) > 0  # fused: the long rows are columns
+    assert mk.mk_packed_size(mk.make_desc(w.with_(wdtype="int8", d_model=2560, n_q_heads=20, n_kv_heads=4,
+                                                  d_ffn=8320))) > 0
+
+
 # ------------------------------------------------------------------ packer
 def test_quantisers_match_oracle_bytes(mk):
     rng = np.random.default_rng(5)

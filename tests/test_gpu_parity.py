@@ -235,6 +235,43 @@ def test_tiny_quantised_teacher_forced(mk, wd, sms):
     dec.close()
 
 
+def _pow2_scaled(bits, k):
+    # bf16 bits times 2^k: exact (no value of these weights under- or overflows)
+    f = synthetic.bits_to_f32(bits, "bf16") * np.float32(2.0 ** k)
+    return (f.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+
+
+@pytest.mark.parametrize("wd", ["int8", "int4"])
+def test_integer_dot_input_range(mk, wd):
+    # int8/int4 GEMVs multiply their codes by a fixed-point copy of the input
+    # whose step D = 2^E follows max|x| (c15b).  The ends of that range on the
+    # tiny model: all-zero inputs (every other forced token has a zero
+    # embedding row, so layer 0's QKV input vanishes and D falls back to 1),
+    # attention outputs about 2^-4 of the usual (W_v scaled: O's input takes
+    # a smaller E) and SwiGLU outputs about 2^8 of the usual (W_up scaled: the
+    # down projection's input takes a larger E).  W_v is not scaled further:
+    # the split-KV partials are fp16 values of v's magnitude, and below fp16's
+    # normal range (6.1e-5) they lose precision whatever the GEMV does.
+    w = synthetic.get_workload("tiny").with_(wdtype=wd)
+    weights = dict(weights_for("tiny"))
+    for layer in range(w.n_layers):
+        weights[f"l{layer}.wv"] = _pow2_scaled(weights[f"l{layer}.wv"], -4)
+        weights[f"l{layer}.wup"] = _pow2_scaled(weights[f"l{layer}.wup"], 8)
+    prompt = synthetic.generate_prompt(w)
+    forced_tail = synthetic.gen.random_tokens(w, w.decode_steps - 1, 11)
+    emb = weights["embed"].copy()
+    emb[np.unique(forced_tail[::2])] = 0
+    weights["embed"] = emb
+    desc = mk.make_desc(w)
+    dec = mk.Decoder(desc, mk.pack_model(desc, weights))
+    dec.prefill(prompt)
+    lg, ids = dec.teacher_forced(np.concatenate([prompt[-1:], forced_tail]).astype(np.int32))
+    ref = L.forward_full(oracle_model(w, weights), np.concatenate([prompt, forced_tail]), last=w.decode_steps)
+    check_logits(lg, ref, label=f"tiny-{wd}-input-range")
+    assert np.array_equal(ids, lg.argmax(axis=1))
+    dec.close()
+
+
 @pytest.mark.parametrize("wd", ["int8", "int4", "fp8"])
 def test_8b_shape_quantised_teacher_forced(mk, wd):
     # d_model 4096: 16 lines per column block, i.e. a block spans 2 (int8) or
