@@ -89,8 +89,8 @@ def dequant_int4(q, s16, group=128):
 
 
 # ----------------------------------------------------------------- FP8 E4M3, block-scaled
-# The Netra Kernel summary ("TL;DR": FP8 serving ops) and BASELINE's next rows
-# name FP8 weights; the pages fix no format details.  Readings: the OCP FP8
+# The Netra Kernel summary ("TL;DR": FP8 serving ops) names FP8; the pages fix
+# no format details for weights.  Readings: the OCP FP8
 # E4M3 format (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; exponent 0
 # holds the subnormals m * 2^-9; S.1111.111 is NaN and there is no infinity, so
 # the largest finite magnitude is 1.75 * 2^8 = 448), one fp16 scale per 128
