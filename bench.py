@@ -82,12 +82,26 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
 
 
-def kernel_source_hash():
+KERNEL_SOURCES = ("decode_megakernel_02_gb300/csrc/mk_vm.cuh", "decode_megakernel_02_gb300/csrc/mk_internal.h",
+                  "decode_megakernel_02_gb300/csrc/mk_schedule.cpp")
+
+
+def code_only(text):
+    """The source text without comments, blank lines and trailing spaces: an
+    edit of the comments leaves the kernel, and so this form, unchanged."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*$", "", line).rstrip() for line in text.splitlines())
+    return "\n".join(line for line in lines if line)
+
+
+def kernel_source_hash(read=None):
+    """Hash of the decode kernel's code (the kernel, its internal header and the
+    schedule lowering), ignoring comments.  `read(path)` returns a file's text
+    (default: the working tree)."""
+    read = read or (lambda f: open(os.path.join(ROOT, f)).read())
     h = hashlib.sha256()
-    for f in ("decode_megakernel_02_gb300/csrc/mk_vm.cuh", "decode_megakernel_02_gb300/csrc/mk_internal.h",
-              "decode_megakernel_02_gb300/csrc/mk_schedule.cpp"):
-        with open(os.path.join(ROOT, f), "rb") as fh:
-            h.update(fh.read())
+    for f in KERNEL_SOURCES:
+        h.update(code_only(read(f)).encode())
     return h.hexdigest()[:16]
 
 

@@ -18,7 +18,8 @@
 //    ahead across task boundaries and counter waits: the copies of the next
 //    task's first rows are in flight while this warp waits or reduces.
 //  * Warp groups own whole rows: each lane holds a fixed fragment of the
-//    input vector in registers (fp32 pairs for packed fma.rn.f32x2) and the
+//    input vector in registers (fp32 pairs for packed fma.rn.f32x2; for int8
+//    and int4 codes, the bytes of a 24-bit fixed-point copy for dp4a) and the
 //    rows of a batch are reduced with one transposed warp reduction; large K
 //    is split over 2-8 warps that combine through shared memory.
 //  * Counters are u32 words on their own 128-byte lines; a wait is an
@@ -932,9 +933,10 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[N], int lane) {
 // fixed by the schedule (tasks in queue order, for each GEMV task the batches
 // q = grp, grp + ngroups, ... of its warp group), so the copies run ahead
 // across counter waits and across tasks: a task usually starts with its first
-// batches already on chip.  A slot holds RW rows: the lane's chunks j of each
-// row at [(r * MAXG + j) * 512 + lane * 16] and the row's quantisation
-// trailer (scales) at [RW * MAXG * 512 + r * TRAILER].
+// batches already on chip.  A slot holds RW = rw_of<WT>() rows (2 for 16-bit
+// and fp8 codes, 4 for int8 and int4): the lane's chunks j of each row at
+// [(r * NGM + j) * 512 + lane * 16] and the row's quantisation trailer
+// (scales) at [RW * NGM * 512 + r * TRAILER], TRAILER = trailer_of<WT>().
 
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(smem_dst)),
