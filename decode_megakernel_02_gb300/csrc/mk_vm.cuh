@@ -100,9 +100,12 @@ __device__ __forceinline__ unsigned long long e4m3x2_pair(uint32_t two) {
 struct AttnScratch {
     float q[MAX_REP * 128];         // roped, scaled queries of one KV group
     float kcur[128], vcur[128];     // this step's K and V (bf16-rounded)
-    float sc[MAX_REP * ATTN_TILE];  // scores / probabilities of a tile
-    uint16_t sv[ATTN_TILE * 128];   // V rows of the current tile (bf16)
+    float sc[MAX_REP * ATTN_TILE];  // scores of a tile, [head][position]
+    float pt[ATTN_TILE * MAX_REP];  // probabilities of a tile, [position][head]
+    uint16_t sv[ATTN_TILE * 128];   // V rows of the current tile (bf16); after the last
+                                    // tile, the P.V partial sums of the position subsets
 };
+static_assert(4 * (NT / 64) * 128 * sizeof(float) <= sizeof(AttnScratch::sv), "P.V subset sums, four heads");
 struct MergeScratch {
     float mw[MAX_HC];               // per (head, chunk) max, then weight
     float ml[MAX_HC];               // per (head, chunk) sum
@@ -1745,10 +1748,12 @@ __device__ __forceinline__ bool gemv_task(Ctx& c, const TaskRec& t, int task_id,
 // One (KV head, chunk) task: RoPE for the group's queries and this step's
 // key, K/V append at pos (last chunk only), then an online-softmax pass over
 // the chunk's positions in tiles of ATTN_TILE.  Warp w owns positions
-// w, w+8, ... of a tile for the scores (its K rows in registers) and stages
-// their V rows in shared memory; for P.V each thread owns fixed output
-// elements (head, dim).  The first tile's rows are requested before the
-// queries are rotated, so cache reads overlap the qkv reads.  Writes, per
+// w, w+8, ... of a tile for the scores (its K rows and the queries in
+// registers) and stages their V rows in shared memory; for P.V each thread
+// owns two adjacent dims of every head over one subset of a tile's positions
+// (one V word and one probability vector per position), and the subsets are
+// added once after the last tile.  The first tile's rows are requested
+// before the queries are rotated, so cache reads overlap the qkv reads.  Writes, per
 // query head, the chunk's running max m, its sum l = sum e^(s - m), and its
 // output normalised by l (bounded by max|v|, so fp16 holds it at any chunk
 // length); a merge weights each chunk by e^(m - M) * l.  Two tiles of cache
@@ -1761,7 +1766,7 @@ static __device__ __forceinline__ bool attn_task(Ctx& c, const TaskRec& t, int t
     AttnScratch& at = *c.at;
     constexpr int DPL = HD / 32;            // dims per lane
     constexpr int PPW = ATTN_TILE / NW;     // positions per warp per tile
-    constexpr int OPT = MAX_REP * HD / NT;  // output elements per thread (upper bound)
+    constexpr int NDP = HD / 2, NPS = NT / NDP;  // P.V: dim pairs, position subsets
     const int rep = p.Hq / p.Hkv, g = t.row0, ch = t.nrows, C = t.K, l = t.layer;
     const int pos = p.pos0 + step, len = pos + 1;
     const int j0 = (int)((int64_t)ch * len / C), j1 = (int)((int64_t)(ch + 1) * len / C);
@@ -1870,29 +1875,39 @@ static __device__ __forceinline__ bool attn_task(Ctx& c, const TaskRec& t, int t
             vbase[(size_t)pos * HD + i] = __bfloat16_as_ushort(__float2bfloat16_rn(at.vcur[i]));
         }
     }
-    float acc[OPT];
+    // The queries in registers: lane dims lane*DPL .. +DPL of every head.
+    float qr[MAX_REP][DPL];
 #pragma unroll
-    for (int e = 0; e < OPT; ++e) acc[e] = 0.f;
+    for (int h = 0; h < MAX_REP; ++h)
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) qr[h][i] = h < rep ? at.q[h * HD + c.lane * DPL + i] : 0.f;
+    // P.V: thread (dp, ps) accumulates dims 2dp, 2dp+1 of every head over the
+    // positions ps, ps + NPS, ... of each tile; the NPS partial sums of a
+    // head's dim are added after the last tile.
+    const int dp = c.tid % NDP, ps = c.tid / NDP;
+    float acc[MAX_REP][2];
+#pragma unroll
+    for (int h = 0; h < MAX_REP; ++h) acc[h][0] = acc[h][1] = 0.f;
 
     for (int jt = j0; jt < j1; jt += ATTN_TILE) {
         const int n = min(ATTN_TILE, j1 - jt);
         stage_v(jt, n);
         // scores for (position k, head h), four heads at a time: PPW*4 partial
         // sums per lane, transposed so that lane pairs hold the totals
-        for (int h0 = 0; h0 < rep; h0 += 4) {
+#pragma unroll
+        for (int h0 = 0; h0 < MAX_REP; h0 += 4) {
+            if (h0 >= rep) break;
             float v[PPW * 4];
 #pragma unroll
             for (int k = 0; k < PPW; ++k)
 #pragma unroll
                 for (int hh = 0; hh < 4; ++hh) {
                     float sacc = 0.f;
-                    if (h0 + hh < rep) {
 #pragma unroll
-                        for (int i = 0; i < DPL; ++i)
-                            sacc = fmaf(at.q[(h0 + hh) * HD + c.lane * DPL + i],
-                                        __uint_as_float((i & 1) ? (kraw[k][i >> 1] & 0xFFFF0000u) : (kraw[k][i >> 1] << 16)),
-                                        sacc);
-                    }
+                    for (int i = 0; i < DPL; ++i)
+                        sacc = fmaf(qr[h0 + hh][i],
+                                    __uint_as_float((i & 1) ? (kraw[k][i >> 1] & 0xFFFF0000u) : (kraw[k][i >> 1] << 16)),
+                                    sacc);
                     v[k * 4 + hh] = sacc;
                 }
             const float sc = transpose_reduce<PPW * 4>(v, c.lane);
@@ -1909,7 +1924,7 @@ static __device__ __forceinline__ bool attn_task(Ctx& c, const TaskRec& t, int t
             for (int o = 16; o; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, o));
             const float m_old = sh.m[h], m_new = fmaxf(m_old, mt);
             const float pa = c.lane < n ? expf(a - m_new) : 0.f;
-            if (c.lane < n) at.sc[h * ATTN_TILE + c.lane] = pa;
+            at.pt[c.lane * MAX_REP + h] = pa;
             const float ls = warp_sum(pa);
             if (c.lane == 0) {
                 const float al = expf(m_old - m_new);
@@ -1920,13 +1935,26 @@ static __device__ __forceinline__ bool attn_task(Ctx& c, const TaskRec& t, int t
         }
         bar_consumers();
 #pragma unroll
-        for (int e = 0; e < OPT; ++e) {
-            const int oe = c.tid + NT * e, h = oe / HD, dd = oe % HD;
+        for (int h = 0; h < MAX_REP; ++h) {
             if (h < rep) {
-                float a = acc[e] * sh.alpha[h];
-                const float* pr = at.sc + h * ATTN_TILE;
-                for (int jj = 0; jj < n; ++jj) a = fmaf(pr[jj], bf16_bits_to_f32(at.sv[jj * HD + dd]), a);
-                acc[e] = a;
+                const float al = sh.alpha[h];
+                acc[h][0] *= al;
+                acc[h][1] *= al;
+            }
+        }
+        for (int jj = ps; jj < n; jj += NPS) {
+            const uint32_t vv = *(const uint32_t*)(at.sv + jj * HD + 2 * dp);
+            const float v0 = bf16_bits_to_f32(vv & 0xFFFFu), v1 = bf16_bits_to_f32(vv >> 16);
+#pragma unroll
+            for (int h0 = 0; h0 < MAX_REP; h0 += 4) {
+                if (h0 >= rep) break;
+                const float4 pr = *(const float4*)(at.pt + jj * MAX_REP + h0);
+                const float pw[4] = {pr.x, pr.y, pr.z, pr.w};
+#pragma unroll
+                for (int hh = 0; hh < 4; ++hh) {
+                    acc[h0 + hh][0] = fmaf(pw[hh], v0, acc[h0 + hh][0]);
+                    acc[h0 + hh][1] = fmaf(pw[hh], v1, acc[h0 + hh][1]);
+                }
             }
         }
         bar_consumers();  // the next tile overwrites scores and V rows
@@ -1946,15 +1974,30 @@ static __device__ __forceinline__ bool attn_task(Ctx& c, const TaskRec& t, int t
         }
     }
     if (p.trace && c.tid == 0) c.sh->t_ph[1] = gtimer();
+    // The position subsets' sums, four heads at a time, through the V tile's
+    // region (free: every tile ended with a barrier).
+    float* red = reinterpret_cast<float*>(at.sv);  // [ps][head of the round][HD]
 #pragma unroll
-    for (int e = 0; e < OPT; ++e) {
-        const int oe = c.tid + NT * e, h = oe / HD, dd = oe % HD;
-        if (h < rep) {  // stored normalised (acc / l), so its range is that of v
-            const float lh = sh.l[h];
-            const uint16_t v = __half_as_ushort(__float2half_rn(lh > 0.f ? acc[e] / lh : 0.f));
+    for (int h0 = 0; h0 < MAX_REP; h0 += 4) {
+        if (h0 >= rep) break;
 #pragma unroll
-            for (int k = 0; k < PART_COPIES; ++k) p.part_acc[(((size_t)k * p.Hq + g * rep + h) * C + ch) * HD + dd] = v;
+        for (int hh = 0; hh < 4; ++hh)
+            *(float2*)(red + ((size_t)ps * 4 + hh) * HD + 2 * dp) = make_float2(acc[h0 + hh][0], acc[h0 + hh][1]);
+        bar_consumers();
+        for (int oe = c.tid; oe < 4 * HD; oe += NT) {
+            const int hh = oe / HD, dd = oe % HD, h = h0 + hh;
+            if (h < rep) {  // stored normalised (acc / l), so its range is that of v
+                float a = 0.f;
+#pragma unroll
+                for (int q = 0; q < NPS; ++q) a += red[((size_t)q * 4 + hh) * HD + dd];
+                const float lh = sh.l[h];
+                const uint16_t v = __half_as_ushort(__float2half_rn(lh > 0.f ? a / lh : 0.f));
+#pragma unroll
+                for (int k = 0; k < PART_COPIES; ++k)
+                    p.part_acc[(((size_t)k * p.Hq + g * rep + h) * C + ch) * HD + dd] = v;
+            }
         }
+        bar_consumers();  // the next round overwrites the sums
     }
     if (c.tid < rep) {
         const float2 mlv = make_float2(sh.m[c.tid], sh.l[c.tid]);
