@@ -38,3 +38,20 @@ def test_two_gloo_ranks_take_the_slowest_time():
     assert [o[1] for o in out] == [15.0, 15.0]
     # whole-job tokens/s: both replicas' tokens over the slowest replica's time
     assert out[0][2] == pytest.approx(2 * 768 / 0.015)
+
+
+def test_kernel_hash_follows_code_not_comments():
+    # bench.py reports the ncu traffic of profiles/ only while the kernel's code
+    # is the one that was captured: comment edits keep the hash, code edits change it.
+    sys.path.insert(0, ROOT)
+    import bench
+    src = {f: open(os.path.join(ROOT, f)).read() for f in bench.KERNEL_SOURCES}
+    h0 = bench.kernel_source_hash(lambda f: src[f])
+    assert h0 == bench.kernel_source_hash()
+    f = bench.KERNEL_SOURCES[0]
+    commented = dict(src)
+    commented[f] = "// a new comment line\n" + src[f].replace("\n", "  // trailing note\n", 1) + "\n/* block\n   comment */\n"
+    assert bench.kernel_source_hash(lambda g: commented[g]) == h0
+    changed = dict(src)
+    changed[f] = src[f] + "\nconstexpr int unused_probe = 1;\n"
+    assert bench.kernel_source_hash(lambda g: changed[g]) != h0
